@@ -1,0 +1,99 @@
+"""ctypes wrapper over the C oracle — test infrastructure only.
+
+Marshals CPU torch tensors to the C functions in pkv_oracle.c; it computes
+nothing itself. Tensors must be contiguous CPU tensors in the layouts of the C
+file's header: q [S][Hq][D], pools [NB][Hk][B][D], block_tables [S][M] int32,
+context_lens [S] int32, slot_mapping [N] int64, pairs [n][2] int64.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import build_oracle
+
+_CODES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = build_oracle.build()
+        L = ctypes.CDLL(path)
+        vp, i32, i64p, i32p = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p
+        L.oracle_decode.argtypes = [vp, i32, i32, i32, i32, i32, i32, vp, vp, i32, i32p, i32,
+                                    i32p, ctypes.c_double, vp]
+        L.oracle_decode.restype = i32
+        L.oracle_append.argtypes = [vp, vp, i64p, i32, vp, vp, i32, i32, i32, i32, i32]
+        L.oracle_append.restype = i32
+        L.oracle_block_copy.argtypes = [i64p, i32, vp, vp, i32, i32, i32, i32, i32]
+        L.oracle_block_copy.restype = i32
+        L.oracle_decode_elem.argtypes = [i32, ctypes.c_uint32]
+        L.oracle_decode_elem.restype = ctypes.c_double
+        L.oracle_num_threads.argtypes = []
+        L.oracle_num_threads.restype = i32
+        _lib = L
+    return _lib
+
+
+def _cpu(t: torch.Tensor) -> torch.Tensor:
+    assert t.device.type == "cpu", "the oracle takes CPU tensors"
+    return t.contiguous()
+
+
+def decode(q, k_pool, v_pool, block_tables, context_lens, scale: float,
+           seq_ids: Optional[Sequence[int]] = None) -> np.ndarray:
+    """fp64 attention output [S'][Hq][D] for the sequences `seq_ids` (all if None)."""
+    q, k_pool, v_pool = _cpu(q), _cpu(k_pool), _cpu(v_pool)
+    bt, cl = _cpu(block_tables).to(torch.int32), _cpu(context_lens).to(torch.int32)
+    if seq_ids is not None:
+        idx = torch.as_tensor(list(seq_ids), dtype=torch.long)
+        q, bt, cl = q[idx].contiguous(), bt[idx].contiguous(), cl[idx].contiguous()
+    assert q.dtype == k_pool.dtype == v_pool.dtype
+    S, Hq, D = q.shape
+    NB, Hk, B, D2 = k_pool.shape
+    assert D2 == D
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    rc = lib().oracle_decode(q.data_ptr(), _CODES[q.dtype], S, Hq, Hk, D, B,
+                             k_pool.data_ptr(), v_pool.data_ptr(), NB,
+                             bt.data_ptr(), bt.shape[1], cl.data_ptr(), float(scale),
+                             out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_decode failed with status {rc}")
+    return out
+
+
+def append(k_new, v_new, slot_mapping, k_pool, v_pool) -> None:
+    """In-place slot write of one K/V row per token into CPU pools."""
+    assert k_pool.is_contiguous() and v_pool.is_contiguous()
+    k_new, v_new = _cpu(k_new), _cpu(v_new)
+    sm = _cpu(slot_mapping).to(torch.int64)
+    NB, Hk, B, D = k_pool.shape
+    rc = lib().oracle_append(k_new.data_ptr(), v_new.data_ptr(), sm.data_ptr(), sm.numel(),
+                             k_pool.data_ptr(), v_pool.data_ptr(), _CODES[k_pool.dtype],
+                             NB, Hk, B, D)
+    if rc != 0:
+        raise ValueError(f"oracle_append failed with status {rc}")
+
+
+def block_copy(pairs, k_pool, v_pool) -> None:
+    """In-place whole-block copy (src -> dst) in CPU pools."""
+    assert k_pool.is_contiguous() and v_pool.is_contiguous()
+    p = _cpu(torch.as_tensor(pairs, dtype=torch.int64).reshape(-1, 2))
+    NB, Hk, B, D = k_pool.shape
+    rc = lib().oracle_block_copy(p.data_ptr(), p.shape[0], k_pool.data_ptr(), v_pool.data_ptr(),
+                                 _CODES[k_pool.dtype], NB, Hk, B, D)
+    if rc != 0:
+        raise ValueError(f"oracle_block_copy failed with status {rc}")
+
+
+def decode_elem(dtype: torch.dtype, bits: int) -> float:
+    return lib().oracle_decode_elem(_CODES[dtype], bits)
+
+
+def num_threads() -> int:
+    return lib().oracle_num_threads()

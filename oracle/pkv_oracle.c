@@ -1,0 +1,244 @@
+/*
+ * CPU oracle for paged KV-cache decode — TEST INFRASTRUCTURE ONLY.
+ *
+ * Only the tests, the package's smoke check and the benchmark's CPU-baseline
+ * leg load this library. The product path (libpkv) never calls it, links it
+ * or shares a line of code with it.
+ *
+ * It is the plain definition of what the paged decode step computes, written
+ * for a reader to check by eye, in fp64, with no blocking, fusion or
+ * reordering:
+ *
+ *   oracle_decode      For each sequence, walk its block table to assemble a
+ *                      contiguous K and V (per kv head), then run dense
+ *                      softmax attention for every query head.
+ *                      - Block table: logical block i holds tokens i*B ..
+ *                        i*B+B-1 and maps to a physical block of the pool
+ *                        ("PagedAttention — Math + Memory Model", section
+ *                        "PagedAttention: blocks and the block table";
+ *                        "KV-cache paging in vLLM", section "PagedAttention:
+ *                        Paging for KV-Caches").
+ *                      - The kernel gathers keys and values through the table
+ *                        for QK^T and the value-weighted sum (same page,
+ *                        section "PagedAttention: blocks and the block table";
+ *                        "KV-cache paging in vLLM", section "The Attention
+ *                        Kernel Change"). Paging changes where the bytes live,
+ *                        not the result, so this is dense attention on the
+ *                        gathered rows.
+ *                      - Grouped queries: q head h reads kv head h / (Hq/Hk)
+ *                        (the pages give only n_kv_heads in the per-token byte
+ *                        count, "PagedAttention — Math + Memory Model",
+ *                        section "The KV cache is big, and it grows"; the
+ *                        contiguous grouping is this library's reading).
+ *   oracle_append      Write each new token's K/V row into its slot,
+ *                      slot = physical_block * B + offset ("KV-Cache
+ *                      Optimization & PagedAttention for Long-Context Agents",
+ *                      section "Key KV-Cache Optimization Principles", item 1:
+ *                      blocks are filled as the model generates).
+ *   oracle_block_copy  Copy a whole physical block (K and V, all heads) to a
+ *                      fresh block ("PagedAttention — Math + Memory Model",
+ *                      section "Copy-on-write").
+ *
+ * Element decoding (fp16 / bf16 / fp32 -> double) follows the IEEE-754
+ * binary16 and bfloat16 bit layouts directly; it does not use any library
+ * conversion.
+ *
+ * Layouts: q [S][Hq][D]; pools [NB][Hk][B][D]; tables [S][M] int32;
+ * lens [S] int32; out [S][Hq][D] double. dtype codes: 0 f32, 1 f16, 2 bf16.
+ *
+ * Return codes: 0 ok, -1 invalid argument, -2 a block id or slot out of range.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_F32 0
+#define OR_F16 1
+#define OR_BF16 2
+
+static size_t elem_size(int dtype) {
+    return dtype == OR_F32 ? 4 : 2;
+}
+
+/* IEEE-754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double decode_f16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)f, -24);              /* subnormal: f * 2^(1-15-10) */
+    } else if (e == 31) {
+        v = f ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(f + 1024), e - 25);   /* (1.f) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of an IEEE-754 binary32. */
+static double decode_bf16(uint16_t h) {
+    uint32_t bits = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+}
+
+static double decode_f32(uint32_t bits) {
+    float f;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+}
+
+static double load_elem(const void *base, int dtype, size_t idx) {
+    if (dtype == OR_F32) {
+        uint32_t b;
+        memcpy(&b, (const char *)base + idx * 4, 4);
+        return decode_f32(b);
+    }
+    uint16_t h;
+    memcpy(&h, (const char *)base + idx * 2, 2);
+    return dtype == OR_F16 ? decode_f16(h) : decode_bf16(h);
+}
+
+/* Exposed so the tests can check the decoders against every bit pattern. */
+double oracle_decode_elem(int dtype, uint32_t bits) {
+    if (dtype == OR_F32) return decode_f32(bits);
+    if (dtype == OR_F16) return decode_f16((uint16_t)bits);
+    return decode_bf16((uint16_t)bits);
+}
+
+/* Attention for one (sequence, kv head): assemble contiguous K/V rows by
+ * walking the block table, then dense softmax attention for each q head of
+ * the group. */
+static int decode_one(const void *q, int dtype, int Hq, int Hk, int B, int D,
+                      const void *k_pool, const void *v_pool, int NB,
+                      const int32_t *table_row, int M, int L, double scale,
+                      int s, int g, double *out) {
+    int G = Hq / Hk;
+    if (L == 0) {
+        for (int j = 0; j < G; ++j)
+            for (int d = 0; d < D; ++d)
+                out[((size_t)s * Hq + g * G + j) * D + d] = 0.0;
+        return 0;
+    }
+    if (L < 0 || (L + B - 1) / B > M) return -1;
+
+    double *Kc = (double *)malloc(sizeof(double) * (size_t)L * D);
+    double *Vc = (double *)malloc(sizeof(double) * (size_t)L * D);
+    double *z = (double *)malloc(sizeof(double) * (size_t)L);
+    double *qh = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!Kc || !Vc || !z || !qh) { free(Kc); free(Vc); free(z); free(qh); return -1; }
+
+    /* gather: token t lives at offset t % B of physical block table[t / B] */
+    for (int t = 0; t < L; ++t) {
+        int32_t phys = table_row[t / B];
+        if (phys < 0 || phys >= NB) { free(Kc); free(Vc); free(z); free(qh); return -2; }
+        size_t row = (((size_t)phys * Hk + g) * B + (t % B)) * D;
+        for (int d = 0; d < D; ++d) {
+            Kc[(size_t)t * D + d] = load_elem(k_pool, dtype, row + d);
+            Vc[(size_t)t * D + d] = load_elem(v_pool, dtype, row + d);
+        }
+    }
+
+    for (int j = 0; j < G; ++j) {
+        int h = g * G + j;
+        size_t qrow = ((size_t)s * Hq + h) * D;
+        for (int d = 0; d < D; ++d) qh[d] = load_elem(q, dtype, qrow + d);
+        /* scores z_t = scale * <q_h, k_t> */
+        double m = -INFINITY;
+        for (int t = 0; t < L; ++t) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += qh[d] * Kc[(size_t)t * D + d];
+            z[t] = scale * acc;
+            if (z[t] > m) m = z[t];
+        }
+        /* softmax weights w_t = exp(z_t - m) / sum exp(z - m) */
+        double sum = 0.0;
+        for (int t = 0; t < L; ++t) {
+            z[t] = exp(z[t] - m);
+            sum += z[t];
+        }
+        /* out = sum_t w_t v_t */
+        for (int d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int t = 0; t < L; ++t) acc += z[t] * Vc[(size_t)t * D + d];
+            out[qrow + d] = acc / sum;
+        }
+    }
+    free(Kc);
+    free(Vc);
+    free(z);
+    free(qh);
+    return 0;
+}
+
+int oracle_decode(const void *q, int dtype, int S, int Hq, int Hk, int D, int B,
+                  const void *k_pool, const void *v_pool, int NB,
+                  const int32_t *block_tables, int M, const int32_t *context_lens,
+                  double scale, double *out) {
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return -1;
+    if (S < 0 || Hq <= 0 || Hk <= 0 || Hq % Hk != 0 || D <= 0 || B <= 0 || M <= 0) return -1;
+    if (dtype < 0 || dtype > 2) return -1;
+    int status = 0;
+    long units = (long)S * Hk;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long u = 0; u < units; ++u) {
+        int s = (int)(u / Hk), g = (int)(u % Hk);
+        int rc = decode_one(q, dtype, Hq, Hk, B, D, k_pool, v_pool, NB,
+                            block_tables + (size_t)s * M, M, context_lens[s], scale, s, g, out);
+        if (rc != 0) {
+#pragma omp critical
+            status = rc;
+        }
+    }
+    return status;
+}
+
+int oracle_append(const void *k_new, const void *v_new, const int64_t *slot_mapping, int N,
+                  void *k_pool, void *v_pool, int dtype, int NB, int Hk, int B, int D) {
+    if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool) return -1;
+    if (dtype < 0 || dtype > 2 || N < 0 || NB <= 0 || Hk <= 0 || B <= 0 || D <= 0) return -1;
+    size_t row_bytes = (size_t)D * elem_size(dtype);
+    for (int i = 0; i < N; ++i) {
+        int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;                 /* negative slot: no write */
+        int64_t blk = slot / B, off = slot % B;
+        if (blk >= NB) return -2;
+        for (int g = 0; g < Hk; ++g) {
+            size_t dst = ((size_t)(blk * Hk + g) * B + (size_t)off) * row_bytes;
+            size_t src = ((size_t)i * Hk + g) * row_bytes;
+            memcpy((char *)k_pool + dst, (const char *)k_new + src, row_bytes);
+            memcpy((char *)v_pool + dst, (const char *)v_new + src, row_bytes);
+        }
+    }
+    return 0;
+}
+
+int oracle_block_copy(const int64_t *pairs, int n, void *k_pool, void *v_pool,
+                      int dtype, int NB, int Hk, int B, int D) {
+    if (!pairs || !k_pool || !v_pool) return -1;
+    if (dtype < 0 || dtype > 2 || n < 0) return -1;
+    size_t blk_bytes = (size_t)Hk * B * D * elem_size(dtype);
+    for (int i = 0; i < n; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= NB || dst < 0 || dst >= NB) return -2;
+        memcpy((char *)k_pool + dst * blk_bytes, (const char *)k_pool + src * blk_bytes, blk_bytes);
+        memcpy((char *)v_pool + dst * blk_bytes, (const char *)v_pool + src * blk_bytes, blk_bytes);
+    }
+    return 0;
+}
+
+/* Number of threads OpenMP uses (1 when built without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
