@@ -1,0 +1,465 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one decode step of the Llama-3-8B-shaped workload (64 sequences,
+32 q / 8 kv heads, head_dim 128, bf16, block size 16, context lengths
+U[512, 4096], blocks drawn at random from a pool of 1.2x the need): append of
+one new token per sequence, then split-K paged decode attention with its
+log-sum-exp merge — every kernel of the path, through the C ABI.
+
+Prints one JSON line (rank 0). `value` is algorithmic KV-cache GB/s of the
+whole step (bytes the method must move: every context token's K and V row,
+q in and out, table entries, lengths, and the appended rows), measured on the
+device with inputs resident in HBM. L2 hygiene: the step cycles through
+three copies of the workload (3 x 0.73 GB, > L2), so each step reads its
+cache cold. `roofline` reports the split-K kernel alone against the measured
+HBM copy bandwidth. `e2e` is the same metric through the same public API with
+the step's inputs copied from pinned host memory and the result read back
+every step. `cpu_baseline` times the fp64 CPU oracle on a sample of the same
+workload.
+
+--impl reference runs the oracle (the only other implementation of this
+path) on the host cores as the reference arm.
+Multi-GPU (--gpus N under torchrun): independent replicas, one workload per
+rank, no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from paged_kv_cache_47_gb300 import workloads as W  # noqa: E402
+
+WORKLOAD_INDEX = 1
+METRIC = "paged decode attention KV GB/s and seq-tokens/s; fraction of GB300 HBM peak"
+UNIT = "GB/s"
+KERNEL_SOURCES = ["decode_kernel.cuh", "device_utils.cuh", "decomp.h", "pkv_internal.h"]
+PROFILE = os.path.join(ROOT, "profiles", "decode_split_kernel_llama3_8b.md")
+
+
+# ------------------------------------------------------------------ helpers
+def step_bytes(st, spec):
+    """Algorithmic bytes of one decode step (decode + append)."""
+    es = torch.tensor([], dtype=W.DTYPES[spec.dtype]).element_size()
+    lens = st.context_lens.long()
+    S = lens.numel()
+    kv = int(lens.sum()) * 2 * spec.num_kv_heads * spec.head_dim * es
+    qo = S * spec.num_q_heads * spec.head_dim * es * 2
+    tables = int(((lens + spec.block_size - 1) // spec.block_size).sum()) * 4
+    decode = kv + qo + tables + 4 * S
+    append = S * spec.num_kv_heads * spec.head_dim * es * 2 * 2 + 8 * S
+    return decode, append
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_47_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the split-K kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    if not os.path.exists(PROFILE):
+        return None
+    vals = {}
+    for line in open(PROFILE):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self, t0=None, t1=None):
+        """Summarise samples whose timestamp falls in [t0, t1] (host wall
+        clock, seconds since the epoch; all samples if not given)."""
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        import datetime
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                f_sm, f_mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            if t0 is not None and not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            sm.append(f_sm)
+            mx = f_mx
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle timing
+def host_inputs_from_generator(st, seed, device):
+    """The step's inputs, re-drawn from the seeded generator and copied to the
+    host, with the oracle's own append applied (post-append cache state)."""
+    from oracle import oracle
+
+    v = W.make_values(st, seed, device=device)
+    h = {k: t.cpu() for k, t in v.items()}
+    del v
+    oracle.append(h["k_new"], h["v_new"], st.slot_mapping, h["k_pool"], h["v_pool"])
+    return h
+
+
+def time_oracle(st, spec, h, target_s, seq_ids=None):
+    """Time oracle decode over the sequences `seq_ids` (all if None), repeated
+    until at least target_s of wall time; returns (GB/s, seq-tok/s, s, reps)."""
+    from oracle import oracle
+
+    ids = list(range(st.context_lens.numel())) if seq_ids is None else list(seq_ids)
+    lens = [int(st.context_lens[i]) for i in ids]
+    es = h["q"].element_size()
+    nbytes = (sum(lens) * 2 * spec.num_kv_heads * spec.head_dim * es
+              + len(ids) * spec.num_q_heads * spec.head_dim * es * 2
+              + sum((L + spec.block_size - 1) // spec.block_size for L in lens) * 4 + 4 * len(ids))
+    scale = 1.0 / math.sqrt(spec.head_dim)
+    spent, reps = 0.0, 0
+    while spent < target_s or reps == 0:
+        t0 = time.perf_counter()
+        oracle.decode(h["q"], h["k_pool"], h["v_pool"], st.block_tables, st.context_lens, scale,
+                      seq_ids=ids)
+        spent += time.perf_counter() - t0
+        reps += 1
+    return nbytes * reps / spent / 1e9, sum(lens) * reps / spent, spent, reps
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import build_oracle, oracle
+    build_oracle.build()
+    spec = W.SPECS[WORKLOAD_INDEX]
+    st = W.make_structure(spec, args.seed)
+    # bounded sample: the first `ref_seqs` sequences of the workload, values
+    # drawn on the host (no GPU involved in this arm)
+    n = min(args.ref_seqs, st.context_lens.numel())
+    lens = st.context_lens[:n].tolist()
+    sub = W.WorkloadSpec("sample", n, spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                         spec.block_size, spec.dtype, spec.std)
+    sst, v = W.make_workload(sub, seed=args.seed, lengths=lens)
+    oracle.append(v["k_new"], v["v_new"], sst.slot_mapping, v["k_pool"], v["v_pool"])
+    for _ in range(args.warmup):
+        time_oracle(sst, sub, v, 0.0)
+    rates, toks, secs = [], [], []
+    for _ in range(args.steps):
+        r, tps, sec, reps = time_oracle(sst, sub, v, 0.0)
+        rates.append(r)
+        toks.append(tps)
+        secs.append(sec / reps)
+    value = statistics.median(rates)
+    sample = f"{n} of {st.context_lens.numel()} sequences ({sum(lens)} context tokens) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * statistics.median(secs), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(spec, st),
+        "seq_tokens_per_s": round(statistics.median(toks), 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(spec, st):
+    return {"workload": "llama3_8b_decode_step", "num_seqs": spec.num_seqs,
+            "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
+            "head_dim": spec.head_dim, "block_size": spec.block_size, "kv_dtype": spec.dtype,
+            "context_lens": f"U[{spec.len_lo},{spec.len_hi}] seed 0, sum {int(st.context_lens.sum())}",
+            "pool_blocks": st.num_blocks, "step": "pkv_append + pkv_decode_attention (split-K + merge)"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    from paged_kv_cache_47_gb300 import binding, build
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        build.build()
+    barrier(world)
+    binding.lib()
+
+    spec = W.SPECS[WORKLOAD_INDEX]
+    st = W.make_structure(spec, args.seed)
+    scale = 1.0 / math.sqrt(spec.head_dim)
+    vals = W.make_values(st, args.seed, device=dev)
+    tables = st.block_tables.to(dev)
+    lens = st.context_lens.to(dev)
+    slots = st.slot_mapping.to(dev)
+    S, Hq, D = vals["q"].shape
+    # three resident copies of the cache so every step reads a cold L2
+    copies = []
+    for c in range(args.copies):
+        kp = vals["k_pool"] if c == 0 else vals["k_pool"].clone()
+        vp = vals["v_pool"] if c == 0 else vals["v_pool"].clone()
+        out = torch.empty(S, Hq, D, dtype=vals["q"].dtype, device=dev)
+        ws = binding.alloc_workspace(kp, Hq)
+        copies.append((kp, vp, out, ws))
+    decode_bytes, append_bytes = step_bytes(st, spec)
+    total_bytes = decode_bytes + append_bytes
+    stream = torch.cuda.current_stream()
+
+    def step(i, evs=None):
+        kp, vp, out, ws = copies[i % len(copies)]
+        binding.append(vals["k_new"], vals["v_new"], slots, kp, vp, stream=stream)
+        binding.decode_attention(vals["q"], kp, vp, tables, lens, scale, out=out, workspace=ws,
+                                 timing_events=evs, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if binding.get_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # per-kernel events on a strided subset of the timed steps
+    stride = max(1, args.steps // 200)
+    kev = {}
+    for i in range(0, args.steps, stride):
+        trio = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        for e in trio:
+            e.record(stream)            # materialise the CUDA event handle
+        kev[i] = trio
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.15)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    epoch0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, kev.get(i))
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clocks = sampler.stop(epoch0, epoch0 + wall)
+
+    ms = t_start.elapsed_time(t_end)
+    ms_max = reduce_max(ms, world, dev)
+    split_ms = [kev[i][0].elapsed_time(kev[i][1]) for i in kev]
+    merge_ms = [kev[i][1].elapsed_time(kev[i][2]) for i in kev]
+    split_avg = sum(split_ms) / len(split_ms)
+    merge_avg = sum(merge_ms) / len(merge_ms)
+    if binding.get_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    per_step_s = ms_max / 1000.0 / args.steps
+    value = world * total_bytes / per_step_s / 1e9
+    seq_tok = world * int(st.context_lens.sum()) / per_step_s
+    peak, peak_kind = peaks()
+
+    # ------------- end to end: host inputs in, result out, every step
+    e2e = run_e2e(args, st, spec, vals, copies, tables, lens, slots, scale, stream, dev,
+                  total_bytes, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "data": "synthetic (seeded N(0,1) values, random block tables)",
+        "config": {**workload_config(spec, st),
+                   "l2": f"inputs > L2: the step cycles through {len(copies)} resident copies "
+                         f"of the cache ({len(copies)} x {2 * st.num_blocks * spec.num_kv_heads * spec.block_size * spec.head_dim * 2 / 1e9:.2f} GB)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "seq_tokens_per_s": round(seq_tok, 1),
+        "hbm_frac_of_measured": round(value / peak / world, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel",
+                     "achieved": round(decode_bytes / (split_avg / 1000.0) / 1e9, 2),
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(decode_bytes / (split_avg / 1000.0) / 1e9 / peak, 4),
+                     "traffic": profiled_traffic(),
+                     "algorithmic_bytes_per_launch": decode_bytes,
+                     "avg_launch_ms": round(split_avg, 5), "merge_avg_ms": round(merge_avg, 5),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import oracle
+        h = host_inputs_from_generator(st, args.seed, dev)
+        r, tps, sec, reps = time_oracle(st, spec, h, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(r, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                                "kind": "oracle", "seq_tokens_per_s": round(tps, 1),
+                                "sample": f"the whole workload ({S} sequences, "
+                                          f"{int(st.context_lens.sum())} context tokens) x {reps} "
+                                          f"repetitions, {sec:.1f} s of fp64 oracle decode"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, st, spec, vals, copies, tables, lens, slots, scale, stream, dev, total_bytes,
+            world):
+    from paged_kv_cache_47_gb300 import binding
+
+    pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
+    h_q, h_kn, h_vn = pin(vals["q"]), pin(vals["k_new"]), pin(vals["v_new"])
+    h_tab, h_len, h_slot = pin(st.block_tables), pin(st.context_lens), pin(st.slot_mapping)
+    d_q, d_kn, d_vn = torch.empty_like(vals["q"]), torch.empty_like(vals["k_new"]), torch.empty_like(vals["v_new"])
+    d_tab, d_len, d_slot = torch.empty_like(tables), torch.empty_like(lens), torch.empty_like(slots)
+    h_out = torch.empty(vals["q"].shape, dtype=vals["q"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_tab, h_len, h_slot))
+    d2h = h_out.numel() * h_out.element_size()
+    steps = min(args.steps, args.e2e_steps)
+
+    def one(i):
+        kp, vp, out, ws = copies[i % len(copies)]
+        for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_tab, h_tab), (d_len, h_len),
+                     (d_slot, h_slot)):
+            d.copy_(h, non_blocking=True)
+        binding.append(d_kn, d_vn, d_slot, kp, vp, stream=stream)
+        binding.decode_attention(d_q, kp, vp, d_tab, d_len, scale, out=out, workspace=ws,
+                                 stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()            # the step's result is on the host
+
+    for i in range(3):
+        one(i)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one(i)
+    dt = time.perf_counter() - t0
+    dt = reduce_max(dt, world, dev)
+    return {"value": round(world * total_bytes * steps / dt / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(1000 * dt / steps, 4)}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seqs", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

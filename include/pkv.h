@@ -1,0 +1,211 @@
+/*
+ * libpkv — paged KV-cache decode for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of the hot path: writing each new token's K/V into its slot of a
+ * paged pool, decode attention that gathers K/V through per-sequence block
+ * tables, and the whole-block copy behind copy-on-write.
+ *
+ * Data model ("PagedAttention — Math + Memory Model", section "PagedAttention:
+ * blocks and the block table"; "KV-cache paging in vLLM", section
+ * "PagedAttention: Paging for KV-Caches"): the KV cache is cut into physical
+ * blocks of B tokens held in one device pool; a per-sequence block table maps
+ * logical block i (tokens i*B .. i*B+B-1) to a physical block id.
+ *
+ * Layouts (row-major, contiguous, device memory unless stated otherwise):
+ *   k_pool, v_pool   [num_blocks][num_kv_heads][block_size][head_dim]   dtype
+ *                    One (block, kv head) chunk is block_size*head_dim
+ *                    contiguous elements.
+ *   q, out           [num_seqs][num_q_heads][head_dim]
+ *   k_new, v_new     [num_tokens][num_kv_heads][head_dim]                dtype
+ *   block_tables     [num_seqs][max_blocks_per_seq] int32
+ *   context_lens     [num_seqs] int32 (tokens, including the one appended
+ *                    this step)
+ *   slot_mapping     [num_tokens] int64, slot = block_id*block_size + offset
+ *
+ * Grouped queries: q head h attends with kv head h / (num_q_heads /
+ * num_kv_heads).
+ *
+ * Ownership: every pointer belongs to the caller. Calls that take a `stream`
+ * (a cudaStream_t passed as void*, NULL = the legacy default stream) only
+ * enqueue work: they return before the GPU runs it, and the caller keeps the
+ * buffers alive until the stream has passed that point. The library allocates
+ * no device memory on these paths; decode attention uses a caller-provided
+ * workspace.
+ *
+ * Errors: each call returns a pkv_status. Arguments the host can check (null
+ * pointers, sizes, alignment, unsupported shapes) are rejected before any
+ * launch, with nothing enqueued. Values that live on the device (block ids,
+ * slots, context lengths) are checked by the kernels: a bad value sets a bit
+ * in a per-device error word and the access is skipped or clamped, never
+ * faulting; pkv_get_error reads and clears that word. pkv_last_error_message
+ * gives the text of the last failure on the calling thread.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_F32 = 0,
+    PKV_F16 = 1,
+    PKV_BF16 = 2
+} pkv_dtype;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,   /* null pointer, bad size, misalignment       */
+    PKV_ERR_UNSUPPORTED = -2,   /* dtype, head_dim, block_size or shape        */
+    PKV_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed        */
+    PKV_ERR_OUT_OF_RANGE = -4,  /* the device error word was non-zero          */
+    PKV_ERR_TIMEOUT = -5,       /* a bounded on-chip wait gave up              */
+    PKV_ERR_WORKSPACE = -6      /* workspace missing or too small              */
+} pkv_status;
+
+/* Bits of the device error word (see pkv_get_error). */
+#define PKV_DEVERR_BLOCK_ID   0x1u  /* a block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_CONTEXT    0x2u  /* a context length < 0 or > max_blocks*block_size */
+#define PKV_DEVERR_TIMEOUT    0x4u  /* an on-chip barrier wait ran out of time */
+#define PKV_DEVERR_SLOT       0x8u  /* an append slot outside the pool */
+
+/* Shape of one paged K/V pool pair. */
+typedef struct {
+    int32_t num_blocks;    /* physical blocks in each pool, >= 1               */
+    int32_t block_size;    /* tokens per block B: 8, 16 or 32                  */
+    int32_t num_kv_heads;  /* Hk >= 1                                          */
+    int32_t head_dim;      /* D: 64 or 128                                     */
+    int32_t dtype;         /* pkv_dtype of the pools, q, k_new and v_new       */
+} pkv_cache_desc;
+
+/*
+ * pkv_append — write one K row and one V row per (token, kv head) into its slot.
+ *
+ * Passage: blocks are filled as the model generates tokens ("KV-Cache
+ * Optimization & PagedAttention for Long-Context Agents", section "Key
+ * KV-Cache Optimization Principles", item 1; "PagedAttention — Math + Memory
+ * Model", section "PagedAttention: blocks and the block table": a sequence
+ * that needs slot B+1 gets a new block appended to its table — the block is
+ * allocated by the caller; this call only writes the slot).
+ *
+ * For token i with s = slot_mapping[i] >= 0, for every kv head g:
+ *   k_pool[s / B][g][s % B][:] = k_new[i][g][:]   (same for v)
+ * Tokens with s < 0 are skipped. Byte-exact copy. Slots are unique per call
+ * (duplicates: one of the writers wins, which one is unspecified). A slot past
+ * the pool sets PKV_DEVERR_SLOT and is skipped.
+ * Pointers: k_new, v_new, slot_mapping, k_pool, v_pool on the device, 16-byte
+ * aligned. num_tokens == 0 is a no-op.
+ */
+pkv_status pkv_append(const pkv_cache_desc *cache, const void *k_new, const void *v_new,
+                      const int64_t *slot_mapping, int32_t num_tokens,
+                      void *k_pool, void *v_pool, void *stream);
+
+/*
+ * pkv_decode_workspace_bytes — bytes of workspace pkv_decode_attention needs.
+ *
+ * The split-K partials are bounded by the number of CTAs of one launch on the
+ * current device, not by the batch or the context length: num_seqs and
+ * max_context_len are accepted for a stable signature and do not change the
+ * result. Returns 0 if the arguments are invalid or no device is present.
+ */
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc *cache, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_context_len);
+
+/*
+ * pkv_decode_attention — one decode step of paged attention, split-K over the
+ * context with a log-sum-exp merge.
+ *
+ * Passage: the attention kernel reads the block table and gathers keys and
+ * values from the scattered physical blocks for QK^T and the value-weighted
+ * sum ("PagedAttention — Math + Memory Model", section "PagedAttention: blocks
+ * and the block table"; "KV-cache paging in vLLM", section "The Attention
+ * Kernel Change").
+ *
+ * For sequence s with L = context_lens[s] and q head h (kv head g = h / G,
+ * G = num_q_heads / num_kv_heads):
+ *   z_t = scale * <q[s][h], K_t>,  t < L, K_t = k_pool[tab[s][t/B]][g][t%B]
+ *   out[s][h] = sum_t softmax(z)_t * V_t
+ * computed with fp32 accumulation and written in out_dtype (round to nearest
+ * even). L == 0 writes zeros. Pool rows past L in a last block are never used.
+ *
+ * q, k_pool, v_pool: 16-byte aligned device pointers (dtype cache->dtype).
+ * out: device, out_dtype any pkv_dtype. block_tables has max_blocks_per_seq
+ * columns; every L must satisfy L <= max_blocks_per_seq * block_size (a larger
+ * value is clamped and sets PKV_DEVERR_CONTEXT). Block ids outside the pool
+ * set PKV_DEVERR_BLOCK_ID and read as zeros.
+ * workspace: device memory of at least pkv_decode_workspace_bytes(...) bytes,
+ * 16-byte aligned, owned by the caller, reused by every call on `stream`
+ * (two streams need two workspaces). Its contents need no initialisation.
+ * num_q_heads must be a multiple of num_kv_heads. num_seqs == 0 is a no-op.
+ */
+pkv_status pkv_decode_attention(const pkv_cache_desc *cache, const void *q, int32_t num_seqs,
+                                int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                                const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                const int32_t *context_lens, float scale, void *out,
+                                int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/* Tuning and measurement options for pkv_decode_attention_ex. Zero-initialise
+ * for the defaults. */
+typedef struct {
+    int32_t num_ctas;        /* CTAs of the split-K launch; 0 = SMs x occupancy */
+    int32_t consumer;        /* 0 auto; 1 CUDA-core (SIMT) math; 2 tensor-core
+                                mma (16-bit dtypes only)                        */
+    void *timing_events[3];  /* optional cudaEvent_t recorded on `stream` before
+                                the split-K kernel, between it and the merge,
+                                and after the merge (NULL = not recorded)       */
+} pkv_decode_options;
+
+/* Workspace bytes for pkv_decode_attention_ex with options->num_ctas = num_ctas
+ * (0 = the default launch). */
+size_t pkv_decode_workspace_bytes_ex(const pkv_cache_desc *cache, int32_t num_q_heads,
+                                     int32_t num_ctas);
+
+/* pkv_decode_attention with options (NULL = defaults). Same contract. */
+pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, int32_t num_seqs,
+                                   int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, float scale, void *out,
+                                   int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                   void *stream, const pkv_decode_options *options);
+
+/*
+ * pkv_block_copy — copy whole physical blocks, K and V, all kv heads.
+ *
+ * Passage: copy-on-write copies the one block a writer hits while others
+ * still share it ("PagedAttention — Math + Memory Model", section
+ * "Copy-on-write"; the refcount decision and the table update are the
+ * caller's).
+ *
+ * For each pair i: pool[dst_i][:][:][:] = pool[src_i][:][:][:] for both pools.
+ * src_dst_pairs is HOST memory, [num_pairs][2] int64 (src, dst); the library
+ * reads it during the call and passes the ids to the kernel by value, so the
+ * caller may reuse it on return. Rejected with PKV_ERR_INVALID_ARG (nothing
+ * enqueued): an id outside [0, num_blocks), two pairs with the same dst, or a
+ * dst that is also some pair's src. Byte-exact. num_pairs == 0 is a no-op.
+ */
+pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pairs,
+                          int32_t num_pairs, void *k_pool, void *v_pool, void *stream);
+
+/*
+ * pkv_get_error — synchronise `stream`, then read and clear the device error
+ * word of the current device (PKV_DEVERR_* bits) into *device_error_word.
+ * Returns PKV_OK when the word was zero, PKV_ERR_OUT_OF_RANGE or
+ * PKV_ERR_TIMEOUT (when that bit is set) otherwise.
+ */
+pkv_status pkv_get_error(int32_t *device_error_word, void *stream);
+
+/* Static text for a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* Text of the last non-OK status returned on the calling thread ("" if none). */
+const char *pkv_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,178 @@
+"""Python binding over libpkv's C ABI (include/pkv.h).
+
+Argument marshalling only: every step of the hot path runs in libpkv's CUDA
+kernels. There is no CPU fallback; if the library is missing or a call fails,
+these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
+DTYPE_CODE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+CODE_DTYPE = {v: k for k, v in DTYPE_CODE.items()}
+
+STATUS = {0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED", -3: "PKV_ERR_CUDA",
+          -4: "PKV_ERR_OUT_OF_RANGE", -5: "PKV_ERR_TIMEOUT", -6: "PKV_ERR_WORKSPACE"}
+DEVERR_BLOCK_ID, DEVERR_CONTEXT, DEVERR_TIMEOUT, DEVERR_SLOT = 0x1, 0x2, 0x4, 0x8
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+class DecodeOptions(ctypes.Structure):
+    _fields_ = [("num_ctas", ctypes.c_int32), ("consumer", ctypes.c_int32),
+                ("timing_events", ctypes.c_void_p * 3)]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libpkv (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libpkv is not built ({path}); run paged_kv_cache_47_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        dp = ctypes.POINTER(CacheDesc)
+        L.pkv_append.argtypes = [dp, vp, vp, vp, i32, vp, vp, vp]
+        L.pkv_append.restype = i32
+        L.pkv_decode_workspace_bytes.argtypes = [dp, i32, i32, i32]
+        L.pkv_decode_workspace_bytes.restype = sz
+        L.pkv_decode_workspace_bytes_ex.argtypes = [dp, i32, i32]
+        L.pkv_decode_workspace_bytes_ex.restype = sz
+        dec = [dp, vp, i32, i32, vp, vp, vp, i32, vp, ctypes.c_float, vp, i32, vp, sz, vp]
+        L.pkv_decode_attention.argtypes = dec
+        L.pkv_decode_attention.restype = i32
+        L.pkv_decode_attention_ex.argtypes = dec + [ctypes.POINTER(DecodeOptions)]
+        L.pkv_decode_attention_ex.restype = i32
+        L.pkv_block_copy.argtypes = [dp, vp, i32, vp, vp, vp]
+        L.pkv_block_copy.restype = i32
+        L.pkv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
+        L.pkv_get_error.restype = i32
+        L.pkv_status_string.argtypes = [i32]
+        L.pkv_status_string.restype = ctypes.c_char_p
+        L.pkv_last_error_message.argtypes = []
+        L.pkv_last_error_message.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise PkvError(status, lib().pkv_last_error_message().decode())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def cache_desc(k_pool: torch.Tensor) -> CacheDesc:
+    """Descriptor of a pool tensor [NB][Hk][B][D]."""
+    NB, Hk, B, D = k_pool.shape
+    return CacheDesc(NB, B, Hk, D, DTYPE_CODE[k_pool.dtype])
+
+
+def _pools(k_pool, v_pool):
+    if k_pool.shape != v_pool.shape or k_pool.dtype != v_pool.dtype:
+        raise ValueError("k_pool and v_pool differ in shape or dtype")
+    if not (k_pool.is_contiguous() and v_pool.is_contiguous()):
+        raise ValueError("pools must be contiguous")
+    return cache_desc(k_pool)
+
+
+def append(k_new, v_new, slot_mapping, k_pool, v_pool, stream=None) -> None:
+    """Write k_new/v_new [N][Hk][D] into the pools at slot_mapping [N] (int64)."""
+    desc = _pools(k_pool, v_pool)
+    k_new, v_new = k_new.contiguous(), v_new.contiguous()
+    sm = slot_mapping.contiguous()
+    assert sm.dtype == torch.int64 and k_new.dtype == k_pool.dtype
+    _check(lib().pkv_append(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(sm), sm.numel(),
+                            _ptr(k_pool), _ptr(v_pool), _stream(stream)))
+
+
+def workspace_bytes(k_pool, num_q_heads: int, num_ctas: int = 0) -> int:
+    desc = cache_desc(k_pool)
+    return int(lib().pkv_decode_workspace_bytes_ex(ctypes.byref(desc), num_q_heads, num_ctas))
+
+
+def alloc_workspace(k_pool, num_q_heads: int, num_ctas: int = 0) -> torch.Tensor:
+    n = workspace_bytes(k_pool, num_q_heads, num_ctas)
+    if n == 0:
+        raise PkvError(-1, "workspace size query failed")
+    return torch.empty(n, dtype=torch.uint8, device=k_pool.device)
+
+
+def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                     out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
+                     workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                     consumer: int = 0, timing_events: Optional[Sequence] = None,
+                     stream=None) -> torch.Tensor:
+    """Paged decode attention: out[s][h] = softmax(scale q K^T) V over context_lens[s] tokens."""
+    desc = _pools(k_pool, v_pool)
+    S, Hq, D = q.shape
+    q = q.contiguous()
+    bt = block_tables.contiguous()
+    cl = context_lens.contiguous()
+    assert bt.dtype == torch.int32 and cl.dtype == torch.int32 and q.dtype == k_pool.dtype
+    if out is None:
+        out = torch.empty(S, Hq, D, dtype=out_dtype or q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(k_pool, Hq, num_ctas)
+    opts = DecodeOptions()
+    opts.num_ctas = num_ctas
+    opts.consumer = consumer
+    if timing_events is not None:
+        for i, ev in enumerate(timing_events):
+            opts.timing_events[i] = None if ev is None else ev.cuda_event
+    _check(lib().pkv_decode_attention_ex(
+        ctypes.byref(desc), _ptr(q), S, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(bt), bt.shape[1],
+        _ptr(cl), float(scale), _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream), ctypes.byref(opts)))
+    return out
+
+
+def block_copy(pairs, k_pool, v_pool, stream=None) -> None:
+    """Copy whole blocks src -> dst; pairs is host data [n][2] (list or CPU tensor)."""
+    desc = _pools(k_pool, v_pool)
+    p = torch.as_tensor(pairs, dtype=torch.int64).reshape(-1, 2).contiguous()
+    assert p.device.type == "cpu", "block-copy pairs are host memory"
+    _check(lib().pkv_block_copy(ctypes.byref(desc), _ptr(p), p.shape[0], _ptr(k_pool),
+                                _ptr(v_pool), _stream(stream)))
+
+
+def get_error(stream=None) -> int:
+    """Synchronise and read+clear the device error word (PKV_DEVERR_* bits)."""
+    w = ctypes.c_int32(0)
+    lib().pkv_get_error(ctypes.byref(w), _stream(stream))
+    return int(w.value)

@@ -1,0 +1,842 @@
+// Split-K paged decode attention for sm_103a.
+//
+// What it computes ("PagedAttention — Math + Memory Model", section
+// "PagedAttention: blocks and the block table"; "KV-cache paging in vLLM",
+// section "The Attention Kernel Change"): for every sequence and q head,
+// softmax(scale * q K^T) V over the sequence's context, where the K/V rows of
+// token t live at offset t % B of physical block block_tables[s][t / B].
+//
+// How (GB300 design):
+//  * Persistent, stream-K: one CTA per SM (x occupancy) takes an equal share
+//    of the flattened (sequence, kv-head unit, 64-token tile) space
+//    (decomp.h). Partial results of units cut by a CTA boundary are merged by
+//    log-sum-exp in decode_merge_kernel; whole units are written directly.
+//  * Warps 4-7 are producers: they walk the CTA's tiles, read block-table
+//    entries a few tiles ahead, and gather each (physical block, kv head)
+//    chunk with 16-byte cp.async copies into a ring of NST shared-memory
+//    stages, written in the 128-byte-swizzled order the math warps read
+//    without bank conflicts. Completion is tracked by mbarriers
+//    (cp.async.mbarrier.arrive). The copy engine (TMA) is not used for K/V:
+//    on GB300 it sustains only about six requests per microsecond per SM, so
+//    with the 2-8 KB chunks of a paged cache it reaches 2.2-5.5 TB/s, while
+//    16-byte loads reach 6.2-6.6 TB/s on the same random-chunk pattern.
+//    The unit's q rows ride along with its first tile.
+//  * Warps 0-3 are consumers: each takes 16 of the tile's 64 tokens and keeps
+//    its own online-softmax state (running max m, sum l, accumulator) in fp32
+//    registers, in base 2 with scale*log2(e) folded in. At the end of a
+//    segment the four warps combine their states through shared memory.
+//  * Math: with >= 3 q heads per kv head on 16-bit data the products run on
+//    tensor cores (mma.sync m16n8k16, tokens as M, q heads as N, fp32
+//    accumulate; P is split into hi+lo 16-bit parts so the PV product keeps
+//    fp32-level accuracy). Otherwise they run on CUDA cores with each lane
+//    owning a slice of head_dim (reduce-scatter for the dot products).
+//  * Every mbarrier wait is bounded (device_utils.cuh); there is no
+//    __syncthreads or named barrier after the producer/consumer split.
+#pragma once
+
+#include <math_constants.h>
+
+#include "decomp.h"
+#include "device_utils.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// compile-time shared-memory plan of one kernel variant
+// ---------------------------------------------------------------------------
+template <typename T, int D, int GMAX, bool MMA>
+struct SplitCfg {
+    static constexpr int ES = (int)sizeof(T);
+    static constexpr int ROWB = D * ES;              // bytes of one K or V row
+    static constexpr int NP = ROWB / 128;            // 128-byte swizzle planes per row
+    static constexpr int PLANE = PKV_TILE_TOKENS * 128;
+    static constexpr int KVB = NP * PLANE;           // bytes of one tile of K (or V)
+    static constexpr int QB = ((GMAX * ROWB + 1023) / 1024) * 1024;
+    static constexpr int STAGE = 2 * KVB + QB;       // multiple of 1024
+    static constexpr int NTN = GMAX / 8;             // mma n-tiles (MMA only)
+    static constexpr int COMB_O = kConsumerWarps * GMAX * D * 4;
+    static constexpr int COMB_ML = 2 * kConsumerWarps * GMAX * 4;
+    static constexpr int PBUF = MMA ? kConsumerWarps * NTN * 2 * 256 : 0;
+    static constexpr int SEQ_MAX = (2 * kMaxSeqsPerLaunch + 1) * 4;
+    static constexpr int SMEM_LIMIT = 227 * 1024;
+    static constexpr int PER_STAGE_EXTRA = (int)sizeof(TileMeta) + 16;  // meta + 2 barriers
+    static constexpr int FIXED = 1024 /*alignment slack*/ + COMB_O + COMB_ML + PBUF + 16 /*comb bars*/
+                                 + SEQ_MAX + 64;
+    static constexpr int NST_FIT = (SMEM_LIMIT - FIXED) / (STAGE + PER_STAGE_EXTRA);
+    static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
+    static_assert(NST >= 2, "shared-memory plan leaves fewer than two stages");
+    static_assert(ROWB % 128 == 0, "rows must be whole 128-byte planes");
+
+    // offsets from the 1024-aligned base
+    static constexpr int OFF_META = NST * STAGE;
+    static constexpr int OFF_FULL = OFF_META + NST * (int)sizeof(TileMeta);
+    static constexpr int OFF_EMPTY = OFF_FULL + NST * 8;
+    static constexpr int OFF_CBAR = OFF_EMPTY + NST * 8;   // comb_full, comb_empty
+    static constexpr int OFF_COMB_O = OFF_CBAR + 16;
+    static constexpr int OFF_COMB_M = OFF_COMB_O + COMB_O;
+    static constexpr int OFF_COMB_L = OFF_COMB_M + kConsumerWarps * GMAX * 4;
+    static constexpr int OFF_PBUF = OFF_COMB_L + kConsumerWarps * GMAX * 4;
+    static constexpr int OFF_SEQ = OFF_PBUF + PBUF;
+
+    static size_t smem_bytes(int S) { return 1024 + OFF_SEQ + (size_t)(2 * S + 1) * 4; }
+};
+
+// ---------------------------------------------------------------------------
+// per-sequence tile prefix, shared by the split-K and merge kernels
+// ---------------------------------------------------------------------------
+// seq_len[s]   = context length clamped to [0, M*B] (a clamp flags the error word)
+// seq_prefix[s]= U * sum_{s'<s} ceil(seq_len[s'] / 64), seq_prefix[S] = NT
+// Ends with __syncthreads(); all threads of the block must call it.
+__device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq_prefix,
+                                                 int *seq_len, bool report) {
+    const int tid = threadIdx.x;
+    const int max_len = p.M * p.B;
+    for (int s = tid; s < p.S; s += blockDim.x) {
+        int bad = 0;
+        int L = pkv_clamp_len(p.context_lens[s], max_len, &bad);
+        if (bad && report) atomicOr(p.err, PKV_DEVERR_CONTEXT);
+        seq_len[s] = L;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        const int lane = tid;
+        int running = 0;
+        for (int base = 0; base < p.S; base += 32) {
+            const int s = base + lane;
+            const int n = (s < p.S) ? pkv_tiles_of_len(seq_len[s]) * p.U : 0;
+            int incl = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (s < p.S) seq_prefix[s] = running + incl - n;
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) seq_prefix[p.S] = running;
+    }
+    __syncthreads();
+}
+
+// Position in the flattened tile space.
+struct Cursor {
+    int s, u, ti, n, L;
+};
+
+__device__ __forceinline__ void cursor_at(Cursor &c, int64_t tau, const int *seq_prefix,
+                                          const int *seq_len, int S) {
+    c.s = pkv_find_seq(seq_prefix, S, tau);
+    c.L = seq_len[c.s];
+    c.n = pkv_tiles_of_len(c.L);
+    const int off = (int)(tau - seq_prefix[c.s]);
+    c.u = off / c.n;
+    c.ti = off - c.u * c.n;
+}
+
+__device__ __forceinline__ void cursor_next(Cursor &c, const int *seq_len, int S, int U) {
+    if (++c.ti < c.n) return;
+    c.ti = 0;
+    if (++c.u < U) return;
+    c.u = 0;
+    do {
+        ++c.s;
+    } while (c.s < S && seq_len[c.s] == 0);
+    if (c.s < S) {
+        c.L = seq_len[c.s];
+        c.n = pkv_tiles_of_len(c.L);
+    }
+}
+
+// Swizzled shared-memory address of 16-byte chunk `chunk` (0..8*NP-1) of row r
+// in a tile stored as NP planes of [64 rows][128 bytes] with a 128-byte
+// XOR swizzle (chunk index XOR row%8 within each 1024-byte atom).
+__device__ __forceinline__ uint32_t swz(uint32_t base, int r, int chunk) {
+    const int pl = chunk >> 3, c = chunk & 7;
+    return base + pl * (PKV_TILE_TOKENS * 128) + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// small vector loads from shared memory
+// ---------------------------------------------------------------------------
+template <typename T, int N>
+__device__ __forceinline__ void lds_vec(uint32_t addr, float (&out)[N]) {
+    if constexpr (sizeof(T) == 4) {
+        if constexpr (N == 4) {
+            float4 v;
+            asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                         : "r"(addr));
+            out[0] = v.x; out[1] = v.y; out[2] = v.z; out[3] = v.w;
+        } else {
+            static_assert(N == 2, "");
+            float2 v;
+            asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+            out[0] = v.x; out[1] = v.y;
+        }
+    } else {
+        uint32_t w[N / 2];
+        if constexpr (N == 4) {
+            asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "r"(addr));
+        } else {
+            static_assert(N == 2, "");
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[0]) : "r"(addr));
+        }
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const T *h = reinterpret_cast<const T *>(&w[i]);
+            out[2 * i] = Elem<T>::to_f32(h[0]);
+            out[2 * i + 1] = Elem<T>::to_f32(h[1]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// consumer state
+// ---------------------------------------------------------------------------
+template <typename T, int D, int GMAX, bool MMA>
+struct Consumer;
+
+// CUDA-core math: lane owns EPL = D/32 consecutive elements of head_dim.
+template <typename T, int D, int GMAX>
+struct Consumer<T, D, GMAX, false> {
+    static constexpr int EPL = D / 32;
+    static constexpr int TB = GMAX <= 2 ? 16 : (GMAX == 4 ? 8 : (GMAX == 8 ? 4 : 2));
+    static constexpr int LOGTB = TB == 16 ? 4 : (TB == 8 ? 3 : (TB == 4 ? 2 : 1));
+    float qf[GMAX][EPL];
+    float m[GMAX], l[GMAX];
+    float acc[GMAX][EPL];
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            m[h] = -CUDART_INF_F;
+            l[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[h][e] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void load_q(const uint8_t *qslot, int gca, float scale_log2,
+                                           int lane) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const T *row = reinterpret_cast<const T *>(qslot + h * D * sizeof(T));
+                qf[h][e] = (h < gca) ? Elem<T>::to_f32(row[lane * EPL + e]) * scale_log2 : 0.f;
+            }
+        }
+    }
+
+    // lane's token within a batch after the reduce-scatter, and the inverse
+    static __device__ __forceinline__ int token_of_lane(int lane) {
+        int t = 0;
+#pragma unroll
+        for (int k = 0; k < LOGTB; ++k) t |= ((lane >> (4 - k)) & 1) << (LOGTB - 1 - k);
+        return t;
+    }
+    static __device__ __forceinline__ int lane_of_token(int t) {
+        int ln = 0;
+#pragma unroll
+        for (int k = 0; k < LOGTB; ++k) ln |= ((t >> (LOGTB - 1 - k)) & 1) << (4 - k);
+        return ln;
+    }
+
+    __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int ntok, int warp, int lane) {
+        const int chunk = (lane * EPL * (int)sizeof(T)) >> 4;
+        const int within = (lane * EPL * (int)sizeof(T)) & 15;
+        const int tl = token_of_lane(lane);
+#pragma unroll 1
+        for (int b0 = 0; b0 < 16; b0 += TB) {
+            const int rbase = 16 * warp + b0;
+            if (rbase >= ntok) break;
+            // partial dots of this lane's head_dim slice for TB tokens
+            float part[GMAX][TB];
+#pragma unroll
+            for (int t = 0; t < TB; ++t) {
+                float kf[EPL];
+                lds_vec<T, EPL>(swz(sK, rbase + t, chunk) + within, kf);
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) a = fmaf(qf[h][e], kf[e], a);
+                    part[h][t] = a;
+                }
+            }
+            // reduce-scatter over the warp: afterwards part[h][0] is the full
+            // dot product of token tl (held by 32/TB lanes)
+#pragma unroll
+            for (int k = 0; k < LOGTB; ++k) {
+                const int mask = 16 >> k;
+                const bool up = (lane & mask) != 0;
+                const int half = TB >> (k + 1);
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+#pragma unroll
+                    for (int i = 0; i < half; ++i) {
+                        const float send = up ? part[h][i] : part[h][i + half];
+                        const float keep = up ? part[h][i + half] : part[h][i];
+                        part[h][i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = LOGTB; k < 5; ++k) {
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h)
+                    part[h][0] += __shfl_xor_sync(0xffffffffu, part[h][0], 16 >> k);
+            }
+            const bool valid = rbase + tl < ntok;
+            float p[GMAX];
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) {
+                const float sc = valid ? part[h][0] : -CUDART_INF_F;
+                float mx = sc;
+#pragma unroll
+                for (int k = 0; k < 5; ++k) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16 >> k));
+                const float mn = fmaxf(m[h], mx);
+                const float alpha = exp2f(m[h] - mn);
+                p[h] = exp2f(sc - mn);
+                float ps = p[h];
+#pragma unroll
+                for (int k = 0; k < LOGTB; ++k) ps += __shfl_xor_sync(0xffffffffu, ps, 16 >> k);
+                l[h] = l[h] * alpha + ps;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[h][e] *= alpha;
+                m[h] = mn;
+            }
+            // P V
+#pragma unroll
+            for (int t = 0; t < TB; ++t) {
+                if (rbase + t < ntok) {
+                    float vf[EPL];
+                    lds_vec<T, EPL>(swz(sV, rbase + t, chunk) + within, vf);
+                    const int src = lane_of_token(t);
+#pragma unroll
+                    for (int h = 0; h < GMAX; ++h) {
+                        const float pt = __shfl_sync(0xffffffffu, p[h], src);
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) acc[h][e] = fmaf(pt, vf[e], acc[h][e]);
+                    }
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void write_comb(float *comb_o, float *comb_m, float *comb_l,
+                                               int warp, int lane) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            float *o = comb_o + (warp * GMAX + h) * D + lane * EPL;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] = acc[h][e];
+            if (lane == 0) {
+                comb_m[warp * GMAX + h] = m[h];
+                comb_l[warp * GMAX + h] = l[h];
+            }
+        }
+    }
+};
+
+// Tensor-core math: per warp, S^T[16 tokens x 8 heads] = K Q^T and
+// O^T[D x 8 heads] += V^T P^T with mma.sync m16n8k16 (fp32 accumulate).
+template <typename T, int D, int GMAX>
+struct Consumer<T, D, GMAX, true> {
+    static constexpr int NTN = GMAX / 8;
+    static constexpr int KS = D / 16;
+    uint32_t qb[NTN][KS][2];
+    float acc[KS][NTN][4];
+    float m[NTN][2], l[NTN][2];
+    uint32_t pbuf;  // this warp's P staging buffer (NTN x {hi, lo} x 256 B)
+    float scale_log2;
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                m[nt][hh] = -CUDART_INF_F;
+                l[nt][hh] = 0.f;
+            }
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[ks][nt][i] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void load_q(const uint8_t *qslot, int gca, float sl2, int lane) {
+        scale_log2 = sl2;
+        const int h_in = lane >> 2;        // n index (q head within the n-tile)
+        const int k_in = (lane & 3) * 2;   // k index pair
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            const int h = nt * 8 + h_in;
+            const uint32_t *row = reinterpret_cast<const uint32_t *>(qslot + h * D * sizeof(T));
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                qb[nt][ks][0] = (h < gca) ? row[(ks * 16 + k_in) >> 1] : 0u;
+                qb[nt][ks][1] = (h < gca) ? row[(ks * 16 + 8 + k_in) >> 1] : 0u;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int ntok, int warp, int lane) {
+        const int r0 = 16 * warp;
+        const int nval = ntok - r0;
+        if (nval <= 0) return;
+        // ---- S^T = K Q^T
+        float s[NTN][4];
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
+        {
+            const int row = r0 + (lane & 15);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int chunk = ks * 2 + (lane >> 4);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(swz(sK, row, chunk), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt)
+                    MmaOp<T>::run(s[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+            }
+        }
+        // ---- online softmax (tokens rA, rB; heads 8nt + 2*(lane%4) + hh)
+        const int rA = r0 + (lane >> 2), rB = rA + 8;
+        const bool vA = rA < ntok, vB = rB < ntok;
+        float p[NTN][4];
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float sa = vA ? s[nt][hh] * scale_log2 : -CUDART_INF_F;
+                const float sb = vB ? s[nt][2 + hh] * scale_log2 : -CUDART_INF_F;
+                float mx = fmaxf(sa, sb);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(m[nt][hh], mx);
+                const float alpha = exp2f(m[nt][hh] - mn);
+                m[nt][hh] = mn;
+                p[nt][hh] = exp2f(sa - mn);
+                p[nt][2 + hh] = exp2f(sb - mn);
+                l[nt][hh] = l[nt][hh] * alpha + p[nt][hh] + p[nt][2 + hh];
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    acc[ks][nt][hh] *= alpha;
+                    acc[ks][nt][2 + hh] *= alpha;
+                }
+            }
+        }
+        // ---- P^T as the B operand: stage [token][head] hi/lo pairs, reload transposed
+        __syncwarp();
+        uint32_t bh[NTN][2], bl[NTN][2];
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            const uint32_t hi = pbuf + nt * 512, lo = hi + 256;
+            float r00, r01, r10, r11;
+            const uint32_t hA = Elem<T>::pack2(p[nt][0], p[nt][1], r00, r01);
+            const uint32_t hB = Elem<T>::pack2(p[nt][2], p[nt][3], r10, r11);
+            float d0, d1;
+            const uint32_t lA = Elem<T>::pack2(p[nt][0] - r00, p[nt][1] - r01, d0, d1);
+            const uint32_t lB = Elem<T>::pack2(p[nt][2] - r10, p[nt][3] - r11, d0, d1);
+            const uint32_t offA = (lane >> 2) * 16 + (lane & 3) * 4;
+            const uint32_t offB = offA + 8 * 16;
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(hi + offA), "r"(hA) : "memory");
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(hi + offB), "r"(hB) : "memory");
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(lo + offA), "r"(lA) : "memory");
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(lo + offB), "r"(lB) : "memory");
+        }
+        __syncwarp();
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            const uint32_t hi = pbuf + nt * 512, lo = hi + 256;
+            ldsm_x2_t(hi + (lane & 15) * 16, bh[nt][0], bh[nt][1]);
+            ldsm_x2_t(lo + (lane & 15) * 16, bl[nt][0], bl[nt][1]);
+        }
+        // ---- O^T += V^T P^T
+        {
+            const int tok = r0 + (lane & 7) + ((lane >> 4) << 3);
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int chunk = mt * 2 + ((lane >> 3) & 1);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(swz(sV, tok, chunk), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt) {
+                    MmaOp<T>::run(acc[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                    MmaOp<T>::run(acc[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                }
+            }
+        }
+        __syncwarp();  // P buffer reads done before the next tile rewrites it
+    }
+
+    __device__ __forceinline__ void write_comb(float *comb_o, float *comb_m, float *comb_l,
+                                               int warp, int lane) {
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float lt = l[nt][hh];
+                lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+                lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+                lt += __shfl_xor_sync(0xffffffffu, lt, 16);
+                const int h = nt * 8 + (lane & 3) * 2 + hh;
+                if (lane < 4) {
+                    comb_m[warp * GMAX + h] = m[nt][hh];
+                    comb_l[warp * GMAX + h] = lt;
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const int h = nt * 8 + (lane & 3) * 2;
+                const int d = mt * 16 + (lane >> 2);
+                float *o = comb_o + (warp * GMAX + h) * D;
+                o[d] = acc[mt][nt][0];
+                o[D + d] = acc[mt][nt][1];
+                o[d + 8] = acc[mt][nt][2];
+                o[D + d + 8] = acc[mt][nt][3];
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// the split-K kernel
+// ---------------------------------------------------------------------------
+template <typename T, int D, int GMAX, bool MMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_split_kernel(const DecodeParams p) {
+    using Cfg = SplitCfg<T, D, GMAX, MMA>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    TileMeta *meta = reinterpret_cast<TileMeta *>(smem + Cfg::OFF_META);
+    const uint32_t full0 = sbase + Cfg::OFF_FULL;
+    const uint32_t empty0 = sbase + Cfg::OFF_EMPTY;
+    const uint32_t comb_full = sbase + Cfg::OFF_CBAR;
+    const uint32_t comb_empty = comb_full + 8;
+    float *comb_o = reinterpret_cast<float *>(smem + Cfg::OFF_COMB_O);
+    float *comb_m = reinterpret_cast<float *>(smem + Cfg::OFF_COMB_M);
+    float *comb_l = reinterpret_cast<float *>(smem + Cfg::OFF_COMB_L);
+    int *seq_prefix = reinterpret_cast<int *>(smem + Cfg::OFF_SEQ);
+    int *seq_len = seq_prefix + p.S + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cta = blockIdx.x, C = p.C;
+
+    if (tid == 0) {
+        for (int i = 0; i < Cfg::NST; ++i) {
+            mbar_init(full0 + 8 * i, kProducerThreads + 1);
+            mbar_init(empty0 + 8 * i, kConsumerWarps);
+        }
+        mbar_init(comb_full, kConsumerWarps);
+        mbar_init(comb_empty, kConsumerWarps);
+        fence_mbarrier_init();
+    }
+    // inputs may come from the previous kernel on the stream (launched with
+    // programmatic serialisation): wait for it before reading any of them
+    grid_dependency_wait();
+    build_seq_arrays(p, seq_prefix, seq_len, cta == 0);
+
+    // zero-length sequences: zeros, written by CTA s % C
+    for (int s = 0; s < p.S; ++s) {
+        if (seq_len[s] == 0 && s % C == cta) {
+            for (int i = tid; i < p.Hq * D; i += kThreads)
+                store_out(p.out, (size_t)s * p.Hq * D + i, p.out_dtype, 0.f);
+        }
+    }
+
+    const int64_t NT = seq_prefix[p.S];
+    const int64_t t_begin = NT ? pkv_split(cta, C, NT) : 0, t_end = NT ? pkv_split(cta + 1, C, NT) : 0;
+    const int n_my = (int)(t_end - t_begin);
+    // merge descriptor of boundary cta+1: set when this CTA's last segment is
+    // the start of a unit that continues into later CTAs (this CTA is the
+    // unit's first owner), else marked empty
+    if (tid == 0 && cta + 1 < C) {
+        MergeDesc md;
+        md.s = -1;
+        md.h0 = md.gca = md.slot_first = md.c_last = 0;
+        md.nt = (int)NT;
+        md.pad0 = md.pad1 = 0;
+        if (n_my > 0) {
+            Cursor c;
+            cursor_at(c, t_end - 1, seq_prefix, seq_len, p.S);
+            const int64_t T_u = (int64_t)seq_prefix[c.s] + (int64_t)c.u * c.n;
+            if (T_u >= t_begin && T_u + c.n > t_end) {
+                const int g = c.u / p.NC, chunk = c.u - (c.u / p.NC) * p.NC;
+                md.s = c.s;
+                md.h0 = g * p.G + chunk * p.GC;
+                md.gca = min(p.GC, p.G - chunk * p.GC);
+                md.slot_first = pkv_partial_slot(cta, C, NT, T_u);
+                md.c_last = pkv_owner(T_u + c.n - 1, C, NT);
+            }
+        }
+        p.ws_desc[cta + 1] = md;
+    }
+    grid_dependents_launch();   // the merge kernel may start its launch now
+    if (n_my <= 0) return;
+
+    if (warp >= kConsumerWarps) {
+        // ======================= producer warps =======================
+        // 128 threads gather each tile with 16-byte cp.async copies straight
+        // into the swizzled stage layout. Thread pt copies one physical block
+        // of the tile (tpb threads per block), so it needs one block-table
+        // entry per tile; entries are loaded LA tiles ahead into a register
+        // ring whose slots are fixed by unrolling the loop LA times. Rows past
+        // the context, blocks past the tile and out-of-pool block ids are
+        // zero-filled (src-size 0): no address outside the pool is formed
+        // and the math warps never see stale or garbage rows.
+        constexpr int LA = 8;
+        constexpr int CPR = Cfg::ROWB / 16;          // 16-byte chunks per row
+        const int pt = tid - kConsumerWarps * 32;     // 0 .. kProducerThreads-1
+        const int bpt = PKV_TILE_TOKENS / p.B;        // blocks per tile
+        const int tpb = kProducerThreads / bpt;       // producer threads per block
+        const int jblk = pt / tpb;
+        const int tb = pt - jblk * tpb;
+        const uint8_t *kpool = static_cast<const uint8_t *>(p.kp);
+        const uint8_t *vpool = static_cast<const uint8_t *>(p.vp);
+        Cursor cur, la;
+        cursor_at(cur, t_begin, seq_prefix, seq_len, p.S);
+        la = cur;
+        auto load_entry = [&](const Cursor &c) -> int {
+            const int ntok = min(PKV_TILE_TOKENS, c.L - c.ti * PKV_TILE_TOKENS);
+            if (jblk * p.B >= ntok) return -1;
+            return __ldg(p.block_tables + (size_t)c.s * p.M + c.ti * bpt + jblk);
+        };
+        int ent[LA];
+#pragma unroll
+        for (int k = 0; k < LA; ++k) {
+            ent[k] = -1;
+            if (k < n_my) {
+                ent[k] = load_entry(la);
+                cursor_next(la, seq_len, p.S, p.U);
+            }
+        }
+        bool ok = true;
+        for (int it0 = 0; it0 < n_my && ok; it0 += LA) {
+#pragma unroll
+            for (int k = 0; k < LA; ++k) {
+                const int it = it0 + k;
+                if (it >= n_my || !ok) break;
+                const int e = ent[k];
+                if (it + LA < n_my) {
+                    ent[k] = load_entry(la);
+                    cursor_next(la, seq_len, p.S, p.U);
+                }
+                const int stage = it % Cfg::NST;
+                const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
+                if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, p.err)) {
+                    ok = false;
+                    break;
+                }
+                const int ntok = min(PKV_TILE_TOKENS, cur.L - cur.ti * PKV_TILE_TOKENS);
+                const bool first = (it == 0) || (cur.ti == 0);
+                const int g = cur.u / p.NC;
+                const int chunk = cur.u - g * p.NC;
+                const int h0 = g * p.G + chunk * p.GC;
+                const int gca = min(p.GC, p.G - chunk * p.GC);
+                const uint32_t full = full0 + 8 * stage;
+                const uint32_t sK = sbase + stage * Cfg::STAGE;
+                const uint32_t sV = sK + Cfg::KVB;
+                const uint32_t sQ = sV + Cfg::KVB;
+                // ---- K and V rows of block jblk of this tile
+                const bool blk_ok = e >= 0 && e < p.NB;
+                if (tb == 0 && jblk * p.B < ntok && !blk_ok) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+                const size_t blk_base = blk_ok ? ((size_t)e * p.Hk + g) * p.B * Cfg::ROWB : 0;
+#pragma unroll
+                for (int c = 0; c < CPR / 2; ++c) {
+                    const int idx = tb + c * tpb;            // chunk within the block
+                    const int rb = idx / CPR, ch = idx - (idx / CPR) * CPR;
+                    const int row = jblk * p.B + rb;         // row of the tile
+                    const bool v = blk_ok && row < ntok;
+                    const size_t off = v ? blk_base + (size_t)rb * Cfg::ROWB + ch * 16 : 0;
+                    cp_async_16(swz(sK, row, ch), kpool + off, v);
+                    cp_async_16(swz(sV, row, ch), vpool + off, v);
+                }
+                // ---- q rows of the unit ride along with its first tile
+                if (first) {
+                    const uint8_t *qsrc = static_cast<const uint8_t *>(p.q) +
+                                          ((size_t)cur.s * p.Hq + h0) * Cfg::ROWB;
+                    for (int i = pt; i < gca * CPR; i += kProducerThreads)
+                        cp_async_16(sQ + i * 16, qsrc + (size_t)i * 16, true);
+                }
+                cp_async_arrive_noinc(full);
+                if (pt == 0) {
+                    const int64_t T_u = (int64_t)seq_prefix[cur.s] + (int64_t)cur.u * cur.n;
+                    const bool last = (it == n_my - 1) || (cur.ti == cur.n - 1);
+                    const bool whole = (T_u >= t_begin) && (T_u + cur.n <= t_end);
+                    TileMeta mt;
+                    mt.s = cur.s;
+                    mt.h0 = h0;
+                    mt.gca = gca;
+                    mt.ntok = ntok;
+                    mt.flags = (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0);
+                    mt.slot = T_u > t_begin ? 1 : 0;
+                    mt.pad0 = mt.pad1 = 0;
+                    meta[stage] = mt;
+                    mbar_arrive(full);   // release: the record is visible with the data
+                }
+                cursor_next(cur, seq_len, p.S, p.U);
+            }
+        }
+        cp_async_wait_all();   // this thread's copies land before it exits
+        return;
+    }
+
+    // ======================= consumer warps =======================
+    Consumer<T, D, GMAX, MMA> cs;
+    if constexpr (MMA) cs.pbuf = sbase + Cfg::OFF_PBUF + warp * Cfg::NTN * 512;
+    cs.reset();
+    int seg = 0;
+    for (int it = 0; it < n_my; ++it) {
+        const int stage = it % Cfg::NST;
+        const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
+        if (!mbar_wait(full0 + 8 * stage, ph, p.err)) return;
+        const TileMeta mt = meta[stage];
+        const uint32_t sK = sbase + stage * Cfg::STAGE;
+        const uint32_t sV = sK + Cfg::KVB;
+        if (mt.flags & kFirst) {
+            cs.reset();
+            cs.load_q(smem + stage * Cfg::STAGE + 2 * Cfg::KVB, mt.gca, p.scale_log2, lane);
+        }
+        cs.tile(sK, sV, mt.ntok, warp, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+
+        if (mt.flags & kLast) {
+            // combine the four warps' softmax states for this segment
+            if (!mbar_wait(comb_empty, ((uint32_t)seg & 1u) ^ 1u, p.err)) return;
+            cs.write_comb(comb_o, comb_m, comb_l, warp, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(comb_full);
+            if (!mbar_wait(comb_full, (uint32_t)seg & 1u, p.err)) return;
+            const int base = (cta * 2 + mt.slot) * p.GC;
+            for (int idx = warp * 32 + lane; idx < mt.gca * D; idx += kConsumerWarps * 32) {
+                const int j = idx / D, d = idx - (idx / D) * D;
+                float M = -CUDART_INF_F;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * GMAX + j]);
+                float Ls = 0.f, O = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float wt = exp2f(comb_m[w * GMAX + j] - M);
+                    Ls = fmaf(wt, comb_l[w * GMAX + j], Ls);
+                    O = fmaf(wt, comb_o[(w * GMAX + j) * D + d], O);
+                }
+                const float o = O / Ls;
+                if (mt.flags & kWhole) {
+                    store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype, o);
+                } else {
+                    p.ws_o[(size_t)(base + j) * D + d] = o;
+                    if (d == 0) p.ws_lse[base + j] = M + log2f(Ls);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(comb_empty);
+            ++seg;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// log-sum-exp merge of partials of units cut by CTA boundaries
+// ---------------------------------------------------------------------------
+// Block j (1 <= j < C) merges the unit described by descriptor j (written by
+// split-K CTA j-1 when that unit starts in its range and runs past it):
+//   lse = log2 sum_p 2^{lse_p},  out = sum_p 2^{lse_p - lse} o_p
+// over the partials of CTAs j-1 .. c_last; CTAs with an empty tile range
+// wrote nothing and are skipped.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
+    grid_dependency_wait();   // partials come from the split-K kernel just before
+    const int j = blockIdx.x + 1;
+    const MergeDesc md = p.ws_desc[j];
+    if (md.s < 0) return;
+    const int C = p.C;
+    const int64_t NT = md.nt;
+    const int c_first = j - 1;
+    for (int idx = threadIdx.x; idx < md.gca * D; idx += blockDim.x) {
+        const int jj = idx / D, d = idx - (idx / D) * D;
+        float M = -CUDART_INF_F;
+        for (int c = c_first; c <= md.c_last; ++c) {
+            if (pkv_cta_empty(c, C, NT)) continue;
+            const int slot = c == c_first ? md.slot_first : 0;
+            M = fmaxf(M, p.ws_lse[(c * 2 + slot) * p.GC + jj]);
+        }
+        float W = 0.f, O = 0.f;
+        for (int c = c_first; c <= md.c_last; ++c) {
+            if (pkv_cta_empty(c, C, NT)) continue;
+            const int slot = c == c_first ? md.slot_first : 0;
+            const int b = (c * 2 + slot) * p.GC + jj;
+            const float w = exp2f(p.ws_lse[b] - M);
+            W += w;
+            O = fmaf(w, p.ws_o[(size_t)b * D + d], O);
+        }
+        store_out(p.out, ((size_t)md.s * p.Hq + md.h0 + jj) * D + d, p.out_dtype, O / W);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host-side launch of one variant
+// ---------------------------------------------------------------------------
+template <typename T, int D, int GMAX, bool MMA>
+struct SplitVariant {
+    using Cfg = SplitCfg<T, D, GMAX, MMA>;
+
+    static cudaError_t prepare(int dev) {
+        static bool done[64] = {false};
+        if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+        if (!done[dev]) {
+            const size_t smem = Cfg::smem_bytes(kMaxSeqsPerLaunch);
+            cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, GMAX, MMA>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            if (e != cudaSuccess) return e;
+            done[dev] = true;
+        }
+        return cudaSuccess;
+    }
+
+    static cudaError_t launch(const DecodeParams &p, cudaStream_t st) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = prepare(dev);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)p.C);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = Cfg::smem_bytes(p.S);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA>, p);
+    }
+
+    static int max_ctas_per_sm() {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || prepare(dev) != cudaSuccess) return 0;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &n, decode_split_kernel<T, D, GMAX, MMA>, kThreads,
+                Cfg::smem_bytes(kMaxSeqsPerLaunch)) != cudaSuccess)
+            return 0;
+        return n;
+    }
+
+    static const DecodeVariant *get() {
+        static const DecodeVariant v{&launch, &max_ctas_per_sm};
+        return &v;
+    }
+};
+
+}  // namespace pkv

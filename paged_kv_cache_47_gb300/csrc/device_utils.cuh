@@ -1,0 +1,205 @@
+// Device helpers for the sm_103a kernels: mbarrier, cp.async, programmatic
+// dependent launch, ldmatrix, mma.sync and element conversions, as inline PTX.
+//
+// Every wait on an mbarrier is bounded in time: after PKV_WAIT_LIMIT_NS the
+// waiter sets PKV_DEVERR_TIMEOUT in the error word and returns false, so a
+// protocol mistake ends the kernel instead of hanging the GPU.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+#define PKV_WAIT_LIMIT_NS 2000000000ull  // 2 s: far above any legitimate wait
+
+namespace pkv {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// PKV_WAIT_LIMIT_NS. Returns false (and flags the error word) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > PKV_WAIT_LIMIT_NS) {
+            atomicOr(err, PKV_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the preceding kernel on the stream has completed and its memory
+// is visible (a no-op when this kernel was launched without programmatic
+// serialisation).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next kernel on the stream (if launched with programmatic
+// serialisation) to be scheduled before this grid finishes.
+__device__ __forceinline__ void grid_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- cp.async (LSU path)
+// 16-byte global -> shared copy that bypasses L1. When `valid` is false the
+// source is not read (src-size 0) and the 16 destination bytes are zeroed.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, bool valid) {
+    const uint32_t n = valid ? 16u : 0u;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n)
+                 : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- ldmatrix / mma
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(addr));
+}
+
+template <typename T>
+struct MmaOp;
+
+template <>
+struct MmaOp<__nv_bfloat16> {
+    static __device__ __forceinline__ void run(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+};
+
+template <>
+struct MmaOp<__half> {
+    static __device__ __forceinline__ void run(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+};
+
+// ---------------------------------------------------------------- conversions
+// Element type traits: widen to fp32, and pack two fp32 into a 32-bit pair
+// (lower index in the low half) with round-to-nearest-even.
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static __device__ __forceinline__ float to_f32(float x) { return x; }
+};
+
+template <>
+struct Elem<__half> {
+    static __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+    static __device__ __forceinline__ uint32_t pack2(float lo, float hi, float &lo_r, float &hi_r) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        float2 f = __half22float2(h);
+        lo_r = f.x;
+        hi_r = f.y;
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ uint32_t pack2(float lo, float hi, float &lo_r, float &hi_r) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        float2 f = __bfloat1622float2(h);
+        lo_r = f.x;
+        hi_r = f.y;
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+// Store one fp32 value as out_dtype (round to nearest even).
+__device__ __forceinline__ void store_out(void *out, size_t idx, int out_dtype, float v) {
+    if (out_dtype == PKV_F32) {
+        static_cast<float *>(out)[idx] = v;
+    } else if (out_dtype == PKV_F16) {
+        static_cast<__half *>(out)[idx] = __float2half_rn(v);
+    } else {
+        static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+    }
+}
+
+}  // namespace pkv

@@ -1,0 +1,356 @@
+// The C ABI of libpkv (include/pkv.h): argument checks, kernel dispatch and
+// the device error word.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <unordered_set>
+
+#include "../../include/pkv.h"
+#include "decomp.h"
+#include "pkv_internal.h"
+
+namespace {
+
+// ---------------------------------------------------------------- errors
+thread_local char g_msg[512] = "";
+
+pkv_status fail(pkv_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// One error word per device, in the library's own static device memory.
+__device__ unsigned int g_pkv_error_word;
+
+constexpr int kMaxDevices = 64;
+unsigned *g_err_ptr[kMaxDevices] = {nullptr};
+std::mutex g_err_mu;
+
+pkv_status device_error_ptr(unsigned **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lk(g_err_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_pkv_error_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        g_err_ptr[dev] = static_cast<unsigned *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------- checks
+int elem_bytes(int dtype) { return dtype == PKV_F32 ? 4 : 2; }
+bool valid_dtype(int dtype) { return dtype == PKV_F32 || dtype == PKV_F16 || dtype == PKV_BF16; }
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+pkv_status check_cache(const pkv_cache_desc *c) {
+    if (!c) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
+    if (!valid_dtype(c->dtype)) return fail(PKV_ERR_UNSUPPORTED, "dtype %d", c->dtype);
+    if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32)
+        return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", c->block_size);
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c->head_dim);
+    if (c->num_kv_heads < 1) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads %d", c->num_kv_heads);
+    if (c->num_blocks < 1) return fail(PKV_ERR_INVALID_ARG, "num_blocks %d", c->num_blocks);
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------- decode plan
+struct Plan {
+    int G, GC, NC, U;
+    bool mma;
+    int gmax;
+    const pkv::DecodeVariant *variant;
+};
+
+pkv_status make_plan(const pkv_cache_desc *c, int Hq, const pkv_decode_options *o, Plan *pl) {
+    if (Hq < 1 || Hq % c->num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
+                    Hq, c->num_kv_heads);
+    const int consumer = o ? o->consumer : 0;
+    if (consumer < 0 || consumer > 2) return fail(PKV_ERR_INVALID_ARG, "consumer %d", consumer);
+    pl->G = Hq / c->num_kv_heads;
+    pl->GC = pl->G < pkv::kMaxHeadsPerUnit ? pl->G : pkv::kMaxHeadsPerUnit;
+    pl->NC = (pl->G + pl->GC - 1) / pl->GC;
+    pl->U = c->num_kv_heads * pl->NC;
+    const bool half = c->dtype != PKV_F32;
+    if (consumer == 2 && !half)
+        return fail(PKV_ERR_UNSUPPORTED, "tensor-core math needs fp16 or bf16 K/V");
+    pl->mma = half && (consumer == 2 || (consumer == 0 && pl->G >= 3));
+    if (pl->mma) {
+        pl->gmax = pl->GC <= 8 ? 8 : 16;
+    } else {
+        int g = 1;
+        while (g < pl->GC) g <<= 1;
+        pl->gmax = g;
+    }
+    const int D = c->head_dim;
+    pl->variant = c->dtype == PKV_F32   ? pkv::find_variant_f32(D, pl->gmax, pl->mma)
+                  : c->dtype == PKV_F16 ? pkv::find_variant_f16(D, pl->gmax, pl->mma)
+                                        : pkv::find_variant_bf16(D, pl->gmax, pl->mma);
+    if (!pl->variant) return fail(PKV_ERR_UNSUPPORTED, "no kernel variant for this shape");
+    return PKV_OK;
+}
+
+pkv_status default_ctas(const Plan &pl, int *C) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
+    int occ = pl.variant->max_ctas_per_sm();
+    if (occ < 1) return fail(PKV_ERR_CUDA, "split-K kernel cannot be resident (occupancy 0)");
+    if (occ > pkv::kMaxCtasPerSm) occ = pkv::kMaxCtasPerSm;
+    *C = sms * occ;
+    return PKV_OK;
+}
+
+// workspace: [C] merge descriptors, then [C][2][GC][D] partial outputs, then
+// [C][2][GC] partial log2-sum-exp2 values
+size_t workspace_for(int C, int GC, int D) {
+    return (size_t)C * sizeof(pkv::MergeDesc) + (size_t)C * 2 * GC * (size_t)(D + 1) * sizeof(float);
+}
+
+pkv_status max_default_ctas(int *C) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
+    *C = sms * pkv::kMaxCtasPerSm;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+        case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_OUT_OF_RANGE: return "device-side value out of range";
+        case PKV_ERR_TIMEOUT: return "on-chip wait timed out";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char *pkv_last_error_message(void) { return g_msg; }
+
+pkv_status pkv_append(const pkv_cache_desc *cache, const void *k_new, const void *v_new,
+                      const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,
+                      void *v_pool, void *stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_pool || !v_pool)
+        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(slot_mapping, 8))
+        return fail(PKV_ERR_INVALID_ARG, "pointers must be 16-byte aligned (slot_mapping 8)");
+    unsigned *err = nullptr;
+    if ((st = device_error_ptr(&err)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_append(cache->dtype, k_new, v_new, slot_mapping, num_tokens, k_pool,
+                                       v_pool, cache->num_blocks, cache->num_kv_heads,
+                                       cache->block_size, cache->head_dim, err,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return PKV_OK;
+}
+
+pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pairs,
+                          int32_t num_pairs, void *k_pool, void *v_pool, void *stream) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs %d", num_pairs);
+    if (num_pairs == 0) return PKV_OK;
+    if (!src_dst_pairs || !k_pool || !v_pool)
+        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16))
+        return fail(PKV_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+    std::unordered_set<int64_t> srcs, dsts;
+    for (int i = 0; i < num_pairs; ++i) {
+        const int64_t s = src_dst_pairs[2 * i], d = src_dst_pairs[2 * i + 1];
+        if (s < 0 || s >= cache->num_blocks || d < 0 || d >= cache->num_blocks)
+            return fail(PKV_ERR_INVALID_ARG, "pair %d (%lld -> %lld) outside [0, %d)", i,
+                        (long long)s, (long long)d, cache->num_blocks);
+        if (!dsts.insert(d).second)
+            return fail(PKV_ERR_INVALID_ARG, "block %lld is the destination of two pairs", (long long)d);
+        srcs.insert(s);
+    }
+    for (int64_t d : dsts)
+        if (srcs.count(d))
+            return fail(PKV_ERR_INVALID_ARG, "block %lld is both a source and a destination",
+                        (long long)d);
+    const size_t block_bytes = (size_t)cache->num_kv_heads * cache->block_size * cache->head_dim *
+                               elem_bytes(cache->dtype);
+    for (int base = 0; base < num_pairs; base += pkv::kCopyPairsPerLaunch) {
+        pkv::CopyPairs cp;
+        const int n = num_pairs - base < pkv::kCopyPairsPerLaunch ? num_pairs - base
+                                                                 : pkv::kCopyPairsPerLaunch;
+        for (int i = 0; i < n; ++i) {
+            cp.src[i] = src_dst_pairs[2 * (base + i)];
+            cp.dst[i] = src_dst_pairs[2 * (base + i) + 1];
+        }
+        cudaError_t e = pkv::launch_block_copy(cp, n, k_pool, v_pool, block_bytes,
+                                               static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
+    }
+    return PKV_OK;
+}
+
+size_t pkv_decode_workspace_bytes_ex(const pkv_cache_desc *cache, int32_t num_q_heads,
+                                     int32_t num_ctas) {
+    if (check_cache(cache) != PKV_OK) return 0;
+    if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0 || num_ctas < 0) return 0;
+    int C = num_ctas;
+    if (C == 0 && max_default_ctas(&C) != PKV_OK) return 0;
+    const int G = num_q_heads / cache->num_kv_heads;
+    const int GC = G < pkv::kMaxHeadsPerUnit ? G : pkv::kMaxHeadsPerUnit;
+    return workspace_for(C, GC, cache->head_dim);
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc *cache, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t max_context_len) {
+    (void)num_seqs;
+    (void)max_context_len;
+    return pkv_decode_workspace_bytes_ex(cache, num_q_heads, 0);
+}
+
+pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, int32_t num_seqs,
+                                   int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, float scale, void *out,
+                                   int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                   void *stream, const pkv_decode_options *options) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d", num_seqs);
+    if (!valid_dtype(out_dtype)) return fail(PKV_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
+    if (max_blocks_per_seq < 1)
+        return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
+    if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+    Plan pl;
+    if ((st = make_plan(cache, num_q_heads, options, &pl)) != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
+        !aligned(out, elem_bytes(out_dtype)) || !aligned(block_tables, 4) ||
+        !aligned(context_lens, 4))
+        return fail(PKV_ERR_INVALID_ARG, "q and the pools must be 16-byte aligned");
+    // flattened tile count must fit in int32
+    const int64_t max_tiles_per_unit =
+        ((int64_t)max_blocks_per_seq * cache->block_size + PKV_TILE_TOKENS - 1) / PKV_TILE_TOKENS;
+    const int64_t chunk_seqs = num_seqs < pkv::kMaxSeqsPerLaunch ? num_seqs : pkv::kMaxSeqsPerLaunch;
+    if (chunk_seqs * pl.U * max_tiles_per_unit >= (int64_t)INT32_MAX)
+        return fail(PKV_ERR_UNSUPPORTED, "batch x context too large for one launch");
+
+    int C = options ? options->num_ctas : 0;
+    if (C < 0) return fail(PKV_ERR_INVALID_ARG, "num_ctas %d", C);
+    if (C == 0 && (st = default_ctas(pl, &C)) != PKV_OK) return st;
+    const size_t need = workspace_for(C, pl.GC, cache->head_dim);
+    if (C > 1 && (!workspace || workspace_bytes < need))
+        return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    workspace ? workspace_bytes : (size_t)0);
+    if (workspace && !aligned(workspace, 16))
+        return fail(PKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+
+    unsigned *err = nullptr;
+    if ((st = device_error_ptr(&err)) != PKV_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int es = elem_bytes(cache->dtype);
+    const int oes = elem_bytes(out_dtype);
+    const int D = cache->head_dim;
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    if (options)
+        for (int i = 0; i < 3; ++i) ev[i] = static_cast<cudaEvent_t>(options->timing_events[i]);
+
+    for (int s0 = 0; s0 < num_seqs; s0 += pkv::kMaxSeqsPerLaunch) {
+        const int S = num_seqs - s0 < pkv::kMaxSeqsPerLaunch ? num_seqs - s0 : pkv::kMaxSeqsPerLaunch;
+        pkv::DecodeParams p;
+        p.q = static_cast<const uint8_t *>(q) + (size_t)s0 * num_q_heads * D * es;
+        p.out = static_cast<uint8_t *>(out) + (size_t)s0 * num_q_heads * D * oes;
+        p.out_dtype = out_dtype;
+        p.block_tables = block_tables + (size_t)s0 * max_blocks_per_seq;
+        p.context_lens = context_lens + s0;
+        p.M = max_blocks_per_seq;
+        p.S = S;
+        p.Hq = num_q_heads;
+        p.Hk = cache->num_kv_heads;
+        p.G = pl.G;
+        p.NC = pl.NC;
+        p.GC = pl.GC;
+        p.U = pl.U;
+        p.B = cache->block_size;
+        p.NB = cache->num_blocks;
+        p.scale_log2 = scale * 1.4426950408889634f;
+        p.ws_desc = static_cast<pkv::MergeDesc *>(workspace);
+        p.ws_o = workspace ? reinterpret_cast<float *>(p.ws_desc + C) : nullptr;
+        p.ws_lse = workspace ? p.ws_o + (size_t)C * 2 * pl.GC * D : nullptr;
+        p.C = C;
+        p.err = err;
+        p.kp = k_pool;
+        p.vp = v_pool;
+        const bool first = s0 == 0;
+        cudaError_t e;
+        if (first && ev[0] && (e = cudaEventRecord(ev[0], s)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+        if ((e = pl.variant->launch(p, s)) != cudaSuccess)
+            return cuda_fail(e, "split-K decode launch");
+        if (first && ev[1] && (e = cudaEventRecord(ev[1], s)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+        if ((e = pkv::launch_merge(p, D, s)) != cudaSuccess) return cuda_fail(e, "merge launch");
+        if (first && ev[2] && (e = cudaEventRecord(ev[2], s)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+    }
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_attention(const pkv_cache_desc *cache, const void *q, int32_t num_seqs,
+                                int32_t num_q_heads, const void *k_pool, const void *v_pool,
+                                const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                const int32_t *context_lens, float scale, void *out,
+                                int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                void *stream) {
+    return pkv_decode_attention_ex(cache, q, num_seqs, num_q_heads, k_pool, v_pool, block_tables,
+                                   max_blocks_per_seq, context_lens, scale, out, out_dtype,
+                                   workspace, workspace_bytes, stream, nullptr);
+}
+
+pkv_status pkv_get_error(int32_t *device_error_word, void *stream) {
+    if (!device_error_word) return fail(PKV_ERR_INVALID_ARG, "device_error_word is NULL");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned w = 0;
+    e = cudaMemcpyFromSymbol(&w, g_pkv_error_word, sizeof(w));
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbol(g_pkv_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    *device_error_word = (int32_t)w;
+    if (w == 0) return PKV_OK;
+    if (w & PKV_DEVERR_TIMEOUT) return fail(PKV_ERR_TIMEOUT, "device error word 0x%x", w);
+    return fail(PKV_ERR_OUT_OF_RANGE, "device error word 0x%x", w);
+}
+
+}  // extern "C"

@@ -1,0 +1,93 @@
+// Internal declarations shared by libpkv's translation units (not part of the
+// C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kConsumerWarps = 4;                  // math warps of the split-K kernel
+constexpr int kProducerWarps = 4;                  // gather (cp.async) warps
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+constexpr int kMergeThreads = 128;
+constexpr int kMaxSeqsPerLaunch = 1024;            // larger batches are launched in chunks
+constexpr int kMaxCtasPerSm = 2;                   // cap used to size the workspace
+constexpr int kMaxHeadsPerUnit = 16;               // q heads carried by one work unit
+
+// Per-tile record the producer warp hands to the math warps with each stage.
+struct TileMeta {
+    int s;       // sequence (within this launch)
+    int h0;      // first q head of the unit
+    int gca;     // q heads in the unit
+    int ntok;    // valid tokens in this tile (1..64)
+    int flags;   // kFirst | kLast | kWhole
+    int slot;    // partial slot (0/1) when the segment is not a whole unit
+    int pad0, pad1;
+};
+constexpr int kFirst = 1;  // first tile of this CTA's segment of a unit
+constexpr int kLast = 2;   // last tile of this CTA's segment of a unit
+constexpr int kWhole = 4;  // the segment is the whole unit: write the output directly
+
+// Written by split-K CTA j-1 for the merge block of boundary j.
+struct MergeDesc {
+    int s;           // sequence, or -1 when boundary j cuts no unit it starts
+    int h0, gca;     // q heads of the unit
+    int slot_first;  // partial slot used by CTA j-1
+    int c_last;      // last CTA holding a partial of the unit
+    int nt;          // total tiles of the launch
+    int pad0, pad1;
+};
+
+struct DecodeParams {
+    const void *q;              // [S][Hq][D]
+    void *out;                  // [S][Hq][D] in out_dtype
+    int out_dtype;
+    const int32_t *block_tables;  // [S][M]
+    const int32_t *context_lens;  // [S]
+    int M;                      // table width
+    int S, Hq, Hk, G;           // sequences, q heads, kv heads, group size
+    int NC, GC, U;              // head chunks per kv head, heads per chunk, units per seq
+    int B, NB;                  // block size, physical blocks
+    float scale_log2;           // scale * log2(e)
+    float *ws_o;                // [C][2][GC][D] partial outputs (normalised)
+    float *ws_lse;              // [C][2][GC]     partial log2-sum-exp2
+    MergeDesc *ws_desc;         // [C]            merge descriptors
+    int C;                      // CTAs of the split-K launch
+    unsigned *err;              // device error word
+    const void *kp, *vp;        // pools [NB][Hk][B][D]
+};
+
+using SplitLaunchFn = cudaError_t (*)(const DecodeParams &, cudaStream_t);
+using MaxCtasFn = int (*)();
+
+struct DecodeVariant {
+    SplitLaunchFn launch;
+    MaxCtasFn max_ctas_per_sm;  // occupancy of the split-K kernel (0 = cannot run)
+};
+
+// Variant lookup per K/V dtype (defined in decode_<dtype>.cu). gmax is the
+// compile-time head capacity (1, 2, 4, 8 or 16); mma selects the tensor-core
+// math (16-bit dtypes, gmax 8 or 16). Returns nullptr if not built.
+const DecodeVariant *find_variant_f32(int D, int gmax, bool mma);
+const DecodeVariant *find_variant_f16(int D, int gmax, bool mma);
+const DecodeVariant *find_variant_bf16(int D, int gmax, bool mma);
+
+cudaError_t launch_merge(const DecodeParams &p, int D, cudaStream_t st);
+
+cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
+                          const int64_t *slot_mapping, int num_tokens, void *k_pool, void *v_pool,
+                          int NB, int Hk, int B, int D, unsigned *err, cudaStream_t st);
+
+constexpr int kCopyPairsPerLaunch = 128;
+struct CopyPairs {
+    long long src[kCopyPairsPerLaunch];
+    long long dst[kCopyPairsPerLaunch];
+};
+cudaError_t launch_block_copy(const CopyPairs &pairs, int n, void *k_pool, void *v_pool,
+                              size_t block_bytes, cudaStream_t st);
+
+}  // namespace pkv

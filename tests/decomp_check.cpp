@@ -1,0 +1,115 @@
+// Host-side check of the split-K work decomposition (csrc/decomp.h).
+//
+// For random batches it replays what the split-K kernel's producer decides
+// for every CTA (segments, whole-unit writes, partial slots) and what the
+// merge kernel reads, and checks that
+//   * every tile belongs to exactly one CTA and pkv_owner inverts pkv_split,
+//   * each CTA writes at most one partial per slot,
+//   * every unit is finished exactly once: either whole by one CTA, or merged
+//     by exactly one merge block that reads exactly the partials written for
+//     it, which together cover all its tiles.
+// Prints "OK" and exits 0 on success.
+#include <cstdio>
+#include <cstdlib>
+#include <random>
+#include <vector>
+
+#include "decomp.h"
+
+static int fails = 0;
+#define CHECK(c, ...)                                 \
+    do {                                              \
+        if (!(c)) {                                   \
+            if (fails++ < 10) {                       \
+                std::printf("FAIL %s:%d ", __FILE__, __LINE__); \
+                std::printf(__VA_ARGS__);             \
+                std::printf("\n");                    \
+            }                                         \
+        }                                             \
+    } while (0)
+
+int main() {
+    std::mt19937_64 rng(12345);
+    for (int trial = 0; trial < 3000 && fails == 0; ++trial) {
+        const int S = 1 + rng() % 40;
+        const int U = 1 + rng() % 6;
+        const int C = 1 + rng() % 200;
+        std::vector<int> len(S), n(S), prefix(S + 1, 0);
+        for (int s = 0; s < S; ++s) {
+            const int kind = rng() % 6;
+            len[s] = kind == 0 ? 0 : (kind == 1 ? 1 + rng() % 64 : 1 + rng() % 3000);
+            n[s] = pkv_tiles_of_len(len[s]);
+            prefix[s + 1] = prefix[s] + n[s] * U;
+        }
+        const int64_t NT = prefix[S];
+        if (NT == 0) continue;
+        const int units = S * U;
+        std::vector<int> whole(units, 0), merged(units, 0), covered(units, 0);
+        std::vector<int> slot_unit(2 * C, -1), slot_tiles(2 * C, 0);
+
+        for (int64_t t = 0; t < NT; ++t) {
+            const int c = pkv_owner(t, C, NT);
+            CHECK(c >= 0 && c < C && pkv_split(c, C, NT) <= t && t < pkv_split(c + 1, C, NT),
+                  "owner of tile %lld", (long long)t);
+        }
+        // producer replay
+        for (int c = 0; c < C; ++c) {
+            const int64_t t0 = pkv_split(c, C, NT), t1 = pkv_split(c + 1, C, NT);
+            int64_t t = t0;
+            while (t < t1) {
+                const int s = pkv_find_seq(prefix.data(), S, t);
+                CHECK(prefix[s] <= t && t < prefix[s + 1], "find_seq");
+                const int u = (int)((t - prefix[s]) / n[s]);
+                const int64_t Tu = prefix[s] + (int64_t)u * n[s];
+                const int64_t seg_end = (Tu + n[s] < t1) ? Tu + n[s] : t1;
+                const int unit = s * U + u;
+                const bool is_whole = Tu >= t0 && Tu + n[s] <= t1;
+                if (is_whole) {
+                    whole[unit]++;
+                } else {
+                    const int slot = Tu > t0 ? 1 : 0;
+                    CHECK(slot == pkv_partial_slot(c, C, NT, Tu), "slot rule");
+                    CHECK(slot_unit[2 * c + slot] == -1, "CTA %d writes slot %d twice", c, slot);
+                    slot_unit[2 * c + slot] = unit;
+                    slot_tiles[2 * c + slot] = (int)(seg_end - t);
+                }
+                t = seg_end;
+            }
+        }
+        // merge replay
+        for (int j = 1; j < C; ++j) {
+            const int64_t tau = pkv_split(j, C, NT);
+            if (tau >= NT) continue;
+            const int s = pkv_find_seq(prefix.data(), S, tau);
+            const int u = (int)((tau - prefix[s]) / n[s]);
+            const int64_t Tu = prefix[s] + (int64_t)u * n[s];
+            const int cf = pkv_owner(Tu, C, NT);
+            if (cf + 1 != j) continue;
+            const int cl = pkv_owner(Tu + n[s] - 1, C, NT);
+            const int unit = s * U + u;
+            merged[unit]++;
+            for (int c = cf; c <= cl; ++c) {
+                if (pkv_cta_empty(c, C, NT)) continue;
+                const int slot = pkv_partial_slot(c, C, NT, Tu);
+                CHECK(slot_unit[2 * c + slot] == unit, "merge of unit %d reads CTA %d slot %d", unit,
+                      c, slot);
+                covered[unit] += slot_tiles[2 * c + slot];
+            }
+        }
+        for (int s = 0; s < S; ++s)
+            for (int u = 0; u < U; ++u) {
+                const int unit = s * U + u;
+                if (n[s] == 0) {
+                    CHECK(whole[unit] == 0 && merged[unit] == 0, "empty unit touched");
+                    continue;
+                }
+                CHECK(whole[unit] + merged[unit] == 1, "unit %d finished %d+%d times (trial %d)",
+                      unit, whole[unit], merged[unit], trial);
+                if (merged[unit]) CHECK(covered[unit] == n[s], "unit %d covers %d of %d tiles", unit,
+                                        covered[unit], n[s]);
+            }
+    }
+    if (fails) return 1;
+    std::printf("OK\n");
+    return 0;
+}

@@ -1,0 +1,122 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every entry
+point include/pkv.h declares; host-side argument checks reject bad calls
+before touching a GPU; the split-K decomposition is consistent."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from paged_kv_cache_47_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (pkv_\w+)", out))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(L, n)
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert L.pkv_status_string(code) not in (b"", b"unknown status")
+    assert L.pkv_status_string(-99) == b"unknown status"
+
+
+def _desc(nb=8, b=16, hk=2, d=64, dt=binding.PKV_BF16):
+    return binding.CacheDesc(nb, b, hk, d, dt)
+
+
+def _append(L, desc, kn=16, vn=16, sm=16, n=1, kp=16, vp=16):
+    return L.pkv_append(ctypes.byref(desc) if desc is not None else None, kn, vn, sm, n, kp, vp,
+                        None)
+
+
+def test_append_rejects_bad_arguments(L):
+    assert _append(L, None) == -1
+    assert _append(L, _desc(dt=7)) == -2
+    assert _append(L, _desc(b=12)) == -2
+    assert _append(L, _desc(d=96)) == -2
+    assert _append(L, _desc(hk=0)) == -1
+    assert _append(L, _desc(nb=0)) == -1
+    assert _append(L, _desc(), n=-1) == -1
+    assert _append(L, _desc(), n=0) == 0           # no-op
+    assert _append(L, _desc(), kn=None) == -1
+    assert _append(L, _desc(), kp=24) == -1        # misaligned
+    assert b"aligned" in L.pkv_last_error_message()
+
+
+def _decode(L, desc, S=1, Hq=4, q=16, kp=16, vp=16, bt=16, M=4, cl=16, scale=1.0, out=16,
+            odt=2, ws=16, wsb=1 << 30, opts=None):
+    return L.pkv_decode_attention_ex(ctypes.byref(desc), q, S, Hq, kp, vp, bt, M, cl, scale,
+                                     out, odt, ws, wsb, None,
+                                     ctypes.byref(opts) if opts is not None else None)
+
+
+def test_decode_rejects_bad_arguments(L):
+    d = _desc()
+    assert _decode(L, d, Hq=3) == -1                       # Hq % Hk
+    assert _decode(L, d, S=-1) == -1
+    assert _decode(L, d, odt=5) == -2
+    assert _decode(L, d, M=0) == -1
+    assert _decode(L, d, scale=float("nan")) == -1
+    o = binding.DecodeOptions()
+    o.consumer = 2
+    assert _decode(L, _desc(dt=binding.PKV_F32), opts=o) == -2   # mma needs 16-bit
+    o.consumer = 3
+    assert _decode(L, d, opts=o) == -1
+    assert _decode(L, d, S=0) == 0                         # no-op
+    assert _decode(L, d, q=None) == -1
+    assert _decode(L, d, q=8) == -1                        # misaligned q
+
+
+def test_block_copy_rejects_bad_pairs(L):
+    d = _desc(nb=10)
+
+    def call(pairs):
+        p = torch.tensor(pairs, dtype=torch.int64)
+        return L.pkv_block_copy(ctypes.byref(d), p.data_ptr(), p.shape[0], 16, 16, None)
+
+    assert call([[0, 10]]) == -1          # out of range
+    assert call([[-1, 3]]) == -1
+    assert call([[1, 2], [3, 2]]) == -1   # same destination twice
+    assert call([[1, 2], [2, 3]]) == -1   # a destination that is also a source
+    assert L.pkv_block_copy(ctypes.byref(d), None, 1, 16, 16, None) == -1
+    assert L.pkv_block_copy(ctypes.byref(d), None, 0, 16, 16, None) == 0
+
+
+def test_workspace_size_formula(L):
+    d = _desc(hk=8, d=128)
+    # C CTAs x (32-byte merge descriptor + 2 slots x heads-per-unit x (D outputs + 1 lse) x 4 bytes)
+    assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 32, 10) == 10 * (32 + 2 * 4 * 129 * 4)
+    assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 8 * 40, 3) == 3 * (32 + 2 * 16 * 129 * 4)
+    assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 33, 10) == 0
+
+
+def test_decomposition_exhaustive(tmp_path):
+    exe = tmp_path / "decomp_check"
+    subprocess.run(["g++", "-O2", "-std=c++17", "-I", os.path.join(ROOT, "paged_kv_cache_47_gb300", "csrc"),
+                    os.path.join(ROOT, "tests", "decomp_check.cpp"), "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and r.stdout.strip() == "OK", r.stdout

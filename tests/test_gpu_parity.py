@@ -1,0 +1,273 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Append and block copy must be byte-exact. Decode attention must match the fp64
+oracle within max-abs 2e-3 for fp16/bf16 K/V and 1e-5 for fp32 K/V (the
+tolerance of the decode-attention target). Small cases compare every output
+element and cover the edge cases; the five workloads at full size compare
+sampled sequences (every head of each) in the launch configuration the
+benchmark times.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from paged_kv_cache_47_gb300 import binding, build, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.lib()
+    yield
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+def run_step(st, vals, *, out_dtype=None, num_ctas=0, consumer=0, check_pools=True):
+    """Copy-on-write + append + decode on the GPU and in the oracle; returns
+    (gpu_out as float64 numpy, oracle_out, GPU pools)."""
+    dev = "cuda"
+    spec = st.spec
+    scale = 1.0 / math.sqrt(spec.head_dim)
+    # oracle side (CPU copies of the inputs)
+    kp_o = vals["k_pool"].detach().cpu().clone()
+    vp_o = vals["v_pool"].detach().cpu().clone()
+    if st.cow_pairs.numel():
+        oracle.block_copy(st.cow_pairs, kp_o, vp_o)
+    oracle.append(vals["k_new"].cpu(), vals["v_new"].cpu(), st.slot_mapping, kp_o, vp_o)
+    ref = oracle.decode(vals["q"].cpu(), kp_o, vp_o, st.block_tables, st.context_lens, scale)
+    # CUDA side
+    kp = vals["k_pool"].to(dev).clone()
+    vp = vals["v_pool"].to(dev).clone()
+    if st.cow_pairs.numel():
+        binding.block_copy(st.cow_pairs, kp, vp)
+    binding.append(vals["k_new"].to(dev), vals["v_new"].to(dev), st.slot_mapping.to(dev), kp, vp)
+    out = binding.decode_attention(vals["q"].to(dev), kp, vp, st.block_tables.to(dev),
+                                   st.context_lens.to(dev), scale, out_dtype=out_dtype,
+                                   num_ctas=num_ctas, consumer=consumer)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    if check_pools:
+        assert torch.equal(_bits(kp.cpu()), _bits(kp_o)), "K pool differs after append/copy"
+        assert torch.equal(_bits(vp.cpu()), _bits(vp_o)), "V pool differs after append/copy"
+    return out.double().cpu().numpy(), ref, (kp, vp)
+
+
+def assert_close(got, ref, dtype, what=""):
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), f"non-finite output {what}"
+    m = float(err.max()) if err.size else 0.0
+    assert m <= TOL[dtype], f"max abs err {m:.3e} > {TOL[dtype]} {what}"
+    return m
+
+
+def spec_like(i, **kw):
+    return W.SPECS[i].__class__(**{**W.SPECS[i].__dict__, **kw})
+
+
+# ----------------------------------------------------------------- small cases
+RAGGED = [1, 2, 15, 16, 17, 63, 64, 65, 127, 129, 300, 1000]
+
+
+def test_tiny_workload_full():
+    st, vals = W.make_workload(0, seed=0)
+    got, ref, _ = run_step(st, vals)
+    assert_close(got, ref, "f32")
+
+
+@pytest.mark.parametrize("num_ctas", [0, 1, 3, 7, 64, 600])
+def test_gqa4_bf16_ragged_ctas(num_ctas):
+    spec = spec_like(1, num_seqs=len(RAGGED))
+    st, vals = W.make_workload(spec, seed=1, lengths=RAGGED)
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32, num_ctas=num_ctas)
+    assert_close(got, ref, "bf16", f"ctas={num_ctas}")
+
+
+@pytest.mark.parametrize("consumer", [1, 2])
+@pytest.mark.parametrize("dtype,Hq,Hk", [("bf16", 32, 8), ("f16", 8, 8), ("f16", 16, 8),
+                                          ("bf16", 24, 8), ("bf16", 64, 8), ("f16", 40, 2)])
+def test_forced_consumers(consumer, dtype, Hq, Hk):
+    spec = W.WorkloadSpec("t", 5, Hq, Hk, 128, 16, dtype, 1.0)
+    st, vals = W.make_workload(spec, seed=2, lengths=[1, 40, 64, 333, 777])
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32, consumer=consumer, num_ctas=9)
+    assert_close(got, ref, dtype, f"consumer={consumer}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("Hq,Hk,D,B", [(4, 4, 64, 16), (8, 2, 64, 8), (16, 1, 128, 32),
+                                        (12, 4, 128, 8), (20, 1, 64, 16)])
+def test_shapes_and_dtypes(dtype, Hq, Hk, D, B):
+    spec = W.WorkloadSpec("t", 4, Hq, Hk, D, B, dtype, 1.0)
+    st, vals = W.make_workload(spec, seed=3, lengths=[5, 70, 129, 450])
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32, num_ctas=5)
+    assert_close(got, ref, dtype)
+
+
+def test_mha_fp16_small():
+    spec = spec_like(2, num_seqs=6)
+    st, vals = W.make_workload(spec, seed=4, lengths=[128, 129, 700, 2048, 1, 64])
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32)
+    assert_close(got, ref, "f16")
+
+
+def test_prefix_sharing_with_copy_on_write_small():
+    spec = spec_like(3, num_seqs=5, shared_prefix=256, suffix_lo=0, suffix_hi=300)
+    st, vals = W.make_workload(spec, seed=5)
+    assert st.cow_pairs.shape[0] == 4
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32, num_ctas=11)
+    assert_close(got, ref, "f16")
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_long_context_gqa8_small(B):
+    spec = spec_like(4, num_seqs=2)
+    st, vals = W.make_workload(spec, seed=6, block_size=B, lengths=[3001, 5000])
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32)
+    assert_close(got, ref, "bf16", f"B={B}")
+
+
+def test_zero_length_sequences_give_zeros():
+    spec = W.WorkloadSpec("t", 4, 8, 2, 64, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=7, lengths=[0, 33, 0, 90])
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32, num_ctas=4)
+    assert np.all(got[0] == 0) and np.all(got[2] == 0)
+    assert_close(got, ref, "bf16")
+
+
+def test_native_output_is_rne_of_fp32_output():
+    spec = spec_like(1, num_seqs=4)
+    st, vals = W.make_workload(spec, seed=8, lengths=[3, 100, 1500, 4096])
+    f32, _, _ = run_step(st, vals, out_dtype=torch.float32, check_pools=False)
+    b16, ref, _ = run_step(st, vals, out_dtype=torch.bfloat16, check_pools=False)
+    rne = torch.from_numpy(f32).float().to(torch.bfloat16).double().numpy()
+    assert np.array_equal(b16, rne)
+
+
+def test_repeated_calls_are_deterministic():
+    spec = spec_like(1, num_seqs=5)
+    st, vals = W.make_workload(spec, seed=9, lengths=[17, 500, 1200, 64, 4000])
+    a, _, _ = run_step(st, vals, out_dtype=torch.float32, check_pools=False)
+    b, _, _ = run_step(st, vals, out_dtype=torch.float32, check_pools=False)
+    assert np.array_equal(a, b)
+
+
+def test_many_sequences_chunked_launch():
+    # more sequences than one launch carries: the library splits the batch
+    spec = W.WorkloadSpec("t", 1100, 8, 8, 64, 16, "f16", 1.0, 1, 40)
+    st, vals = W.make_workload(spec, seed=10)
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32)
+    assert_close(got, ref, "f16")
+
+
+# ----------------------------------------------------------------- device-side checks
+def test_out_of_range_block_id_sets_error_word():
+    spec = W.WorkloadSpec("t", 2, 8, 2, 64, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=11, lengths=[40, 20])
+    bt = st.block_tables.clone()
+    bt[0, 1] = st.num_blocks + 5
+    dev = "cuda"
+    kp, vp = vals["k_pool"].to(dev), vals["v_pool"].to(dev)
+    binding.append(vals["k_new"].to(dev), vals["v_new"].to(dev), st.slot_mapping.to(dev), kp, vp)
+    binding.get_error()
+    out = binding.decode_attention(vals["q"].to(dev), kp, vp, bt.to(dev),
+                                   st.context_lens.to(dev), 0.125, out_dtype=torch.float32)
+    w = binding.get_error()
+    assert w & binding.DEVERR_BLOCK_ID
+    assert torch.isfinite(out[1]).all()
+
+
+def test_context_len_past_table_sets_error_word():
+    spec = W.WorkloadSpec("t", 2, 8, 2, 64, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=12, lengths=[40, 20])
+    cl = st.context_lens.clone()
+    cl[1] = 10_000
+    dev = "cuda"
+    binding.get_error()
+    binding.decode_attention(vals["q"].to(dev), vals["k_pool"].to(dev), vals["v_pool"].to(dev),
+                             st.block_tables.to(dev), cl.to(dev), 0.125)
+    assert binding.get_error() & binding.DEVERR_CONTEXT
+
+
+def test_append_slot_past_pool_sets_error_word():
+    kp = torch.zeros(4, 2, 16, 64, dtype=torch.float16, device="cuda")
+    vp = torch.zeros_like(kp)
+    kn = torch.ones(2, 2, 64, dtype=torch.float16, device="cuda")
+    binding.get_error()
+    binding.append(kn, kn, torch.tensor([3, 4 * 16], dtype=torch.int64, device="cuda"), kp, vp)
+    assert binding.get_error() & binding.DEVERR_SLOT
+    assert torch.all(kp[0, :, 3] == 1) and int((kp != 0).sum()) == 2 * 64
+
+
+def test_block_copy_leaves_other_blocks_untouched():
+    g = torch.Generator().manual_seed(13)
+    kp = torch.randn(20, 3, 8, 64, generator=g).to(torch.bfloat16)
+    vp = torch.randn(20, 3, 8, 64, generator=g).to(torch.bfloat16)
+    pairs = [[1, 5], [7, 2], [19, 0]]
+    ko, vo = kp.clone(), vp.clone()
+    oracle.block_copy(pairs, ko, vo)
+    kg, vg = kp.cuda(), vp.cuda()
+    binding.block_copy(pairs, kg, vg)
+    assert torch.equal(_bits(kg.cpu()), _bits(ko)) and torch.equal(_bits(vg.cpu()), _bits(vo))
+
+
+def test_many_block_copy_pairs():
+    NB = 600
+    kp = torch.arange(NB * 2 * 16 * 64, dtype=torch.float32).view(NB, 2, 16, 64)
+    vp = -kp
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(1)).tolist()
+    pairs = [[perm[i], perm[i + 300]] for i in range(300)]
+    ko, vo = kp.clone(), vp.clone()
+    oracle.block_copy(pairs, ko, vo)
+    kg, vg = kp.cuda(), vp.cuda()
+    binding.block_copy(pairs, kg, vg)
+    assert torch.equal(kg.cpu(), ko) and torch.equal(vg.cpu(), vo)
+
+
+# ----------------------------------------------------------------- full-size workloads
+def _full(i, block_size=None, samples=3, seed=0):
+    spec = W.SPECS[i] if block_size is None else W.SPECS[i].with_block_size(block_size)
+    st = W.make_structure(spec, seed)
+    vals = W.make_values(st, seed, device="cuda")
+    dev = "cuda"
+    scale = 1.0 / math.sqrt(spec.head_dim)
+    kp, vp = vals["k_pool"].clone(), vals["v_pool"].clone()
+    if st.cow_pairs.numel():
+        binding.block_copy(st.cow_pairs, kp, vp)
+    binding.append(vals["k_new"], vals["v_new"], st.slot_mapping.to(dev), kp, vp)
+    out = binding.decode_attention(vals["q"], kp, vp, st.block_tables.to(dev),
+                                   st.context_lens.to(dev), scale)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    # oracle on host copies
+    kp_o, vp_o = vals["k_pool"].cpu(), vals["v_pool"].cpu()
+    if st.cow_pairs.numel():
+        oracle.block_copy(st.cow_pairs, kp_o, vp_o)
+    oracle.append(vals["k_new"].cpu(), vals["v_new"].cpu(), st.slot_mapping, kp_o, vp_o)
+    assert torch.equal(_bits(kp.cpu()), _bits(kp_o)) and torch.equal(_bits(vp.cpu()), _bits(vp_o))
+    S = st.context_lens.numel()
+    lens = st.context_lens.tolist()
+    pick = sorted({int(np.argmax(lens)), int(np.argmin(lens))} |
+                  set(torch.randperm(S, generator=torch.Generator().manual_seed(seed))[:samples].tolist()))
+    ref = oracle.decode(vals["q"].cpu(), kp_o, vp_o, st.block_tables, st.context_lens, scale,
+                        seq_ids=pick)
+    got = out[pick].double().cpu().numpy()
+    return assert_close(got, ref, spec.dtype, f"workload {i} B={spec.block_size}")
+
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3])
+def test_full_workload_sampled(i):
+    _full(i)
+
+
+@pytest.mark.parametrize("B", [8, 16, 32])
+def test_full_long_context_sampled(B):
+    _full(4, block_size=B, samples=1)
