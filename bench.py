@@ -167,12 +167,19 @@ def dist_env():
 
 
 def reduce_max(x: float, world: int, device) -> float:
+    """Max of x over all ranks (the slowest rank sets the job's time)."""
     if world == 1:
         return x
     import torch.distributed as dist
     t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_gbs(bytes_per_rank_step: int, steps: int, max_rank_seconds: float, world: int) -> float:
+    """Whole-job GB/s: every rank moves bytes_per_rank_step per step (replicas,
+    weak scaling) and the job takes as long as its slowest rank."""
+    return world * bytes_per_rank_step * steps / max_rank_seconds / 1e9
 
 
 def barrier(world: int):
@@ -354,7 +361,7 @@ def run_ours(args):
         raise RuntimeError("device error word set during the timed region")
 
     per_step_s = ms_max / 1000.0 / args.steps
-    value = world * total_bytes / per_step_s / 1e9
+    value = job_gbs(total_bytes, args.steps, ms_max / 1000.0, world)
     seq_tok = world * int(st.context_lens.sum()) / per_step_s
     peak, peak_kind = peaks()
 
