@@ -173,6 +173,37 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
                                    void *stream, const pkv_decode_options *options);
 
 /*
+ * pkv_decode_attention_static — pkv_decode_attention for callers that cannot
+ * allocate device memory. The pages have no counterpart to this entry point.
+ *
+ * Some callers cannot provide the split-K workspace: a program that has
+ * already given its whole device-memory budget to the KV-cache pool, a
+ * plug-in that may only use memory its host framework owns, or code on a
+ * path where cudaMalloc (which can synchronise the device) is not allowed.
+ * This call takes the same inputs and output as pkv_decode_attention, minus
+ * the workspace, and uses instead a fixed scratch array of
+ * PKV_STATIC_SCRATCH_BYTES in the library's own device memory (every GPU that
+ * loads the library holds it until the process exits). It allocates nothing.
+ *
+ * It launches one split-K CTA per SM; a shape whose scratch need exceeds
+ * PKV_STATIC_SCRATCH_BYTES (need = SMs x (32 + 8 x heads-per-unit x
+ * (head_dim + 1)) bytes, heads-per-unit = min(16, num_q_heads/num_kv_heads))
+ * is rejected with PKV_ERR_WORKSPACE and nothing is enqueued.
+ * The first call on a device finds the scratch array's device address (once
+ * per device, with that device current); make that first call before any
+ * stream capture. All calls on a device share the array and it keeps the last
+ * call's contents; nothing in it needs clearing, but calls whose kernels
+ * overlap on the GPU race on it, so order them (e.g. one stream).
+ */
+#define PKV_STATIC_SCRATCH_BYTES (2u << 20)
+pkv_status pkv_decode_attention_static(const pkv_cache_desc *cache, const void *q,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       const void *k_pool, const void *v_pool,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *context_lens, float scale, void *out,
+                                       int32_t out_dtype, void *stream);
+
+/*
  * pkv_block_copy — copy whole physical blocks, K and V, all kv heads.
  *
  * Passage: copy-on-write copies the one block a writer hits while others

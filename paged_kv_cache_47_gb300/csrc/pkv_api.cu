@@ -137,6 +137,16 @@ pkv_status max_default_ctas(int *C) {
 
 }  // namespace
 
+namespace pkv {
+pkv_status set_last_error(pkv_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return st;
+}
+}  // namespace pkv
+
 extern "C" {
 
 const char *pkv_status_string(pkv_status s) {

@@ -78,6 +78,9 @@ const DecodeVariant *find_variant_bf16(int D, int gmax, bool mma);
 
 cudaError_t launch_merge(const DecodeParams &p, int D, cudaStream_t st);
 
+// Record the text pkv_last_error_message returns on this thread; returns st.
+pkv_status set_last_error(pkv_status st, const char *fmt, ...);
+
 cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
                           const int64_t *slot_mapping, int num_tokens, void *k_pool, void *v_pool,
                           int NB, int Hk, int B, int D, unsigned *err, cudaStream_t st);
