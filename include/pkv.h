@@ -156,7 +156,8 @@ typedef struct {
                                 mma (16-bit dtypes only)                        */
     void *timing_events[3];  /* optional cudaEvent_t recorded on `stream` before
                                 the split-K kernel, between it and the merge,
-                                and after the merge (NULL = not recorded)       */
+                                and after the merge (NULL = not recorded); under
+                                stream capture they become event-record nodes */
 } pkv_decode_options;
 
 /* Workspace bytes for pkv_decode_attention_ex with options->num_ctas = num_ctas

@@ -162,6 +162,66 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
     return out
 
 
+class PreparedDecode:
+    """A decode-attention call whose arguments are marshalled once.
+
+    For repeated decode steps on stable buffers (the usual serving loop, and
+    CUDA-graph capture): the tensors' addresses, shapes and the workspace are
+    fixed at construction; each call only passes the stream. The caller keeps
+    the tensors alive and rewrites their contents in place between steps.
+    """
+
+    def __init__(self, q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                 out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                 num_ctas: int = 0, consumer: int = 0):
+        self._desc = _pools(k_pool, v_pool)
+        for t in (q, block_tables, context_lens, out):
+            if not t.is_contiguous():
+                raise ValueError("prepared decode needs contiguous tensors")
+        assert block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+        assert q.dtype == k_pool.dtype
+        S, Hq, D = q.shape
+        if workspace is None:
+            workspace = alloc_workspace(k_pool, Hq, num_ctas)
+        self._keep = (q, k_pool, v_pool, block_tables, context_lens, out, workspace)
+        self._opts = DecodeOptions()
+        self._opts.num_ctas = num_ctas
+        self._opts.consumer = consumer
+        self._args = (ctypes.byref(self._desc), q.data_ptr(), S, Hq, k_pool.data_ptr(),
+                      v_pool.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
+                      context_lens.data_ptr(), float(scale), out.data_ptr(),
+                      DTYPE_CODE[out.dtype], workspace.data_ptr(),
+                      workspace.numel() * workspace.element_size())
+        self._fn = lib().pkv_decode_attention_ex
+        self.out = out
+
+    def __call__(self, stream, timing_events: Optional[Sequence] = None) -> None:
+        opts = self._opts
+        for i in range(3):
+            ev = timing_events[i] if timing_events is not None else None
+            opts.timing_events[i] = None if ev is None else ev.cuda_event
+        _check(self._fn(*self._args, _stream(stream), ctypes.byref(opts)))
+
+
+class PreparedAppend:
+    """An append call whose arguments are marshalled once (see PreparedDecode)."""
+
+    def __init__(self, k_new, v_new, slot_mapping, k_pool, v_pool):
+        self._desc = _pools(k_pool, v_pool)
+        for t in (k_new, v_new, slot_mapping):
+            if not t.is_contiguous():
+                raise ValueError("prepared append needs contiguous tensors")
+        assert slot_mapping.dtype == torch.int64 and k_new.dtype == k_pool.dtype
+        self._keep = (k_new, v_new, slot_mapping, k_pool, v_pool)
+        self._args = (ctypes.byref(self._desc), k_new.data_ptr(), v_new.data_ptr(),
+                      slot_mapping.data_ptr(), slot_mapping.numel(), k_pool.data_ptr(),
+                      v_pool.data_ptr())
+        self._fn = lib().pkv_append
+
+    def __call__(self, stream) -> None:
+        _check(self._fn(*self._args, _stream(stream)))
+
+
 def block_copy(pairs, k_pool, v_pool, stream=None) -> None:
     """Copy whole blocks src -> dst; pairs is host data [n][2] (list or CPU tensor)."""
     desc = _pools(k_pool, v_pool)

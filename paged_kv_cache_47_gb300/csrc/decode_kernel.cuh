@@ -751,10 +751,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Block j (1 <= j < C) merges the unit described by descriptor j (written by
 // split-K CTA j-1 when that unit starts in its range and runs past it):
 //   lse = log2 sum_p 2^{lse_p},  out = sum_p 2^{lse_p - lse} o_p
-// over the partials of CTAs j-1 .. c_last; CTAs with an empty tile range
-// wrote nothing and are skipped.
+// over the partials of CTAs j-1 .. c_last, in that order, with a running max
+// (one pass). CTAs with an empty tile range wrote nothing and are skipped.
+// Thread t owns element d = t % D of heads t / D, t / D + 128 / D, ...; all
+// loads of one partial are independent, so the merge costs about two memory
+// round trips (descriptor, then partials).
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
+    constexpr int HPT = kMaxHeadsPerUnit * D / kMergeThreads;  // heads per thread (max)
+    constexpr int HSTEP = kMergeThreads / D;
     grid_dependency_wait();   // partials come from the split-K kernel just before
     const int j = blockIdx.x + 1;
     const MergeDesc md = p.ws_desc[j];
@@ -762,24 +767,41 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const Decod
     const int C = p.C;
     const int64_t NT = md.nt;
     const int c_first = j - 1;
-    for (int idx = threadIdx.x; idx < md.gca * D; idx += blockDim.x) {
-        const int jj = idx / D, d = idx - (idx / D) * D;
-        float M = -CUDART_INF_F;
-        for (int c = c_first; c <= md.c_last; ++c) {
-            if (pkv_cta_empty(c, C, NT)) continue;
-            const int slot = c == c_first ? md.slot_first : 0;
-            M = fmaxf(M, p.ws_lse[(c * 2 + slot) * p.GC + jj]);
+    const int d = threadIdx.x % D;
+    const int h_first = threadIdx.x / D;
+    float M[HPT], W[HPT], O[HPT];
+#pragma unroll
+    for (int k = 0; k < HPT; ++k) {
+        M[k] = -CUDART_INF_F;
+        W[k] = 0.f;
+        O[k] = 0.f;
+    }
+#pragma unroll 2
+    for (int c = c_first; c <= md.c_last; ++c) {
+        if (pkv_cta_empty(c, C, NT)) continue;
+        const int slot = c == c_first ? md.slot_first : 0;
+        const int b0 = (c * 2 + slot) * p.GC;
+        float lse[HPT], o[HPT];
+#pragma unroll
+        for (int k = 0; k < HPT; ++k) {
+            const int h = h_first + k * HSTEP;
+            lse[k] = h < md.gca ? p.ws_lse[b0 + h] : -CUDART_INF_F;
+            o[k] = h < md.gca ? p.ws_o[(size_t)(b0 + h) * D + d] : 0.f;
         }
-        float W = 0.f, O = 0.f;
-        for (int c = c_first; c <= md.c_last; ++c) {
-            if (pkv_cta_empty(c, C, NT)) continue;
-            const int slot = c == c_first ? md.slot_first : 0;
-            const int b = (c * 2 + slot) * p.GC + jj;
-            const float w = exp2f(p.ws_lse[b] - M);
-            W += w;
-            O = fmaf(w, p.ws_o[(size_t)b * D + d], O);
+#pragma unroll
+        for (int k = 0; k < HPT; ++k) {
+            const float mn = fmaxf(M[k], lse[k]);
+            const float a = exp2f(M[k] - mn), w = exp2f(lse[k] - mn);
+            W[k] = W[k] * a + w;
+            O[k] = O[k] * a + w * o[k];
+            M[k] = mn;
         }
-        store_out(p.out, ((size_t)md.s * p.Hq + md.h0 + jj) * D + d, p.out_dtype, O / W);
+    }
+#pragma unroll
+    for (int k = 0; k < HPT; ++k) {
+        const int h = h_first + k * HSTEP;
+        if (h < md.gca)
+            store_out(p.out, ((size_t)md.s * p.Hq + md.h0 + h) * D + d, p.out_dtype, O[k] / W[k]);
     }
 }
 
@@ -822,14 +844,19 @@ struct SplitVariant {
         return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA>, p);
     }
 
+    // occupancy of this variant on the current device (queried once per device)
     static int max_ctas_per_sm() {
+        static int cached[64] = {0};
         int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || prepare(dev) != cudaSuccess) return 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+        if (cached[dev] > 0) return cached[dev];
+        if (prepare(dev) != cudaSuccess) return 0;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                 &n, decode_split_kernel<T, D, GMAX, MMA>, kThreads,
                 Cfg::smem_bytes(kMaxSeqsPerLaunch)) != cudaSuccess)
             return 0;
+        cached[dev] = n;
         return n;
     }
 

@@ -108,11 +108,27 @@ pkv_status make_plan(const pkv_cache_desc *c, int Hq, const pkv_decode_options *
     return PKV_OK;
 }
 
-pkv_status default_ctas(const Plan &pl, int *C) {
-    int dev = 0, sms = 0;
+// SM count of the current device (queried once per device)
+pkv_status sm_count(int *sms) {
+    static int cached[64] = {0};
+    int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device index %d", dev);
+    if (cached[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
+        cached[dev] = n;
+    }
+    *sms = cached[dev];
+    return PKV_OK;
+}
+
+pkv_status default_ctas(const Plan &pl, int *C) {
+    int sms = 0;
+    pkv_status st = sm_count(&sms);
+    if (st != PKV_OK) return st;
     int occ = pl.variant->max_ctas_per_sm();
     if (occ < 1) return fail(PKV_ERR_CUDA, "split-K kernel cannot be resident (occupancy 0)");
     if (occ > pkv::kMaxCtasPerSm) occ = pkv::kMaxCtasPerSm;
@@ -127,12 +143,23 @@ size_t workspace_for(int C, int GC, int D) {
 }
 
 pkv_status max_default_ctas(int *C) {
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
+    int sms = 0;
+    pkv_status st = sm_count(&sms);
+    if (st != PKV_OK) return st;
     *C = sms * pkv::kMaxCtasPerSm;
     return PKV_OK;
+}
+
+// Timing events: under stream capture they must be recorded as external
+// event-record nodes (a plain record would only express a dependency inside
+// the graph); outside capture the external flag is not allowed.
+cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    return cudaEventRecord(ev, s);
 }
 
 }  // namespace
@@ -323,14 +350,14 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
         p.vp = v_pool;
         const bool first = s0 == 0;
         cudaError_t e;
-        if (first && ev[0] && (e = cudaEventRecord(ev[0], s)) != cudaSuccess)
+        if (first && ev[0] && (e = record_timing_event(ev[0], s)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
         if ((e = pl.variant->launch(p, s)) != cudaSuccess)
             return cuda_fail(e, "split-K decode launch");
-        if (first && ev[1] && (e = cudaEventRecord(ev[1], s)) != cudaSuccess)
+        if (first && ev[1] && (e = record_timing_event(ev[1], s)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
         if ((e = pkv::launch_merge(p, D, s)) != cudaSuccess) return cuda_fail(e, "merge launch");
-        if (first && ev[2] && (e = cudaEventRecord(ev[2], s)) != cudaSuccess)
+        if (first && ev[2] && (e = record_timing_event(ev[2], s)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
     }
     return PKV_OK;
