@@ -16,6 +16,15 @@
 
 namespace pkv {
 
+// Programmatic dependent launch (see device_utils.cuh; duplicated here to keep
+// this translation unit free of the decode headers).
+__device__ __forceinline__ void append_wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void append_allow_next_grid() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // grid-stride over (token, vector-in-token); vectors per token = Hk*D*es/16
 __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k_new,
                                                      const uint4 *__restrict__ v_new,
@@ -24,6 +33,11 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
                                                      uint4 *__restrict__ v_pool, int NB, int B,
                                                      int vec_per_row, int vec_per_token,
                                                      unsigned *err) {
+    // launched with programmatic serialisation: the previous kernel on the
+    // stream must be complete before any pool byte is touched; the next one
+    // (the decode) may be scheduled meanwhile
+    append_allow_next_grid();
+    append_wait_prior_grid();
     const int64_t total = (int64_t)num_tokens * vec_per_token;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -56,11 +70,20 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
     const int threads = 256;
     int64_t blocks = (total + threads - 1) / threads;
     if (blocks > 4096) blocks = 4096;
-    append_kernel<<<(int)blocks, threads, 0, st>>>(
-        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping,
-        num_tokens, static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), NB, B, vec_per_row,
-        vec_per_token, err);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_kernel, static_cast<const uint4 *>(k_new),
+                              static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
+                              static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), NB, B,
+                              vec_per_row, vec_per_token, err);
 }
 
 // blockIdx.y = pair; grid-stride over the block's 16-byte vectors.

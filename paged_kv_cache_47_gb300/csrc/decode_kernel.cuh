@@ -760,7 +760,8 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
     constexpr int HPT = kMaxHeadsPerUnit * D / kMergeThreads;  // heads per thread (max)
     constexpr int HSTEP = kMergeThreads / D;
-    grid_dependency_wait();   // partials come from the split-K kernel just before
+    grid_dependents_launch();  // the next kernel (e.g. the next append) may be scheduled
+    grid_dependency_wait();    // partials come from the split-K kernel just before
     const int j = blockIdx.x + 1;
     const MergeDesc md = p.ws_desc[j];
     if (md.s < 0) return;
