@@ -51,6 +51,19 @@ PROFILE = os.path.join(ROOT, "profiles", "decode_split_kernel_llama3_8b.md")
 
 
 # ------------------------------------------------------------------ helpers
+def unique_kv_bytes(st, spec):
+    """K/V bytes of the distinct physical rows the step reads (a block shared
+    by several sequences counted once)."""
+    es = torch.tensor([], dtype=W.DTYPES[spec.dtype]).element_size()
+    B = spec.block_size
+    rows = {}
+    for s, L in enumerate(st.context_lens.tolist()):
+        for j in range(-(-L // B)):
+            b = int(st.block_tables[s, j])
+            rows[b] = max(rows.get(b, 0), min(B, L - j * B))
+    return sum(rows.values()) * 2 * spec.num_kv_heads * spec.head_dim * es
+
+
 def step_bytes(st, spec):
     """Algorithmic bytes of one decode step (decode + append)."""
     es = torch.tensor([], dtype=W.DTYPES[spec.dtype]).element_size()
@@ -267,11 +280,15 @@ def run_reference(args):
 
 
 def workload_config(spec, st):
-    return {"workload": "llama3_8b_decode_step", "num_seqs": spec.num_seqs,
+    return {"workload": spec.name + "_decode_step", "num_seqs": spec.num_seqs,
             "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
             "head_dim": spec.head_dim, "block_size": spec.block_size, "kv_dtype": spec.dtype,
-            "context_lens": f"U[{spec.len_lo},{spec.len_hi}] seed 0, sum {int(st.context_lens.sum())}",
-            "pool_blocks": st.num_blocks, "step": "pkv_append + pkv_decode_attention (split-K + merge)"}
+            "context_lens": (f"{spec.shared_prefix}-token shared prefix + U[{spec.suffix_lo},{spec.suffix_hi}]"
+                             if spec.shared_prefix else f"U[{spec.len_lo},{spec.len_hi}]")
+                            + f" seed 0, sum {int(st.context_lens.sum())}",
+            "pool_blocks": st.num_blocks,
+            "step": ("pkv_block_copy (copy-on-write) + " if st.cow_pairs.numel() else "")
+                    + "pkv_append + pkv_decode_attention (split-K + merge)"}
 
 
 # ------------------------------------------------------------------ our arm
@@ -291,10 +308,16 @@ def run_ours(args):
     barrier(world)
     binding.lib()
 
-    spec = W.SPECS[WORKLOAD_INDEX]
+    spec = W.SPECS[args.workload]
+    if args.block_size:
+        spec = spec.with_block_size(args.block_size)
+    if args.dtype:
+        from dataclasses import replace
+        spec = replace(spec, dtype=args.dtype)
     st = W.make_structure(spec, args.seed)
     scale = 1.0 / math.sqrt(spec.head_dim)
     vals = W.make_values(st, args.seed, device=dev)
+    cow = st.cow_pairs if st.cow_pairs.numel() else None
     tables = st.block_tables.to(dev)
     lens = st.context_lens.to(dev)
     slots = st.slot_mapping.to(dev)
@@ -309,16 +332,27 @@ def run_ours(args):
         copies.append((kp, vp, out, ws))
     decode_bytes, append_bytes = step_bytes(st, spec)
     total_bytes = decode_bytes + append_bytes
+    if cow is not None:
+        es = vals["q"].element_size()
+        total_bytes += cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * spec.head_dim * es
+    # bytes the split-K kernel must bring from HBM: shared blocks once
+    hbm_decode_bytes = decode_bytes - (int(st.context_lens.sum()) * 2 * spec.num_kv_heads *
+                                       spec.head_dim * vals["q"].element_size()) + \
+        unique_kv_bytes(st, spec)
     stream = torch.cuda.current_stream()
     # prepared calls: the C-ABI arguments are marshalled once per cache copy
     calls = []
     for kp, vp, out, ws in copies:
         calls.append((binding.PreparedAppend(vals["k_new"], vals["v_new"], slots, kp, vp),
-                      binding.PreparedDecode(vals["q"], kp, vp, tables, lens, scale, out, ws)))
+                      binding.PreparedDecode(vals["q"], kp, vp, tables, lens, scale, out, ws,
+                                             consumer=args.consumer)))
 
     def step(i, evs=None, s=None):
         app, dec = calls[i % len(calls)]
         s = s if s is not None else torch.cuda.current_stream()
+        if cow is not None:      # copy-on-write of the last shared block, then append
+            kp, vp = copies[i % len(copies)][:2]
+            binding.block_copy(cow, kp, vp, stream=s)
         app(s)
         dec(s, timing_events=evs)
 
@@ -411,14 +445,15 @@ def run_ours(args):
         "seq_tokens_per_s": round(seq_tok, 1),
         "hbm_frac_of_measured": round(value / peak / world, 4),
         "roofline": {"bound": "hbm", "kernel": "decode_split_kernel",
-                     "achieved": round(decode_bytes / (split_avg / 1000.0) / 1e9, 2),
+                     "achieved": round(hbm_decode_bytes / (split_avg / 1000.0) / 1e9, 2),
                      "peak": peak, "unit": "GB/s",
-                     "frac": round(decode_bytes / (split_avg / 1000.0) / 1e9 / peak, 4),
-                     "traffic": profiled_traffic(),
-                     "algorithmic_bytes_per_launch": decode_bytes,
+                     "frac": round(hbm_decode_bytes / (split_avg / 1000.0) / 1e9 / peak, 4),
+                     "traffic": profiled_traffic() if args.workload == WORKLOAD_INDEX and not args.block_size else None,
+                     "algorithmic_bytes_per_launch": hbm_decode_bytes,
+                     "logical_bytes_per_launch": decode_bytes,
                      "avg_launch_ms": round(split_avg, 5), "merge_avg_ms": round(merge_avg, 5),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (3 + (1 if cow is not None else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
         "host_enqueue_s": round(enqueue_s, 4),
@@ -460,11 +495,16 @@ def run_e2e(args, st, spec, vals, copies, tables, lens, slots, scale, stream, de
         calls.append((binding.PreparedAppend(d_kn, d_vn, d_slot, kp, vp),
                       binding.PreparedDecode(d_q, kp, vp, d_tab, d_len, scale, out, ws), out))
 
+    cow = st.cow_pairs if st.cow_pairs.numel() else None
+
     def one(i):
         app, dec, out = calls[i % len(calls)]
         for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_tab, h_tab), (d_len, h_len),
                      (d_slot, h_slot)):
             d.copy_(h, non_blocking=True)
+        if cow is not None:
+            kp, vp = copies[i % len(copies)][:2]
+            binding.block_copy(cow, kp, vp, stream=stream)
         app(stream)
         dec(stream)
         h_out.copy_(out, non_blocking=True)
@@ -495,6 +535,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seqs", type=int, default=16)
     ap.add_argument("--launch", choices=["graph", "eager"], default="eager")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_INDEX,
+                    help="index of the workload (0 tiny, 1 Llama-3-8B-shaped [default], "
+                         "2 OPT-13B-shaped MHA, 3 agent swarm with prefix sharing, "
+                         "4 long-context 70B-shaped)")
+    ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size")
+    ap.add_argument("--dtype", choices=["f32", "f16", "bf16"], default=None,
+                    help="override the workload's K/V dtype")
+    ap.add_argument("--consumer", type=int, default=0,
+                    help="math path: 0 auto, 1 CUDA cores, 2 tensor cores (16-bit only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

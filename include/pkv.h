@@ -152,8 +152,9 @@ pkv_status pkv_decode_attention(const pkv_cache_desc *cache, const void *q, int3
  * for the defaults. */
 typedef struct {
     int32_t num_ctas;        /* CTAs of the split-K launch; 0 = SMs x occupancy */
-    int32_t consumer;        /* 0 auto; 1 CUDA-core (SIMT) math; 2 tensor-core
-                                mma (16-bit dtypes only)                        */
+    int32_t consumer;        /* 0 auto (tensor cores for fp16/bf16, CUDA cores
+                                for fp32); 1 CUDA-core (SIMT) math; 2 tensor-
+                                core mma (16-bit dtypes only)                   */
     void *timing_events[3];  /* optional cudaEvent_t recorded on `stream` before
                                 the split-K kernel, between it and the merge,
                                 and after the merge (NULL = not recorded); under

@@ -92,7 +92,10 @@ pkv_status make_plan(const pkv_cache_desc *c, int Hq, const pkv_decode_options *
     const bool half = c->dtype != PKV_F32;
     if (consumer == 2 && !half)
         return fail(PKV_ERR_UNSUPPORTED, "tensor-core math needs fp16 or bf16 K/V");
-    pl->mma = half && (consumer == 2 || (consumer == 0 && pl->G >= 3));
+    // 16-bit K/V go to the tensor cores whatever the group size: with one
+    // query head per KV head the SIMT path spends its time converting and
+    // reducing, the mma path (query heads padded to n = 8) stays HBM-bound
+    pl->mma = half && consumer != 1;
     if (pl->mma) {
         pl->gmax = pl->GC <= 8 ? 8 : 16;
     } else {

@@ -93,10 +93,12 @@ def test_gqa4_bf16_ragged_ctas(num_ctas):
 
 
 @pytest.mark.parametrize("consumer", [1, 2])
-@pytest.mark.parametrize("dtype,Hq,Hk", [("bf16", 32, 8), ("f16", 8, 8), ("f16", 16, 8),
-                                          ("bf16", 24, 8), ("bf16", 64, 8), ("f16", 40, 2)])
-def test_forced_consumers(consumer, dtype, Hq, Hk):
-    spec = W.WorkloadSpec("t", 5, Hq, Hk, 128, 16, dtype, 1.0)
+@pytest.mark.parametrize("dtype,Hq,Hk,D", [("bf16", 32, 8, 128), ("f16", 8, 8, 128),
+                                            ("f16", 16, 8, 128), ("bf16", 24, 8, 128),
+                                            ("bf16", 64, 8, 128), ("f16", 40, 2, 128),
+                                            ("f16", 4, 4, 64), ("bf16", 8, 4, 64)])
+def test_forced_consumers(consumer, dtype, Hq, Hk, D):
+    spec = W.WorkloadSpec("t", 5, Hq, Hk, D, 16, dtype, 1.0)
     st, vals = W.make_workload(spec, seed=2, lengths=[1, 40, 64, 333, 777])
     got, ref, _ = run_step(st, vals, out_dtype=torch.float32, consumer=consumer, num_ctas=9)
     assert_close(got, ref, dtype, f"consumer={consumer}")
