@@ -3,8 +3,9 @@
 One step = one decode step of the Llama-3-8B-shaped workload (64 sequences,
 32 q / 8 kv heads, head_dim 128, bf16, block size 16, context lengths
 U[512, 4096], blocks drawn at random from a pool of 1.2x the need): append of
-one new token per sequence, then split-K paged decode attention with its
-log-sum-exp merge — every kernel of the path, through the C ABI.
+one new token per sequence, then split-K paged decode attention whose
+log-sum-exp merge runs inside the same kernel — every kernel of the path,
+through the C ABI.
 
 Prints one JSON line (rank 0). `value` is algorithmic KV-cache GB/s of the
 whole step (bytes the method must move: every context token's K and V row,
@@ -288,7 +289,7 @@ def workload_config(spec, st):
                             + f" seed 0, sum {int(st.context_lens.sum())}",
             "pool_blocks": st.num_blocks,
             "step": ("pkv_block_copy (copy-on-write) + " if st.cow_pairs.numel() else "")
-                    + "pkv_append + pkv_decode_attention (split-K + merge)"}
+                    + "pkv_append + pkv_decode_attention (split-K with in-kernel merge)"}
 
 
 # ------------------------------------------------------------------ our arm
@@ -366,14 +367,14 @@ def run_ours(args):
     stride = max(1, args.steps // 200)
     kev = {}
     for i in range(0, args.steps, stride):
-        trio = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        for e in trio:
+        pair = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        for e in pair:
             e.record(stream)            # materialise the CUDA event handle
-        kev[i] = trio
+        kev[i] = pair
     torch.cuda.synchronize()
 
     if args.launch == "graph":
-        # each step replays a captured graph of the same three kernel launches
+        # each step replays a captured graph of the same kernel launches
         def capture(i, evs):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, capture_error_mode="thread_local"):
@@ -416,9 +417,7 @@ def run_ours(args):
     ms = t_start.elapsed_time(t_end)
     ms_max = reduce_max(ms, world, dev)
     split_ms = [kev[i][0].elapsed_time(kev[i][1]) for i in kev]
-    merge_ms = [kev[i][1].elapsed_time(kev[i][2]) for i in kev]
     split_avg = sum(split_ms) / len(split_ms)
-    merge_avg = sum(merge_ms) / len(merge_ms)
     if binding.get_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
@@ -440,7 +439,7 @@ def run_ours(args):
                    "l2": f"inputs > L2: the step cycles through {len(copies)} resident copies "
                          f"of the cache ({len(copies)} x {2 * st.num_blocks * spec.num_kv_heads * spec.block_size * spec.head_dim * 2 / 1e9:.2f} GB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "launch": "CUDA-graph replay of the step's three kernel launches (captured through the C ABI)"
+                   "launch": "CUDA-graph replay of the step's kernel launches (captured through the C ABI)"
                              if args.launch == "graph" else "eager C-ABI calls"},
         "seq_tokens_per_s": round(seq_tok, 1),
         "hbm_frac_of_measured": round(value / peak / world, 4),
@@ -451,9 +450,9 @@ def run_ours(args):
                      "traffic": profiled_traffic() if args.workload == WORKLOAD_INDEX and not args.block_size else None,
                      "algorithmic_bytes_per_launch": hbm_decode_bytes,
                      "logical_bytes_per_launch": decode_bytes,
-                     "avg_launch_ms": round(split_avg, 5), "merge_avg_ms": round(merge_avg, 5),
+                     "avg_launch_ms": round(split_avg, 5),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
-        "gpu_launches": (3 + (1 if cow is not None else 0)) * args.steps,
+        "gpu_launches": (2 + (1 if cow is not None else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
         "host_enqueue_s": round(enqueue_s, 4),

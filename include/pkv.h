@@ -138,7 +138,12 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc *cache, int32_t num_seqs,
  * set PKV_DEVERR_BLOCK_ID and read as zeros.
  * workspace: device memory of at least pkv_decode_workspace_bytes(...) bytes,
  * 16-byte aligned, owned by the caller, reused by every call on `stream`
- * (two streams need two workspaces). Its contents need no initialisation.
+ * (two streams need two workspaces). It must be zero-filled before the first
+ * call that uses it (e.g. one cudaMemsetAsync after allocating): it holds the
+ * arrival counters that let the last CTA holding a piece of a split unit
+ * merge the pieces, and every call puts them back to zero. After a call whose
+ * device error word reports PKV_DEVERR_TIMEOUT some counters may be left
+ * non-zero: zero the workspace again before reusing it.
  * num_q_heads must be a multiple of num_kv_heads. num_seqs == 0 is a no-op.
  */
 pkv_status pkv_decode_attention(const pkv_cache_desc *cache, const void *q, int32_t num_seqs,
@@ -148,17 +153,24 @@ pkv_status pkv_decode_attention(const pkv_cache_desc *cache, const void *q, int3
                                 int32_t out_dtype, void *workspace, size_t workspace_bytes,
                                 void *stream);
 
+/* Largest num_ctas of pkv_decode_options. The workspace begins with a fixed
+ * region of PKV_MAX_DECODE_CTAS x 16 bytes of arrival counters, whatever the
+ * launch, so one zero-filled workspace serves launches of any CTA count. */
+#define PKV_MAX_DECODE_CTAS 4096
+
 /* Tuning and measurement options for pkv_decode_attention_ex. Zero-initialise
  * for the defaults. */
 typedef struct {
-    int32_t num_ctas;        /* CTAs of the split-K launch; 0 = SMs x occupancy */
+    int32_t num_ctas;        /* CTAs of the split-K launch, 0..PKV_MAX_DECODE_CTAS;
+                                0 = SMs x occupancy                             */
     int32_t consumer;        /* 0 auto (tensor cores for fp16/bf16, CUDA cores
                                 for fp32); 1 CUDA-core (SIMT) math; 2 tensor-
                                 core mma (16-bit dtypes only)                   */
-    void *timing_events[3];  /* optional cudaEvent_t recorded on `stream` before
-                                the split-K kernel, between it and the merge,
-                                and after the merge (NULL = not recorded); under
-                                stream capture they become event-record nodes */
+    void *timing_events[2];  /* optional cudaEvent_t recorded on `stream` just
+                                before and just after the decode kernel of the
+                                first 1024 sequences (NULL = not recorded);
+                                under stream capture they become event-record
+                                nodes */
 } pkv_decode_options;
 
 /* Workspace bytes for pkv_decode_attention_ex with options->num_ctas = num_ctas
@@ -188,14 +200,17 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
  * loads the library holds it until the process exits). It allocates nothing.
  *
  * It launches one split-K CTA per SM; a shape whose scratch need exceeds
- * PKV_STATIC_SCRATCH_BYTES (need = SMs x (32 + 8 x heads-per-unit x
- * (head_dim + 1)) bytes, heads-per-unit = min(16, num_q_heads/num_kv_heads))
+ * PKV_STATIC_SCRATCH_BYTES (need = 16 x PKV_MAX_DECODE_CTAS + SMs x 8 x
+ * heads-per-unit x (head_dim + 4) bytes, heads-per-unit = min(16,
+ * num_q_heads/num_kv_heads))
  * is rejected with PKV_ERR_WORKSPACE and nothing is enqueued.
  * The first call on a device finds the scratch array's device address (once
  * per device, with that device current); make that first call before any
- * stream capture. All calls on a device share the array and it keeps the last
- * call's contents; nothing in it needs clearing, but calls whose kernels
- * overlap on the GPU race on it, so order them (e.g. one stream).
+ * stream capture. All calls on a device share the array. It starts zeroed and
+ * every call leaves its arrival counters zero, so it needs no clearing; when
+ * pkv_get_error reports PKV_DEVERR_TIMEOUT it zeroes the array of the current
+ * device again. Calls whose kernels overlap on the GPU race on it, so order
+ * them (e.g. one stream).
  */
 #define PKV_STATIC_SCRATCH_BYTES (2u << 20)
 pkv_status pkv_decode_attention_static(const pkv_cache_desc *cache, const void *q,
@@ -227,7 +242,9 @@ pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pa
  * pkv_get_error — synchronise `stream`, then read and clear the device error
  * word of the current device (PKV_DEVERR_* bits) into *device_error_word.
  * Returns PKV_OK when the word was zero, PKV_ERR_OUT_OF_RANGE or
- * PKV_ERR_TIMEOUT (when that bit is set) otherwise.
+ * PKV_ERR_TIMEOUT (when that bit is set) otherwise. On PKV_DEVERR_TIMEOUT it
+ * also zeroes pkv_decode_attention_static's scratch on the current device
+ * (synchronously); caller-owned workspaces are the caller's to zero.
  */
 pkv_status pkv_get_error(int32_t *device_error_word, void *stream);
 

@@ -31,7 +31,7 @@ class CacheDesc(ctypes.Structure):
 
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int32), ("consumer", ctypes.c_int32),
-                ("timing_events", ctypes.c_void_p * 3)]
+                ("timing_events", ctypes.c_void_p * 2)]
 
 
 class PkvError(RuntimeError):
@@ -127,10 +127,12 @@ def workspace_bytes(k_pool, num_q_heads: int, num_ctas: int = 0) -> int:
 
 
 def alloc_workspace(k_pool, num_q_heads: int, num_ctas: int = 0) -> torch.Tensor:
+    """Split-K workspace, zero-filled as the library requires before first use
+    (its arrival counters; every call leaves them zero again)."""
     n = workspace_bytes(k_pool, num_q_heads, num_ctas)
     if n == 0:
         raise PkvError(-1, "workspace size query failed")
-    return torch.empty(n, dtype=torch.uint8, device=k_pool.device)
+    return torch.zeros(n, dtype=torch.uint8, device=k_pool.device)
 
 
 def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float,
@@ -197,7 +199,7 @@ class PreparedDecode:
 
     def __call__(self, stream, timing_events: Optional[Sequence] = None) -> None:
         opts = self._opts
-        for i in range(3):
+        for i in range(2):
             ev = timing_events[i] if timing_events is not None else None
             opts.timing_events[i] = None if ev is None else ev.cuda_event
         _check(self._fn(*self._args, _stream(stream), ctypes.byref(opts)))

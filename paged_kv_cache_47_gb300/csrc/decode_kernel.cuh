@@ -83,7 +83,7 @@ struct SplitCfg {
 };
 
 // ---------------------------------------------------------------------------
-// per-sequence tile prefix, shared by the split-K and merge kernels
+// per-sequence tile prefix
 // ---------------------------------------------------------------------------
 // seq_len[s]   = context length clamped to [0, M*B] (a clamp flags the error word)
 // seq_prefix[s]= U * sum_{s'<s} ceil(seq_len[s'] / 64), seq_prefix[S] = NT
@@ -117,35 +117,6 @@ __device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq
         if (lane == 0) seq_prefix[p.S] = running;
     }
     __syncthreads();
-}
-
-// Position in the flattened tile space.
-struct Cursor {
-    int s, u, ti, n, L;
-};
-
-__device__ __forceinline__ void cursor_at(Cursor &c, int64_t tau, const int *seq_prefix,
-                                          const int *seq_len, int S) {
-    c.s = pkv_find_seq(seq_prefix, S, tau);
-    c.L = seq_len[c.s];
-    c.n = pkv_tiles_of_len(c.L);
-    const int off = (int)(tau - seq_prefix[c.s]);
-    c.u = off / c.n;
-    c.ti = off - c.u * c.n;
-}
-
-__device__ __forceinline__ void cursor_next(Cursor &c, const int *seq_len, int S, int U) {
-    if (++c.ti < c.n) return;
-    c.ti = 0;
-    if (++c.u < U) return;
-    c.u = 0;
-    do {
-        ++c.s;
-    } while (c.s < S && seq_len[c.s] == 0);
-    if (c.s < S) {
-        c.L = seq_len[c.s];
-        c.n = pkv_tiles_of_len(c.L);
-    }
 }
 
 // Swizzled shared-memory address of 16-byte chunk `chunk` (0..8*NP-1) of row r
@@ -507,6 +478,77 @@ struct Consumer<T, D, GMAX, true> {
 };
 
 // ---------------------------------------------------------------------------
+// log-sum-exp merge of one warp's slice of a unit cut by CTA boundaries
+// ---------------------------------------------------------------------------
+// The partials of the unit come from CTAs c_first .. c_last (those with an
+// empty tile range hold none); the first of them used slot
+// pkv_partial_slot(c_first, ...), the later ones slot 0. With the partials'
+// log2-sum-exp2 values lse_p and normalised outputs o_p,
+//     lse = log2 sum_p 2^{lse_p},   out = sum_p 2^{lse_p - lse} o_p,
+// taken in CTA order with a running maximum (one pass). Loads bypass L1: the
+// other CTAs' slices were written during this launch.
+template <int D, int GMAX>
+__device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMeta &mt,
+                                            int c_first, int warp, int lane, int64_t NT) {
+    // the lane's elements are idx = warp*32 + lane + 128k, k < EPL, taken in
+    // chunks of KC: all loads of one partial for a chunk are issued before
+    // any of them is used, and at most KC elements are live at a time
+    constexpr int EPL = (GMAX * D + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+    constexpr int KC = EPL < 8 ? EPL : 8;
+    const int C = p.C;
+    const int n_el = mt.gca * D;
+    const int c_last = pkv_owner((int64_t)mt.tu + mt.nu - 1, C, NT);
+    const int slot_first = pkv_partial_slot(c_first, C, NT, mt.tu);
+#pragma unroll 1
+    for (int k0 = 0; k0 < EPL; k0 += KC) {
+        if (warp * 32 + k0 * kConsumerWarps * 32 >= n_el) break;
+        float Mx[KC], W[KC], O[KC];
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            Mx[k] = -CUDART_INF_F;
+            W[k] = 0.f;
+            O[k] = 0.f;
+        }
+#pragma unroll 2
+        for (int c = c_first; c <= c_last; ++c) {
+            if (pkv_cta_empty(c, C, NT)) continue;
+            const int slot = c * 2 + (c == c_first ? slot_first : 0);
+            // lane h < gca fetches this warp's copy of head h's lse
+            const float lse_h =
+                lane < mt.gca ? __ldcg(p.ws_lse + (slot * kConsumerWarps + warp) * p.GC + lane)
+                              : 0.f;
+            float o[KC];
+#pragma unroll
+            for (int k = 0; k < KC; ++k) {
+                const int idx = warp * 32 + lane + (k0 + k) * kConsumerWarps * 32;
+                const int j = idx / D, d = idx - (idx / D) * D;
+                o[k] = idx < n_el ? __ldcg(p.ws_o + (size_t)(slot * p.GC + j) * D + d) : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < KC; ++k) {
+                // head of element k0 + k: the same for every lane of the warp
+                const int j = (warp * 32 + (k0 + k) * kConsumerWarps * 32) / D;
+                const float lse = __shfl_sync(0xffffffffu, lse_h, j & 31);
+                const float mn = fmaxf(Mx[k], lse);
+                const float a = exp2f(Mx[k] - mn), w = exp2f(lse - mn);
+                W[k] = W[k] * a + w;
+                O[k] = O[k] * a + w * o[k];
+                Mx[k] = mn;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            const int idx = warp * 32 + lane + (k0 + k) * kConsumerWarps * 32;
+            if (idx < n_el) {
+                const int j = idx / D, d = idx - (idx / D) * D;
+                store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype,
+                          O[k] / W[k]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // the split-K kernel
 // ---------------------------------------------------------------------------
 template <typename T, int D, int GMAX, bool MMA>
@@ -556,31 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t NT = seq_prefix[p.S];
     const int64_t t_begin = NT ? pkv_split(cta, C, NT) : 0, t_end = NT ? pkv_split(cta + 1, C, NT) : 0;
     const int n_my = (int)(t_end - t_begin);
-    // merge descriptor of boundary cta+1: set when this CTA's last segment is
-    // the start of a unit that continues into later CTAs (this CTA is the
-    // unit's first owner), else marked empty
-    if (tid == 0 && cta + 1 < C) {
-        MergeDesc md;
-        md.s = -1;
-        md.h0 = md.gca = md.slot_first = md.c_last = 0;
-        md.nt = (int)NT;
-        md.pad0 = md.pad1 = 0;
-        if (n_my > 0) {
-            Cursor c;
-            cursor_at(c, t_end - 1, seq_prefix, seq_len, p.S);
-            const int64_t T_u = (int64_t)seq_prefix[c.s] + (int64_t)c.u * c.n;
-            if (T_u >= t_begin && T_u + c.n > t_end) {
-                const int g = c.u / p.NC, chunk = c.u - (c.u / p.NC) * p.NC;
-                md.s = c.s;
-                md.h0 = g * p.G + chunk * p.GC;
-                md.gca = min(p.GC, p.G - chunk * p.GC);
-                md.slot_first = pkv_partial_slot(cta, C, NT, T_u);
-                md.c_last = pkv_owner(T_u + c.n - 1, C, NT);
-            }
-        }
-        p.ws_desc[cta + 1] = md;
-    }
-    grid_dependents_launch();   // the merge kernel may start its launch now
+    grid_dependents_launch();   // the next kernel on the stream may start its launch now
     if (n_my <= 0) return;
 
     if (warp >= kConsumerWarps) {
@@ -602,10 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tb = pt - jblk * tpb;
         const uint8_t *kpool = static_cast<const uint8_t *>(p.kp);
         const uint8_t *vpool = static_cast<const uint8_t *>(p.vp);
-        Cursor cur, la;
-        cursor_at(cur, t_begin, seq_prefix, seq_len, p.S);
+        PkvCursor cur, la;
+        pkv_cursor_at(cur, t_begin, seq_prefix, seq_len, p.S);
         la = cur;
-        auto load_entry = [&](const Cursor &c) -> int {
+        auto load_entry = [&](const PkvCursor &c) -> int {
             const int ntok = min(PKV_TILE_TOKENS, c.L - c.ti * PKV_TILE_TOKENS);
             if (jblk * p.B >= ntok) return -1;
             return __ldg(p.block_tables + (size_t)c.s * p.M + c.ti * bpt + jblk);
@@ -616,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ent[k] = -1;
             if (k < n_my) {
                 ent[k] = load_entry(la);
-                cursor_next(la, seq_len, p.S, p.U);
+                pkv_cursor_next(la, seq_len, p.S, p.U);
             }
         }
         bool ok = true;
@@ -628,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int e = ent[k];
                 if (it + LA < n_my) {
                     ent[k] = load_entry(la);
-                    cursor_next(la, seq_len, p.S, p.U);
+                    pkv_cursor_next(la, seq_len, p.S, p.U);
                 }
                 const int stage = it % Cfg::NST;
                 const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
@@ -679,11 +697,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mt.ntok = ntok;
                     mt.flags = (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0);
                     mt.slot = T_u > t_begin ? 1 : 0;
-                    mt.pad0 = mt.pad1 = 0;
+                    mt.tu = (int)T_u;
+                    mt.nu = cur.n;
                     meta[stage] = mt;
                     mbar_arrive(full);   // release: the record is visible with the data
                 }
-                cursor_next(cur, seq_len, p.S, p.U);
+                pkv_cursor_next(cur, seq_len, p.S, p.U);
             }
         }
         cp_async_wait_all();   // this thread's copies land before it exits
@@ -695,6 +714,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (MMA) cs.pbuf = sbase + Cfg::OFF_PBUF + warp * Cfg::NTN * 512;
     cs.reset();
     int seg = 0;
+    // Cut segments whose partial this warp has written (the range's first and
+    // last segment at most). Counting them waits until the CTA's tiles are
+    // done: the fence that must come before a count would otherwise wait
+    // behind the copies in flight and stall the math warps mid-run.
+    TileMeta pend[2];
+    int n_pend = 0;
     for (int it = 0; it < n_my; ++it) {
         const int stage = it % Cfg::NST;
         const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
@@ -718,6 +743,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(comb_full);
             if (!mbar_wait(comb_full, (uint32_t)seg & 1u, p.err)) return;
             const int base = (cta * 2 + mt.slot) * p.GC;
+            const bool whole = (mt.flags & kWhole) != 0;
+            // warp `warp` owns the elements idx = warp*32 + lane + 128k of the
+            // unit's gca x D outputs (head j = idx / D, element d = idx % D)
             for (int idx = warp * 32 + lane; idx < mt.gca * D; idx += kConsumerWarps * 32) {
                 const int j = idx / D, d = idx - (idx / D) * D;
                 float M = -CUDART_INF_F;
@@ -731,78 +759,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     O = fmaf(wt, comb_o[(w * GMAX + j) * D + d], O);
                 }
                 const float o = O / Ls;
-                if (mt.flags & kWhole) {
+                if (whole) {
                     store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype, o);
                 } else {
                     p.ws_o[(size_t)(base + j) * D + d] = o;
-                    if (d == 0) p.ws_lse[base + j] = M + log2f(Ls);
+                    // lane 0 holds one element of every head in the slice:
+                    // it writes the slice's copy of the head's lse
+                    if (lane == 0)
+                        p.ws_lse[((cta * 2 + mt.slot) * kConsumerWarps + warp) * p.GC + j] =
+                            M + log2f(Ls);
                 }
             }
+            if (!whole && warp * 32 < mt.gca * D) pend[n_pend++] = mt;
             __syncwarp();
             if (lane == 0) mbar_arrive(comb_empty);
             ++seg;
         }
     }
-}
-
-// ---------------------------------------------------------------------------
-// log-sum-exp merge of partials of units cut by CTA boundaries
-// ---------------------------------------------------------------------------
-// Block j (1 <= j < C) merges the unit described by descriptor j (written by
-// split-K CTA j-1 when that unit starts in its range and runs past it):
-//   lse = log2 sum_p 2^{lse_p},  out = sum_p 2^{lse_p - lse} o_p
-// over the partials of CTAs j-1 .. c_last, in that order, with a running max
-// (one pass). CTAs with an empty tile range wrote nothing and are skipped.
-// Thread t owns element d = t % D of heads t / D, t / D + 128 / D, ...; all
-// loads of one partial are independent, so the merge costs about two memory
-// round trips (descriptor, then partials).
-template <int D>
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const DecodeParams p) {
-    constexpr int HPT = kMaxHeadsPerUnit * D / kMergeThreads;  // heads per thread (max)
-    constexpr int HSTEP = kMergeThreads / D;
-    grid_dependents_launch();  // the next kernel (e.g. the next append) may be scheduled
-    grid_dependency_wait();    // partials come from the split-K kernel just before
-    const int j = blockIdx.x + 1;
-    const MergeDesc md = p.ws_desc[j];
-    if (md.s < 0) return;
-    const int C = p.C;
-    const int64_t NT = md.nt;
-    const int c_first = j - 1;
-    const int d = threadIdx.x % D;
-    const int h_first = threadIdx.x / D;
-    float M[HPT], W[HPT], O[HPT];
-#pragma unroll
-    for (int k = 0; k < HPT; ++k) {
-        M[k] = -CUDART_INF_F;
-        W[k] = 0.f;
-        O[k] = 0.f;
+    if (n_pend == 0) return;
+    // Count this warp's slices of its cut segments; for each unit, the last of
+    // its partials to arrive merges the slice. Lane 0 releases the whole
+    // warp's stores (ordered before it by __syncwarp) with its counts and
+    // acquires the other partials with them.
+    __syncwarp();
+    unsigned prev[2] = {0u, 0u};
+    if (lane == 0) {
+        fence_acq_rel_gpu();
+        for (int i = 0; i < n_pend; ++i)
+            prev[i] = atomicAdd(p.ws_cnt + pkv_owner(pend[i].tu, C, NT) * kConsumerWarps + warp, 1u);
+        fence_acq_rel_gpu();
     }
-#pragma unroll 2
-    for (int c = c_first; c <= md.c_last; ++c) {
-        if (pkv_cta_empty(c, C, NT)) continue;
-        const int slot = c == c_first ? md.slot_first : 0;
-        const int b0 = (c * 2 + slot) * p.GC;
-        float lse[HPT], o[HPT];
-#pragma unroll
-        for (int k = 0; k < HPT; ++k) {
-            const int h = h_first + k * HSTEP;
-            lse[k] = h < md.gca ? p.ws_lse[b0 + h] : -CUDART_INF_F;
-            o[k] = h < md.gca ? p.ws_o[(size_t)(b0 + h) * D + d] : 0.f;
+    __syncwarp();
+    for (int i = 0; i < n_pend; ++i) {
+        const TileMeta &mt = pend[i];
+        const int c_first = pkv_owner(mt.tu, C, NT);
+        if ((int)__shfl_sync(0xffffffffu, prev[i], 0) + 1 == pkv_unit_parts(mt.tu, mt.nu, C, NT)) {
+            if (lane == 0) p.ws_cnt[c_first * kConsumerWarps + warp] = 0u;   // for the next call
+            merge_slice<D, GMAX>(p, mt, c_first, warp, lane, NT);
         }
-#pragma unroll
-        for (int k = 0; k < HPT; ++k) {
-            const float mn = fmaxf(M[k], lse[k]);
-            const float a = exp2f(M[k] - mn), w = exp2f(lse[k] - mn);
-            W[k] = W[k] * a + w;
-            O[k] = O[k] * a + w * o[k];
-            M[k] = mn;
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < HPT; ++k) {
-        const int h = h_first + k * HSTEP;
-        if (h < md.gca)
-            store_out(p.out, ((size_t)md.s * p.Hq + md.h0 + h) * D + d, p.out_dtype, O[k] / W[k]);
     }
 }
 

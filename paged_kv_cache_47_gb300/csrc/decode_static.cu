@@ -9,12 +9,15 @@
 // memory, declared below. Every GPU that loads the library keeps that array
 // for the life of the process.
 //
-// The array is shared by every call on a device and keeps whatever the last
-// call left in it. The kernels write each merge descriptor and partial before
-// they read it, so nothing in the array has to be cleared between calls; but
-// two calls whose kernels overlap on the GPU (different streams, or unordered
-// graph branches) would use the same bytes at the same time and race, so
-// order such calls (for example, issue them on one stream).
+// The array is shared by every call on a device. Its first bytes are the
+// split-K arrival counters, which must read zero when a call starts: a
+// __device__ array starts zeroed and every call that completes puts the
+// counters back to zero, so nothing has to be cleared between calls. A call
+// whose kernel gave up on a timed-out wait can leave counters set; the error
+// reader then zeroes the array (clear_static_scratch). Two calls whose kernels
+// overlap on the GPU (different streams, or unordered graph branches) would
+// use the same bytes at the same time and race, so order such calls (for
+// example, issue them on one stream).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -62,6 +65,21 @@ pkv_status scratch_for_current_device(void **ptr, int *sms) {
 }
 
 }  // namespace
+
+namespace pkv {
+// Zero the scratch array of the current device if a call has used it there.
+cudaError_t clear_static_scratch() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return e;
+    void *p = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_scratch_mu);
+        p = g_scratch_ptr[dev];
+    }
+    return p ? cudaMemset(p, 0, PKV_STATIC_SCRATCH_BYTES) : cudaSuccess;
+}
+}  // namespace pkv
 
 extern "C" pkv_status pkv_decode_attention_static(
     const pkv_cache_desc *cache, const void *q, int32_t num_seqs, int32_t num_q_heads,

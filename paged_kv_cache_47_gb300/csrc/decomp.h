@@ -16,8 +16,9 @@
 // split(c) = floor(c * NT / C) ("stream-K"): every CTA gets the same number of
 // tiles to within one, whatever the spread of context lengths, so no CTA waits
 // on a long sequence. A unit cut by a CTA boundary yields one partial result
-// per CTA that touches it; partials are merged by log-sum-exp afterwards.
-// A unit entirely inside one CTA range is finished by that CTA directly.
+// per CTA that touches it; the CTA that writes the last of them (found with
+// an arrival counter per unit) merges them by log-sum-exp. A unit entirely
+// inside one CTA range is finished by that CTA directly.
 //
 // Partial slots: each CTA owns two partial slots. Its first segment (which
 // may continue a unit from the previous CTA) uses slot 0; its last segment,
@@ -57,6 +58,15 @@ PKV_HD int pkv_partial_slot(int c, int C, int64_t NT, int64_t unit_start) {
     return unit_start > pkv_split(c, C, NT) ? 1 : 0;
 }
 
+// Number of partials of the unit of n tiles starting at tile T (the CTAs
+// whose range meets [T, T + n)). With NT >= C every CTA has at least one tile,
+// so they are all CTAs from owner(T) to owner(T + n - 1); with NT < C every
+// CTA has at most one tile, so there is one CTA per tile.
+PKV_HD int pkv_unit_parts(int64_t T, int n, int C, int64_t NT) {
+    if (NT < C) return n;
+    return pkv_owner(T + n - 1, C, NT) - pkv_owner(T, C, NT) + 1;
+}
+
 // Clamp a device-provided context length to [0, max_len]; sets *bad on clamp.
 PKV_HD int pkv_clamp_len(int L, int max_len, int *bad) {
     if (L < 0) { *bad = 1; return 0; }
@@ -73,4 +83,36 @@ PKV_HD int pkv_find_seq(const int *seq_prefix, int S, int64_t tau) {
         if ((int64_t)seq_prefix[mid] <= tau) lo = mid; else hi = mid;
     }
     return lo;
+}
+
+// Position of tile tau in the flattened tile space: sequence s (context L,
+// n tiles per unit), unit u of the sequence, tile ti of the unit.
+struct PkvCursor {
+    int s, u, ti, n, L;
+};
+
+PKV_HD void pkv_cursor_at(PkvCursor &c, int64_t tau, const int *seq_prefix, const int *seq_len,
+                          int S) {
+    c.s = pkv_find_seq(seq_prefix, S, tau);
+    c.L = seq_len[c.s];
+    c.n = pkv_tiles_of_len(c.L);
+    const int off = (int)(tau - seq_prefix[c.s]);
+    c.u = off / c.n;
+    c.ti = off - c.u * c.n;
+}
+
+// The next tile in flat order, skipping sequences with no tiles. Past the
+// last tile c.s becomes S and the other fields are left as they were.
+PKV_HD void pkv_cursor_next(PkvCursor &c, const int *seq_len, int S, int U) {
+    if (++c.ti < c.n) return;
+    c.ti = 0;
+    if (++c.u < U) return;
+    c.u = 0;
+    do {
+        ++c.s;
+    } while (c.s < S && seq_len[c.s] == 0);
+    if (c.s < S) {
+        c.L = seq_len[c.s];
+        c.n = pkv_tiles_of_len(c.L);
+    }
 }

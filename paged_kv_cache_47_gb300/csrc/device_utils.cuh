@@ -79,6 +79,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
 // Wait until the preceding kernel on the stream has completed and its memory
 // is visible (a no-op when this kernel was launched without programmatic
 // serialisation).
+// Acquire-release fence at GPU scope: orders this thread's (and, through a
+// preceding __syncwarp, its warp's) earlier memory accesses before later ones
+// for every thread of the GPU.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }

@@ -139,10 +139,14 @@ pkv_status default_ctas(const Plan &pl, int *C) {
     return PKV_OK;
 }
 
-// workspace: [C] merge descriptors, then [C][2][GC][D] partial outputs, then
-// [C][2][GC] partial log2-sum-exp2 values
+// workspace: [PKV_MAX_DECODE_CTAS][4] arrival counters (a fixed region, so
+// that no launch's partials ever land where a launch with more CTAs keeps its
+// counters), then [C][2][GC][D] partial outputs, then [C][2][4][GC] partial
+// log2-sum-exp2 values (one copy per math warp)
+constexpr size_t kCounterBytes = (size_t)PKV_MAX_DECODE_CTAS * pkv::kConsumerWarps * sizeof(unsigned);
 size_t workspace_for(int C, int GC, int D) {
-    return (size_t)C * sizeof(pkv::MergeDesc) + (size_t)C * 2 * GC * (size_t)(D + 1) * sizeof(float);
+    const size_t W = pkv::kConsumerWarps;
+    return kCounterBytes + (size_t)C * 2 * GC * (D + W) * sizeof(float);
 }
 
 pkv_status max_default_ctas(int *C) {
@@ -260,7 +264,9 @@ pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pa
 size_t pkv_decode_workspace_bytes_ex(const pkv_cache_desc *cache, int32_t num_q_heads,
                                      int32_t num_ctas) {
     if (check_cache(cache) != PKV_OK) return 0;
-    if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0 || num_ctas < 0) return 0;
+    if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0 || num_ctas < 0 ||
+        num_ctas > PKV_MAX_DECODE_CTAS)
+        return 0;
     int C = num_ctas;
     if (C == 0 && max_default_ctas(&C) != PKV_OK) return 0;
     const int G = num_q_heads / cache->num_kv_heads;
@@ -305,7 +311,8 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
         return fail(PKV_ERR_UNSUPPORTED, "batch x context too large for one launch");
 
     int C = options ? options->num_ctas : 0;
-    if (C < 0) return fail(PKV_ERR_INVALID_ARG, "num_ctas %d", C);
+    if (C < 0 || C > PKV_MAX_DECODE_CTAS)
+        return fail(PKV_ERR_INVALID_ARG, "num_ctas %d outside [0, %d]", C, PKV_MAX_DECODE_CTAS);
     if (C == 0 && (st = default_ctas(pl, &C)) != PKV_OK) return st;
     const size_t need = workspace_for(C, pl.GC, cache->head_dim);
     if (C > 1 && (!workspace || workspace_bytes < need))
@@ -321,9 +328,9 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
     const int es = elem_bytes(cache->dtype);
     const int oes = elem_bytes(out_dtype);
     const int D = cache->head_dim;
-    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    cudaEvent_t ev[2] = {nullptr, nullptr};
     if (options)
-        for (int i = 0; i < 3; ++i) ev[i] = static_cast<cudaEvent_t>(options->timing_events[i]);
+        for (int i = 0; i < 2; ++i) ev[i] = static_cast<cudaEvent_t>(options->timing_events[i]);
 
     for (int s0 = 0; s0 < num_seqs; s0 += pkv::kMaxSeqsPerLaunch) {
         const int S = num_seqs - s0 < pkv::kMaxSeqsPerLaunch ? num_seqs - s0 : pkv::kMaxSeqsPerLaunch;
@@ -344,8 +351,10 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
         p.B = cache->block_size;
         p.NB = cache->num_blocks;
         p.scale_log2 = scale * 1.4426950408889634f;
-        p.ws_desc = static_cast<pkv::MergeDesc *>(workspace);
-        p.ws_o = workspace ? reinterpret_cast<float *>(p.ws_desc + C) : nullptr;
+        p.ws_cnt = static_cast<unsigned *>(workspace);
+        p.ws_o = workspace ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                                       kCounterBytes)
+                           : nullptr;
         p.ws_lse = workspace ? p.ws_o + (size_t)C * 2 * pl.GC * D : nullptr;
         p.C = C;
         p.err = err;
@@ -358,9 +367,6 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
         if ((e = pl.variant->launch(p, s)) != cudaSuccess)
             return cuda_fail(e, "split-K decode launch");
         if (first && ev[1] && (e = record_timing_event(ev[1], s)) != cudaSuccess)
-            return cuda_fail(e, "cudaEventRecord");
-        if ((e = pkv::launch_merge(p, D, s)) != cudaSuccess) return cuda_fail(e, "merge launch");
-        if (first && ev[2] && (e = record_timing_event(ev[2], s)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
     }
     return PKV_OK;
@@ -389,7 +395,12 @@ pkv_status pkv_get_error(int32_t *device_error_word, void *stream) {
     if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
     *device_error_word = (int32_t)w;
     if (w == 0) return PKV_OK;
-    if (w & PKV_DEVERR_TIMEOUT) return fail(PKV_ERR_TIMEOUT, "device error word 0x%x", w);
+    if (w & PKV_DEVERR_TIMEOUT) {
+        // a kernel that gave up may have left split-K arrival counters set
+        if ((e = pkv::clear_static_scratch()) != cudaSuccess)
+            return cuda_fail(e, "zeroing the static scratch");
+        return fail(PKV_ERR_TIMEOUT, "device error word 0x%x", w);
+    }
     return fail(PKV_ERR_OUT_OF_RANGE, "device error word 0x%x", w);
 }
 

@@ -13,7 +13,6 @@ constexpr int kConsumerWarps = 4;                  // math warps of the split-K 
 constexpr int kProducerWarps = 4;                  // gather (cp.async) warps
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
-constexpr int kMergeThreads = 128;
 constexpr int kMaxSeqsPerLaunch = 1024;            // larger batches are launched in chunks
 constexpr int kMaxCtasPerSm = 2;                   // cap used to size the workspace
 constexpr int kMaxHeadsPerUnit = 16;               // q heads carried by one work unit
@@ -26,21 +25,12 @@ struct TileMeta {
     int ntok;    // valid tokens in this tile (1..64)
     int flags;   // kFirst | kLast | kWhole
     int slot;    // partial slot (0/1) when the segment is not a whole unit
-    int pad0, pad1;
+    int tu;      // first tile of the unit (flattened tile index of the launch)
+    int nu;      // tiles of the unit
 };
 constexpr int kFirst = 1;  // first tile of this CTA's segment of a unit
 constexpr int kLast = 2;   // last tile of this CTA's segment of a unit
 constexpr int kWhole = 4;  // the segment is the whole unit: write the output directly
-
-// Written by split-K CTA j-1 for the merge block of boundary j.
-struct MergeDesc {
-    int s;           // sequence, or -1 when boundary j cuts no unit it starts
-    int h0, gca;     // q heads of the unit
-    int slot_first;  // partial slot used by CTA j-1
-    int c_last;      // last CTA holding a partial of the unit
-    int nt;          // total tiles of the launch
-    int pad0, pad1;
-};
 
 struct DecodeParams {
     const void *q;              // [S][Hq][D]
@@ -53,9 +43,16 @@ struct DecodeParams {
     int NC, GC, U;              // head chunks per kv head, heads per chunk, units per seq
     int B, NB;                  // block size, physical blocks
     float scale_log2;           // scale * log2(e)
+    // Split-K workspace. A unit cut by CTA boundaries is indexed by its first
+    // owner c_first (a CTA starts at most one unit that runs past its range).
+    // Math warp w of each CTA holding a partial owns a fixed slice of the
+    // unit's (head, d) elements: it writes that slice, then counts itself in
+    // ws_cnt[c_first][w]; the warp that arrives last merges the slice over
+    // all partials and puts the counter back to zero.
+    unsigned *ws_cnt;           // [C][kConsumerWarps] arrival counters, zero between calls
     float *ws_o;                // [C][2][GC][D] partial outputs (normalised)
-    float *ws_lse;              // [C][2][GC]     partial log2-sum-exp2
-    MergeDesc *ws_desc;         // [C]            merge descriptors
+    float *ws_lse;              // [C][2][kConsumerWarps][GC] partial log2-sum-exp2, one
+                                //                copy per owning warp
     int C;                      // CTAs of the split-K launch
     unsigned *err;              // device error word
     const void *kp, *vp;        // pools [NB][Hk][B][D]
@@ -76,7 +73,9 @@ const DecodeVariant *find_variant_f32(int D, int gmax, bool mma);
 const DecodeVariant *find_variant_f16(int D, int gmax, bool mma);
 const DecodeVariant *find_variant_bf16(int D, int gmax, bool mma);
 
-cudaError_t launch_merge(const DecodeParams &p, int D, cudaStream_t st);
+// Zero pkv_decode_attention_static's scratch on the current device (after a
+// timed-out wait may have left arrival counters set).
+cudaError_t clear_static_scratch();
 
 // Record the text pkv_last_error_message returns on this thread; returns st.
 pkv_status set_last_error(pkv_status st, const char *fmt, ...);

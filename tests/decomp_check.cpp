@@ -1,15 +1,22 @@
 // Host-side check of the split-K work decomposition (csrc/decomp.h).
 //
 // For random batches it replays what the split-K kernel's producer decides
-// for every CTA (segments, whole-unit writes, partial slots) and what the
-// merge kernel reads, and checks that
+// for every CTA (segments, whole-unit writes, partial slots) and how the
+// partials of a cut unit are merged: each CTA holding one counts itself in
+// the counter of the unit's first owner, CTAs finishing in a random order,
+// and the one that brings the count to pkv_unit_parts merges. It checks that
 //   * every tile belongs to exactly one CTA and pkv_owner inverts pkv_split,
 //   * each CTA writes at most one partial per slot,
+//   * the producer's cursor (pkv_cursor_at / pkv_cursor_next) names the
+//     right sequence, unit and tile at every step of a CTA's walk,
+//   * no two cut units share a counter, pkv_unit_parts equals the number of
+//     CTAs that touch the unit, and every counter ends back at zero,
 //   * every unit is finished exactly once: either whole by one CTA, or merged
-//     by exactly one merge block that reads exactly the partials written for
-//     it, which together cover all its tiles.
+//     once from exactly the partials written for it, which together cover
+//     all its tiles.
 // Prints "OK" and exits 0 on success.
 #include <cstdio>
+#include <algorithm>
 #include <cstdlib>
 #include <random>
 #include <vector>
@@ -46,6 +53,9 @@ int main() {
         const int units = S * U;
         std::vector<int> whole(units, 0), merged(units, 0), covered(units, 0);
         std::vector<int> slot_unit(2 * C, -1), slot_tiles(2 * C, 0);
+        // cut segments each CTA reports at its end: (unit, unit start tile)
+        std::vector<std::vector<std::pair<int, int64_t>>> arrivals(C);
+        std::vector<int> counter(C, 0), counter_unit(C, -1), touching(units, 0);
 
         for (int64_t t = 0; t < NT; ++t) {
             const int c = pkv_owner(t, C, NT);
@@ -63,6 +73,7 @@ int main() {
                 const int64_t Tu = prefix[s] + (int64_t)u * n[s];
                 const int64_t seg_end = (Tu + n[s] < t1) ? Tu + n[s] : t1;
                 const int unit = s * U + u;
+                touching[unit]++;
                 const bool is_whole = Tu >= t0 && Tu + n[s] <= t1;
                 if (is_whole) {
                     whole[unit]++;
@@ -72,30 +83,56 @@ int main() {
                     CHECK(slot_unit[2 * c + slot] == -1, "CTA %d writes slot %d twice", c, slot);
                     slot_unit[2 * c + slot] = unit;
                     slot_tiles[2 * c + slot] = (int)(seg_end - t);
+                    arrivals[c].push_back({unit, Tu});
                 }
                 t = seg_end;
             }
-        }
-        // merge replay
-        for (int j = 1; j < C; ++j) {
-            const int64_t tau = pkv_split(j, C, NT);
-            if (tau >= NT) continue;
-            const int s = pkv_find_seq(prefix.data(), S, tau);
-            const int u = (int)((tau - prefix[s]) / n[s]);
-            const int64_t Tu = prefix[s] + (int64_t)u * n[s];
-            const int cf = pkv_owner(Tu, C, NT);
-            if (cf + 1 != j) continue;
-            const int cl = pkv_owner(Tu + n[s] - 1, C, NT);
-            const int unit = s * U + u;
-            merged[unit]++;
-            for (int c = cf; c <= cl; ++c) {
-                if (pkv_cta_empty(c, C, NT)) continue;
-                const int slot = pkv_partial_slot(c, C, NT, Tu);
-                CHECK(slot_unit[2 * c + slot] == unit, "merge of unit %d reads CTA %d slot %d", unit,
-                      c, slot);
-                covered[unit] += slot_tiles[2 * c + slot];
+            if (t1 > t0) {
+                // the producer's cursor walks [t0, t1) in flat order (and one step
+                // past it, which the lookahead cursor takes)
+                PkvCursor cur;
+                pkv_cursor_at(cur, t0, prefix.data(), len.data(), S);
+                for (int64_t tau = t0; tau <= t1 && tau < NT; ++tau) {
+                    const int s = pkv_find_seq(prefix.data(), S, tau);
+                    const int off = (int)(tau - prefix[s]);
+                    CHECK(cur.s == s && cur.u == off / n[s] && cur.ti == off % n[s] &&
+                              cur.n == n[s] && cur.L == len[s],
+                          "CTA %d: cursor (%d,%d,%d) at tile %lld", c, cur.s, cur.u, cur.ti,
+                          (long long)tau);
+                    pkv_cursor_next(cur, len.data(), S, U);
+                }
             }
         }
+        // arrival replay, CTAs finishing in a random order
+        std::vector<int> order(C);
+        for (int c = 0; c < C; ++c) order[c] = c;
+        std::shuffle(order.begin(), order.end(), rng);
+        for (int c : order) {
+            for (const auto &a : arrivals[c]) {
+                const int unit = a.first, s = unit / U;
+                const int64_t Tu = a.second;
+                const int cf = pkv_owner(Tu, C, NT);
+                CHECK(counter_unit[cf] == -1 || counter_unit[cf] == unit,
+                      "units %d and %d share counter %d", counter_unit[cf], unit, cf);
+                counter_unit[cf] = unit;
+                const int parts = pkv_unit_parts(Tu, n[s], C, NT);
+                CHECK(parts == touching[unit], "unit %d: %d parts, %d CTAs touch it", unit, parts,
+                      touching[unit]);
+                if (++counter[cf] != parts) continue;
+                counter[cf] = 0;   // the merging warp puts the counter back
+                merged[unit]++;
+                const int cl = pkv_owner(Tu + n[s] - 1, C, NT);
+                const int slot_first = pkv_partial_slot(cf, C, NT, Tu);
+                for (int c2 = cf; c2 <= cl; ++c2) {
+                    if (pkv_cta_empty(c2, C, NT)) continue;
+                    const int slot = c2 == cf ? slot_first : 0;
+                    CHECK(slot_unit[2 * c2 + slot] == unit, "merge of unit %d reads CTA %d slot %d",
+                          unit, c2, slot);
+                    covered[unit] += slot_tiles[2 * c2 + slot];
+                }
+            }
+        }
+        for (int c = 0; c < C; ++c) CHECK(counter[c] == 0, "counter %d left at %d", c, counter[c]);
         for (int s = 0; s < S; ++s)
             for (int u = 0; u < U; ++u) {
                 const int unit = s * U + u;

@@ -86,6 +86,11 @@ def test_decode_rejects_bad_arguments(L):
     assert _decode(L, _desc(dt=binding.PKV_F32), opts=o) == -2   # mma needs 16-bit
     o.consumer = 3
     assert _decode(L, d, opts=o) == -1
+    o.consumer = 0
+    o.num_ctas = 4097                                      # above PKV_MAX_DECODE_CTAS
+    assert _decode(L, d, opts=o) == -1
+    o.num_ctas = -1
+    assert _decode(L, d, opts=o) == -1
     assert _decode(L, d, S=0) == 0                         # no-op
     assert _decode(L, d, q=None) == -1
     assert _decode(L, d, q=8) == -1                        # misaligned q
@@ -108,9 +113,12 @@ def test_block_copy_rejects_bad_pairs(L):
 
 def test_workspace_size_formula(L):
     d = _desc(hk=8, d=128)
-    # C CTAs x (32-byte merge descriptor + 2 slots x heads-per-unit x (D outputs + 1 lse) x 4 bytes)
-    assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 32, 10) == 10 * (32 + 2 * 4 * 129 * 4)
-    assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 8 * 40, 3) == 3 * (32 + 2 * 16 * 129 * 4)
+    # 4096 CTAs x 4 arrival counters x 4 bytes, then C CTAs x 2 slots x
+    # heads-per-unit x (D outputs + 4 per-warp lse copies) x 4 bytes
+    cnt = 4096 * 16
+    assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 32, 10) == cnt + 10 * 2 * 4 * 132 * 4
+    assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 8 * 40, 3) == cnt + 3 * 2 * 16 * 132 * 4
+    assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 32, 4097) == 0
     assert L.pkv_decode_workspace_bytes_ex(ctypes.byref(d), 33, 10) == 0
 
 

@@ -92,6 +92,43 @@ def test_gqa4_bf16_ragged_ctas(num_ctas):
     assert_close(got, ref, "bf16", f"ctas={num_ctas}")
 
 
+def test_workspace_reuse_keeps_counters_zero():
+    """One zero-filled workspace, sized for the largest launch, serves calls
+    with different batches, head groupings and CTA counts in a row (a call
+    with more CTAs than the one before it finds that call's partials just past
+    the counters it used). Each call must match the oracle, which needs the
+    counters to read zero when it starts, and must leave every arrival counter
+    of the buffer at zero."""
+    cases = [(41, 32, 8, 152, [1, 70, 513, 1500, 4096, 64, 2000, 333]),
+             (42, 32, 8, 7, [3000, 17, 900]),
+             (43, 16, 16, 600, [65, 129, 5, 64]),
+             (44, 64, 8, 300, [2048, 1, 777, 4000, 4000]),
+             (41, 32, 8, 152, [1, 70, 513, 1500, 4096, 64, 2000, 333])]
+    max_c = max(c[3] for c in cases)
+    ws = None
+    for seed, hq, hk, C, lengths in cases:
+        spec = W.WorkloadSpec("reuse", len(lengths), hq, hk, 128, 16, "bf16", 1.0)
+        st, vals = W.make_workload(spec, seed=seed, lengths=lengths)
+        dev = "cuda"
+        kp, vp = vals["k_pool"].to(dev), vals["v_pool"].to(dev)
+        if ws is None:   # heads-per-unit is 16 at most: size for the largest layout
+            ws = binding.alloc_workspace(kp, 16 * hk, max_c)
+        binding.append(vals["k_new"].to(dev), vals["v_new"].to(dev), st.slot_mapping.to(dev),
+                       kp, vp)
+        scale = 1.0 / math.sqrt(128)
+        out = binding.decode_attention(vals["q"].to(dev), kp, vp, st.block_tables.to(dev),
+                                       st.context_lens.to(dev), scale, out_dtype=torch.float32,
+                                       workspace=ws, num_ctas=C)
+        torch.cuda.synchronize()
+        assert binding.get_error() == 0
+        kp_o, vp_o = vals["k_pool"].clone(), vals["v_pool"].clone()
+        oracle.append(vals["k_new"], vals["v_new"], st.slot_mapping, kp_o, vp_o)
+        ref = oracle.decode(vals["q"], kp_o, vp_o, st.block_tables, st.context_lens, scale)
+        assert_close(out.double().cpu().numpy(), ref, "bf16", f"ctas={C}")
+        counters = ws[: 4096 * 16].view(torch.int32)   # [4096 CTAs][4 math warps]
+        assert int(counters.abs().sum()) == 0, "arrival counters left non-zero"
+
+
 @pytest.mark.parametrize("consumer", [1, 2])
 @pytest.mark.parametrize("dtype,Hq,Hk,D", [("bf16", 32, 8, 128), ("f16", 8, 8, 128),
                                             ("f16", 16, 8, 128), ("bf16", 24, 8, 128),

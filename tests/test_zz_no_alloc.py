@@ -5,10 +5,11 @@ where cudaMalloc's device synchronisation is not allowed). Instead of a
 caller workspace it uses a fixed scratch array inside the library.
 
 Checks, through the C ABI, that two calls in a row (different batches, so the
-second finds the first's leftovers in the shared scratch) match the ordinary
-workspace entry point within the decode tolerance, and that a shape needing
-more scratch than the fixed array is refused. Kept in a file that pytest
-collects last.
+second finds the first's partials in the shared scratch and relies on the
+first having put the split-K arrival counters back to zero) match the
+ordinary workspace entry point within the decode tolerance, and that a shape
+needing more scratch than the fixed array is refused. Kept in a file that
+pytest collects last.
 """
 import ctypes
 import math
@@ -70,9 +71,9 @@ def test_static_scratch_matches_workspace_entry_point(L):
 
 def test_static_scratch_refuses_shapes_that_do_not_fit(L):
     # q heads per kv head 16 at head_dim 128: one CTA per SM needs
-    # SMs x (32 + 8 x 16 x 129) bytes of scratch
+    # 16 x 4096 + SMs x 8 x 16 x 132 bytes of scratch
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    need = sms * (32 + 8 * 16 * 129)
+    need = 16 * 4096 + sms * 8 * 16 * 132
     spec = W.WorkloadSpec("no_alloc_big", 2, 64, 4, 128, 16, "bf16", 1.0)
     st, v = W.make_workload(spec, seed=23, lengths=[100, 200])
     dev = "cuda"
