@@ -30,6 +30,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -87,10 +88,16 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of the decode kernel's code, comments and blank lines left out, so
+    that a committed ncu summary stays valid until the code itself changes."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_47_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_47_gb300", "csrc", name)) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        for line in text.splitlines():
+            line = line.split("//", 1)[0].rstrip()
+            if line:
+                h.update(line.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
@@ -103,7 +110,8 @@ def profiled_traffic():
     for line in open(PROFILE):
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+            m = re.search(r"`([^`]*)`", v)
+            vals[k.strip()] = m.group(1) if m else v.strip()
     if vals.get("kernel_source_hash") != kernel_source_hash():
         return None
     try:
@@ -348,13 +356,19 @@ def run_ours(args):
                       binding.PreparedDecode(vals["q"], kp, vp, tables, lens, scale, out, ws,
                                              consumer=args.consumer)))
 
-    def step(i, evs=None, s=None):
+    def step(i, evs=None, s=None, aevs=None):
         app, dec = calls[i % len(calls)]
         s = s if s is not None else torch.cuda.current_stream()
+        if aevs is not None:
+            aevs[0].record(s)
         if cow is not None:      # copy-on-write of the last shared block, then append
             kp, vp = copies[i % len(copies)][:2]
             binding.block_copy(cow, kp, vp, stream=s)
+        if aevs is not None:
+            aevs[1].record(s)
         app(s)
+        if aevs is not None:
+            aevs[2].record(s)
         dec(s, timing_events=evs)
 
     for i in range(args.warmup):
@@ -371,6 +385,15 @@ def run_ours(args):
         for e in pair:
             e.record(stream)            # materialise the CUDA event handle
         kev[i] = pair
+    # append and copy-on-write events on the same steps (eager launches only:
+    # torch's events are not recorded as nodes of a captured graph)
+    aev = {}
+    if args.launch == "eager":
+        for i in kev:
+            trio = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            for e in trio:
+                e.record(stream)
+            aev[i] = trio
     torch.cuda.synchronize()
 
     if args.launch == "graph":
@@ -391,7 +414,7 @@ def run_ours(args):
             (timed[i] if i in timed else plain[i % len(plain)]).replay()
     else:
         def run_step(i):
-            step(i, kev.get(i))
+            step(i, kev.get(i), aevs=aev.get(i))
 
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -418,6 +441,19 @@ def run_ours(args):
     ms_max = reduce_max(ms, world, dev)
     split_ms = [kev[i][0].elapsed_time(kev[i][1]) for i in kev]
     split_avg = sum(split_ms) / len(split_ms)
+    side = {}
+    if aev:
+        es = vals["q"].element_size()
+        app_ms = sum(aev[i][1].elapsed_time(aev[i][2]) for i in aev) / len(aev)
+        side["append"] = {"avg_us": round(app_ms * 1000, 3), "bytes": append_bytes,
+                          "gbs": round(append_bytes / (app_ms / 1000) / 1e9, 2),
+                          "note": "K/V rows read + written, slots read; launched alone"}
+        if cow is not None:
+            cp_ms = sum(aev[i][0].elapsed_time(aev[i][1]) for i in aev) / len(aev)
+            cp_bytes = cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * spec.head_dim * es
+            side["block_copy"] = {"avg_us": round(cp_ms * 1000, 3), "bytes": cp_bytes,
+                                  "gbs": round(cp_bytes / (cp_ms / 1000) / 1e9, 2),
+                                  "note": "whole K and V blocks read + written"}
     if binding.get_error() != 0:
         raise RuntimeError("device error word set during the timed region")
 
@@ -452,6 +488,7 @@ def run_ours(args):
                      "logical_bytes_per_launch": decode_bytes,
                      "avg_launch_ms": round(split_avg, 5),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "other_kernels": side or None,
         "gpu_launches": (2 + (1 if cow is not None else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
@@ -462,11 +499,23 @@ def run_ours(args):
         from oracle import oracle
         h = host_inputs_from_generator(st, args.seed, dev)
         r, tps, sec, reps = time_oracle(st, spec, h, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(r, 4), "unit": UNIT, "cores": oracle.num_threads(),
+        cores = oracle.num_threads()
+        line["cpu_baseline"] = {"value": round(r, 4), "unit": UNIT, "cores": cores,
                                 "kind": "oracle", "seq_tokens_per_s": round(tps, 1),
                                 "sample": f"the whole workload ({S} sequences, "
                                           f"{int(st.context_lens.sum())} context tokens) x {reps} "
                                           f"repetitions, {sec:.1f} s of fp64 oracle decode"}
+        # the same oracle on one core, over the first sequences only
+        n1 = min(4, S)
+        oracle.set_num_threads(1)
+        try:
+            r1, tps1, sec1, reps1 = time_oracle(st, spec, h, args.cpu_seconds / 4,
+                                                seq_ids=range(n1))
+        finally:
+            oracle.set_num_threads(cores)
+        line["cpu_baseline"]["one_core"] = {
+            "value": round(r1, 4), "unit": UNIT, "seq_tokens_per_s": round(tps1, 1),
+            "sample": f"first {n1} sequences x {reps1} repetitions, {sec1:.1f} s"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -36,6 +36,8 @@ def lib():
         L.oracle_decode_elem.restype = ctypes.c_double
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = i32
+        L.oracle_set_num_threads.argtypes = [i32]
+        L.oracle_set_num_threads.restype = None
         _lib = L
     return _lib
 
@@ -97,3 +99,8 @@ def decode_elem(dtype: torch.dtype, bits: int) -> float:
 
 def num_threads() -> int:
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of later oracle calls (OpenMP); n >= 1."""
+    lib().oracle_set_num_threads(int(n))

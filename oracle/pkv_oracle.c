@@ -242,3 +242,12 @@ int oracle_num_threads(void) {
     return 1;
 #endif
 }
+
+/* Set the number of threads later calls use (n >= 1); no effect without OpenMP. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -9,8 +9,11 @@
 // How (GB300 design):
 //  * Persistent, stream-K: one CTA per SM (x occupancy) takes an equal share
 //    of the flattened (sequence, kv-head unit, 64-token tile) space
-//    (decomp.h). Partial results of units cut by a CTA boundary are merged by
-//    log-sum-exp in decode_merge_kernel; whole units are written directly.
+//    (decomp.h). Whole units are written directly. A unit cut by CTA
+//    boundaries leaves one partial per CTA; after its last tile each math
+//    warp counts its slices of those partials in per-unit arrival counters,
+//    and the warp that completes a count merges that slice by log-sum-exp
+//    (merge_slice). No CTA ever waits for another.
 //  * Warps 4-7 are producers: they walk the CTA's tiles, read block-table
 //    entries a few tiles ahead, and gather each (physical block, kv head)
 //    chunk with 16-byte cp.async copies into a ring of NST shared-memory
@@ -25,11 +28,12 @@
 //    its own online-softmax state (running max m, sum l, accumulator) in fp32
 //    registers, in base 2 with scale*log2(e) folded in. At the end of a
 //    segment the four warps combine their states through shared memory.
-//  * Math: with >= 3 q heads per kv head on 16-bit data the products run on
-//    tensor cores (mma.sync m16n8k16, tokens as M, q heads as N, fp32
-//    accumulate; P is split into hi+lo 16-bit parts so the PV product keeps
-//    fp32-level accuracy). Otherwise they run on CUDA cores with each lane
-//    owning a slice of head_dim (reduce-scatter for the dot products).
+//  * Math: on 16-bit data the products run on tensor cores (mma.sync
+//    m16n8k16, tokens as M, q heads as N padded to 8, fp32 accumulate; P is
+//    split into hi+lo 16-bit parts so the PV product keeps fp32-level
+//    accuracy). On fp32 data (or when forced) they run on CUDA cores with
+//    each lane owning a slice of head_dim (reduce-scatter for the dot
+//    products).
 //  * Every mbarrier wait is bounded (device_utils.cuh); there is no
 //    __syncthreads or named barrier after the producer/consumer split.
 #pragma once
