@@ -36,6 +36,16 @@ def lib():
         L.oracle_decode_elem.restype = ctypes.c_double
         L.oracle_num_threads.argtypes = []
         L.oracle_num_threads.restype = i32
+        L.oracle_append_quant.argtypes = [i32, i32, vp, vp, i64p, i32, vp, vp, vp, vp, i32, i32,
+                                          i32, i32]
+        L.oracle_append_quant.restype = i32
+        L.oracle_decode_quant.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                          i32, i32p, i32, i32p, ctypes.c_double, vp]
+        L.oracle_decode_quant.restype = i32
+        L.oracle_e4m3_decode.argtypes = [i32]
+        L.oracle_e4m3_decode.restype = ctypes.c_double
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        L.oracle_e4m3_encode.restype = i32
         L.oracle_set_num_threads.argtypes = [i32]
         L.oracle_set_num_threads.restype = None
         _lib = L
@@ -104,3 +114,59 @@ def num_threads() -> int:
 def set_num_threads(n: int) -> None:
     """Threads of later oracle calls (OpenMP); n >= 1."""
     lib().oracle_set_num_threads(int(n))
+
+
+# ------------------------------------------------------------------ quantized KV
+QUANT_KINDS = {"int8": 1, "fp8_e4m3": 2}
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one E4M3 code (NaN for the two NaN codes)."""
+    return lib().oracle_e4m3_decode(int(code))
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest E4M3 code of an fp32 value (ties to even, saturating at 448)."""
+    return lib().oracle_e4m3_encode(float(x))
+
+
+def append_quant(kind: str, k_new, v_new, slot_mapping, k_codes, v_codes, k_scales, v_scales):
+    """In-place quantized append: k_new/v_new [N][Hk][D] (fp16/bf16) into code
+    pools [NB][Hk][B][D] (uint8) and scale pools [NB][Hk][B] (fp32)."""
+    for t in (k_codes, v_codes, k_scales, v_scales):
+        assert t.is_contiguous() and t.device.type == "cpu"
+    assert k_codes.dtype == v_codes.dtype == torch.uint8
+    assert k_scales.dtype == v_scales.dtype == torch.float32
+    k_new, v_new = _cpu(k_new), _cpu(v_new)
+    assert k_new.dtype == v_new.dtype and k_new.dtype in (torch.float16, torch.bfloat16)
+    sm = _cpu(slot_mapping).to(torch.int64)
+    NB, Hk, B, D = k_codes.shape
+    rc = lib().oracle_append_quant(QUANT_KINDS[kind], _CODES[k_new.dtype], k_new.data_ptr(),
+                                   v_new.data_ptr(), sm.data_ptr(), sm.numel(),
+                                   k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
+                                   v_scales.data_ptr(), NB, Hk, B, D)
+    if rc != 0:
+        raise ValueError(f"oracle_append_quant failed with status {rc}")
+
+
+def decode_quant(kind: str, q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens,
+                 scale: float, seq_ids: Optional[Sequence[int]] = None) -> np.ndarray:
+    """fp64 attention output [S'][Hq][D] over a quantized cache."""
+    q = _cpu(q)
+    kc, vc, ks, vs = _cpu(k_codes), _cpu(v_codes), _cpu(k_scales), _cpu(v_scales)
+    bt, cl = _cpu(block_tables).to(torch.int32), _cpu(context_lens).to(torch.int32)
+    if seq_ids is not None:
+        idx = torch.as_tensor(list(seq_ids), dtype=torch.long)
+        q, bt, cl = q[idx].contiguous(), bt[idx].contiguous(), cl[idx].contiguous()
+    assert q.dtype in (torch.float16, torch.bfloat16)
+    S, Hq, D = q.shape
+    NB, Hk, B, D2 = kc.shape
+    assert D2 == D and ks.shape == (NB, Hk, B)
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    rc = lib().oracle_decode_quant(q.data_ptr(), _CODES[q.dtype], S, Hq, Hk, D, B,
+                                   QUANT_KINDS[kind], kc.data_ptr(), vc.data_ptr(), ks.data_ptr(),
+                                   vs.data_ptr(), NB, bt.data_ptr(), bt.shape[1], cl.data_ptr(),
+                                   float(scale), out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_decode_quant failed with status {rc}")
+    return out
