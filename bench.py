@@ -53,29 +53,38 @@ PROFILE = os.path.join(ROOT, "profiles", "decode_split_kernel_llama3_8b.md")
 
 
 # ------------------------------------------------------------------ helpers
-def unique_kv_bytes(st, spec):
+def cache_row_bytes(spec, kv_quant):
+    """Bytes of one (token, kv head) row of K (or V) in the cache: D elements,
+    or D 8-bit codes plus a 4-byte scale."""
+    if kv_quant:
+        return spec.head_dim + 4
+    return spec.head_dim * torch.tensor([], dtype=W.DTYPES[spec.dtype]).element_size()
+
+
+def unique_kv_bytes(st, spec, row_bytes):
     """K/V bytes of the distinct physical rows the step reads (a block shared
     by several sequences counted once)."""
-    es = torch.tensor([], dtype=W.DTYPES[spec.dtype]).element_size()
     B = spec.block_size
     rows = {}
     for s, L in enumerate(st.context_lens.tolist()):
         for j in range(-(-L // B)):
             b = int(st.block_tables[s, j])
             rows[b] = max(rows.get(b, 0), min(B, L - j * B))
-    return sum(rows.values()) * 2 * spec.num_kv_heads * spec.head_dim * es
+    return sum(rows.values()) * 2 * spec.num_kv_heads * row_bytes
 
 
-def step_bytes(st, spec):
-    """Algorithmic bytes of one decode step (decode + append)."""
+def step_bytes(st, spec, row_bytes):
+    """Algorithmic bytes of one decode step (decode + append): every context
+    row of K and V in the cache, q in and out, table entries, lengths; the
+    append reads the new K/V activations and writes their cache rows."""
     es = torch.tensor([], dtype=W.DTYPES[spec.dtype]).element_size()
     lens = st.context_lens.long()
     S = lens.numel()
-    kv = int(lens.sum()) * 2 * spec.num_kv_heads * spec.head_dim * es
+    kv = int(lens.sum()) * 2 * spec.num_kv_heads * row_bytes
     qo = S * spec.num_q_heads * spec.head_dim * es * 2
     tables = int(((lens + spec.block_size - 1) // spec.block_size).sum()) * 4
     decode = kv + qo + tables + 4 * S
-    append = S * spec.num_kv_heads * spec.head_dim * es * 2 * 2 + 8 * S
+    append = S * spec.num_kv_heads * 2 * (spec.head_dim * es + row_bytes) + 8 * S
     return decode, append
 
 
@@ -211,15 +220,31 @@ def barrier(world: int):
 
 
 # ------------------------------------------------------------------ oracle timing
-def host_inputs_from_generator(st, seed, device):
+def host_inputs_from_generator(st, seed, device, kv_quant=None):
     """The step's inputs, re-drawn from the seeded generator and copied to the
-    host, with the oracle's own append applied (post-append cache state)."""
+    host, with the oracle's own append applied (post-append cache state). For
+    an 8-bit cache the oracle quantizes every context row itself."""
     from oracle import oracle
 
     v = W.make_values(st, seed, device=device)
     h = {k: t.cpu() for k, t in v.items()}
     del v
     oracle.append(h["k_new"], h["v_new"], st.slot_mapping, h["k_pool"], h["v_pool"])
+    if kv_quant:
+        NB, Hk, B, D = h["k_pool"].shape
+        slots = set()
+        for s, L in enumerate(st.context_lens.tolist()):
+            row = st.block_tables[s].tolist()
+            slots.update(row[t // B] * B + t % B for t in range(L))
+        sl = torch.tensor(sorted(slots), dtype=torch.int64)
+        kr = h["k_pool"][sl // B, :, sl % B].contiguous()
+        vr = h["v_pool"][sl // B, :, sl % B].contiguous()
+        kc = torch.zeros(NB, Hk, B, D, dtype=torch.uint8)
+        ks = torch.zeros(NB, Hk, B, dtype=torch.float32)
+        q = {"k_codes": kc, "v_codes": kc.clone(), "k_scales": ks, "v_scales": ks.clone()}
+        oracle.append_quant(kv_quant, kr, vr, sl, q["k_codes"], q["v_codes"], q["k_scales"],
+                            q["v_scales"])
+        h = {"q": h["q"], "quant": kv_quant, **q}
     return h
 
 
@@ -231,15 +256,21 @@ def time_oracle(st, spec, h, target_s, seq_ids=None):
     ids = list(range(st.context_lens.numel())) if seq_ids is None else list(seq_ids)
     lens = [int(st.context_lens[i]) for i in ids]
     es = h["q"].element_size()
-    nbytes = (sum(lens) * 2 * spec.num_kv_heads * spec.head_dim * es
+    row_bytes = cache_row_bytes(spec, h.get("quant"))
+    nbytes = (sum(lens) * 2 * spec.num_kv_heads * row_bytes
               + len(ids) * spec.num_q_heads * spec.head_dim * es * 2
               + sum((L + spec.block_size - 1) // spec.block_size for L in lens) * 4 + 4 * len(ids))
     scale = 1.0 / math.sqrt(spec.head_dim)
     spent, reps = 0.0, 0
     while spent < target_s or reps == 0:
         t0 = time.perf_counter()
-        oracle.decode(h["q"], h["k_pool"], h["v_pool"], st.block_tables, st.context_lens, scale,
-                      seq_ids=ids)
+        if h.get("quant"):
+            oracle.decode_quant(h["quant"], h["q"], h["k_codes"], h["v_codes"], h["k_scales"],
+                                h["v_scales"], st.block_tables, st.context_lens, scale,
+                                seq_ids=ids)
+        else:
+            oracle.decode(h["q"], h["k_pool"], h["v_pool"], st.block_tables, st.context_lens,
+                          scale, seq_ids=ids)
         spent += time.perf_counter() - t0
         reps += 1
     return nbytes * reps / spent / 1e9, sum(lens) * reps / spent, spent, reps
@@ -300,6 +331,76 @@ def workload_config(spec, st):
                     + "pkv_append + pkv_decode_attention (split-K with in-kernel merge)"}
 
 
+# ------------------------------------------------------------------ cache copies
+class Pools16:
+    """One resident copy of a 16-bit paged cache (K and V pools)."""
+
+    def __init__(self, kp, vp):
+        self.kp, self.vp = kp, vp
+
+    def workspace(self, Hq):
+        from paged_kv_cache_47_gb300 import binding
+        return binding.alloc_workspace(self.kp, Hq)
+
+    def prepared(self, q, kn, vn, slots, tables, lens, scale, out, ws, consumer=0):
+        from paged_kv_cache_47_gb300 import binding
+        return (binding.PreparedAppend(kn, vn, slots, self.kp, self.vp),
+                binding.PreparedDecode(q, self.kp, self.vp, tables, lens, scale, out, ws,
+                                       consumer=consumer))
+
+    def cow(self, pairs, stream):
+        from paged_kv_cache_47_gb300 import binding
+        binding.block_copy(pairs, self.kp, self.vp, stream=stream)
+
+    def clone(self):
+        return Pools16(self.kp.clone(), self.vp.clone())
+
+
+class PoolsQ:
+    """One resident copy of an 8-bit paged cache (codes and row scales)."""
+
+    def __init__(self, cache):
+        self.cache = cache
+
+    @classmethod
+    def fill(cls, code, st, vals, dev):
+        """An 8-bit cache holding every context row before the step's append,
+        quantized by the library from the drawn activations."""
+        from paged_kv_cache_47_gb300 import binding
+        NB, Hk, B, D = vals["k_pool"].shape
+        cache = binding.QuantCache.empty(NB, Hk, B, D, code, vals["q"].dtype, device=dev)
+        slots = set()
+        for s, L in enumerate(st.context_lens.tolist()):
+            row = st.block_tables[s].tolist()
+            slots.update(row[t // B] * B + t % B for t in range(L - 1))
+        sl = torch.tensor(sorted(slots), dtype=torch.int64, device=dev)
+        blk, off = sl // B, sl % B
+        kr = vals["k_pool"][blk, :, off].contiguous()
+        vr = vals["v_pool"][blk, :, off].contiguous()
+        binding.append_quant(kr, vr, sl, cache)
+        torch.cuda.synchronize()
+        return cls(cache)
+
+    def workspace(self, Hq):
+        from paged_kv_cache_47_gb300 import binding
+        return binding.alloc_quant_workspace(self.cache, Hq)
+
+    def prepared(self, q, kn, vn, slots, tables, lens, scale, out, ws, consumer=0):
+        from paged_kv_cache_47_gb300 import binding
+        return (binding.PreparedAppendQuant(kn, vn, slots, self.cache),
+                binding.PreparedDecodeQuant(q, self.cache, tables, lens, scale, out, ws))
+
+    def cow(self, pairs, stream):
+        from paged_kv_cache_47_gb300 import binding
+        binding.block_copy_quant(pairs, self.cache, stream=stream)
+
+    def clone(self):
+        from paged_kv_cache_47_gb300 import binding
+        c = self.cache
+        return PoolsQ(binding.QuantCache(c.k_codes.clone(), c.v_codes.clone(), c.k_scales.clone(),
+                                         c.v_scales.clone(), c.code, c.act_dtype))
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args):
     from paged_kv_cache_47_gb300 import binding, build
@@ -332,29 +433,25 @@ def run_ours(args):
     slots = st.slot_mapping.to(dev)
     S, Hq, D = vals["q"].shape
     # three resident copies of the cache so every step reads a cold L2
-    copies = []
-    for c in range(args.copies):
-        kp = vals["k_pool"] if c == 0 else vals["k_pool"].clone()
-        vp = vals["v_pool"] if c == 0 else vals["v_pool"].clone()
-        out = torch.empty(S, Hq, D, dtype=vals["q"].dtype, device=dev)
-        ws = binding.alloc_workspace(kp, Hq)
-        copies.append((kp, vp, out, ws))
-    decode_bytes, append_bytes = step_bytes(st, spec)
+    base = PoolsQ.fill(args.kv_quant, st, vals, dev) if args.kv_quant else \
+        Pools16(vals["k_pool"], vals["v_pool"])
+    if args.kv_quant:
+        del vals["k_pool"], vals["v_pool"]      # the activations are in the 8-bit cache now
+    copies = [base] + [base.clone() for _ in range(args.copies - 1)]
+    outs = [torch.empty(S, Hq, D, dtype=vals["q"].dtype, device=dev) for _ in copies]
+    wss = [c.workspace(Hq) for c in copies]
+    row_bytes = cache_row_bytes(spec, args.kv_quant)
+    decode_bytes, append_bytes = step_bytes(st, spec, row_bytes)
     total_bytes = decode_bytes + append_bytes
     if cow is not None:
-        es = vals["q"].element_size()
-        total_bytes += cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * spec.head_dim * es
+        total_bytes += cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * row_bytes
     # bytes the split-K kernel must bring from HBM: shared blocks once
     hbm_decode_bytes = decode_bytes - (int(st.context_lens.sum()) * 2 * spec.num_kv_heads *
-                                       spec.head_dim * vals["q"].element_size()) + \
-        unique_kv_bytes(st, spec)
+                                       row_bytes) + unique_kv_bytes(st, spec, row_bytes)
     stream = torch.cuda.current_stream()
     # prepared calls: the C-ABI arguments are marshalled once per cache copy
-    calls = []
-    for kp, vp, out, ws in copies:
-        calls.append((binding.PreparedAppend(vals["k_new"], vals["v_new"], slots, kp, vp),
-                      binding.PreparedDecode(vals["q"], kp, vp, tables, lens, scale, out, ws,
-                                             consumer=args.consumer)))
+    calls = [c.prepared(vals["q"], vals["k_new"], vals["v_new"], slots, tables, lens, scale, o, w,
+                        consumer=args.consumer) for c, o, w in zip(copies, outs, wss)]
 
     def step(i, evs=None, s=None, aevs=None):
         app, dec = calls[i % len(calls)]
@@ -362,8 +459,7 @@ def run_ours(args):
         if aevs is not None:
             aevs[0].record(s)
         if cow is not None:      # copy-on-write of the last shared block, then append
-            kp, vp = copies[i % len(copies)][:2]
-            binding.block_copy(cow, kp, vp, stream=s)
+            copies[i % len(copies)].cow(cow, s)
         if aevs is not None:
             aevs[1].record(s)
         app(s)
@@ -463,17 +559,22 @@ def run_ours(args):
     peak, peak_kind = peaks()
 
     # ------------- end to end: host inputs in, result out, every step
-    e2e = run_e2e(args, st, spec, vals, copies, tables, lens, slots, scale, stream, dev,
-                  total_bytes, world)
+    e2e = run_e2e(args, st, spec, vals, copies, outs, wss, tables, lens, slots, scale, stream,
+                  dev, total_bytes, world)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": args.kv_quant or spec.dtype,
         "data": "synthetic (seeded N(0,1) values, random block tables)",
         "config": {**workload_config(spec, st),
+                   **({"kv_cache": f"{args.kv_quant} codes + fp32 row scales "
+                                   f"({row_bytes} B per token and kv head for K, same for V); "
+                                   f"{spec.dtype} activations; fp16 tensor-core math"}
+                      if args.kv_quant else {}),
                    "l2": f"inputs > L2: the step cycles through {len(copies)} resident copies "
-                         f"of the cache ({len(copies)} x {2 * st.num_blocks * spec.num_kv_heads * spec.block_size * spec.head_dim * 2 / 1e9:.2f} GB)",
+                         f"of the cache ({len(copies)} x {2 * st.num_blocks * spec.num_kv_heads * spec.block_size * row_bytes / 1e9:.2f} GB)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "launch": "CUDA-graph replay of the step's kernel launches (captured through the C ABI)"
                              if args.launch == "graph" else "eager C-ABI calls"},
@@ -483,7 +584,9 @@ def run_ours(args):
                      "achieved": round(hbm_decode_bytes / (split_avg / 1000.0) / 1e9, 2),
                      "peak": peak, "unit": "GB/s",
                      "frac": round(hbm_decode_bytes / (split_avg / 1000.0) / 1e9 / peak, 4),
-                     "traffic": profiled_traffic() if args.workload == WORKLOAD_INDEX and not args.block_size else None,
+                     "traffic": profiled_traffic() if (args.workload == WORKLOAD_INDEX and
+                                                       not args.block_size and
+                                                       not args.kv_quant) else None,
                      "algorithmic_bytes_per_launch": hbm_decode_bytes,
                      "logical_bytes_per_launch": decode_bytes,
                      "avg_launch_ms": round(split_avg, 5),
@@ -497,7 +600,7 @@ def run_ours(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import oracle
-        h = host_inputs_from_generator(st, args.seed, dev)
+        h = host_inputs_from_generator(st, args.seed, dev, args.kv_quant)
         r, tps, sec, reps = time_oracle(st, spec, h, args.cpu_seconds)
         cores = oracle.num_threads()
         line["cpu_baseline"] = {"value": round(r, 4), "unit": UNIT, "cores": cores,
@@ -524,10 +627,8 @@ def run_ours(args):
     return 0
 
 
-def run_e2e(args, st, spec, vals, copies, tables, lens, slots, scale, stream, dev, total_bytes,
-            world):
-    from paged_kv_cache_47_gb300 import binding
-
+def run_e2e(args, st, spec, vals, copies, outs, wss, tables, lens, slots, scale, stream, dev,
+            total_bytes, world):
     pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
     h_q, h_kn, h_vn = pin(vals["q"]), pin(vals["k_new"]), pin(vals["v_new"])
     h_tab, h_len, h_slot = pin(st.block_tables), pin(st.context_lens), pin(st.slot_mapping)
@@ -539,9 +640,8 @@ def run_e2e(args, st, spec, vals, copies, tables, lens, slots, scale, stream, de
     steps = min(args.steps, args.e2e_steps)
 
     calls = []
-    for kp, vp, out, ws in copies:
-        calls.append((binding.PreparedAppend(d_kn, d_vn, d_slot, kp, vp),
-                      binding.PreparedDecode(d_q, kp, vp, d_tab, d_len, scale, out, ws), out))
+    for c, out, ws in zip(copies, outs, wss):
+        calls.append((*c.prepared(d_q, d_kn, d_vn, d_slot, d_tab, d_len, scale, out, ws), out))
 
     cow = st.cow_pairs if st.cow_pairs.numel() else None
 
@@ -551,8 +651,7 @@ def run_e2e(args, st, spec, vals, copies, tables, lens, slots, scale, stream, de
                      (d_slot, h_slot)):
             d.copy_(h, non_blocking=True)
         if cow is not None:
-            kp, vp = copies[i % len(copies)][:2]
-            binding.block_copy(cow, kp, vp, stream=stream)
+            copies[i % len(copies)].cow(cow, stream)
         app(stream)
         dec(stream)
         h_out.copy_(out, non_blocking=True)
@@ -590,6 +689,8 @@ def main():
     ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size")
     ap.add_argument("--dtype", choices=["f32", "f16", "bf16"], default=None,
                     help="override the workload's K/V dtype")
+    ap.add_argument("--kv-quant", choices=["int8", "fp8_e4m3"], default=None,
+                    help="8-bit KV cache (codes + fp32 row scales) instead of the workload's dtype")
     ap.add_argument("--consumer", type=int, default=0,
                     help="math path: 0 auto, 1 CUDA cores, 2 tensor cores (16-bit only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

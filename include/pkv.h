@@ -53,7 +53,9 @@ extern "C" {
 typedef enum {
     PKV_F32 = 0,
     PKV_F16 = 1,
-    PKV_BF16 = 2
+    PKV_BF16 = 2,
+    PKV_INT8 = 3,       /* 8-bit cache codes only (pkv_qcache_desc.code_dtype) */
+    PKV_FP8_E4M3 = 4    /* 8-bit cache codes only (pkv_qcache_desc.code_dtype) */
 } pkv_dtype;
 
 typedef enum {
@@ -237,6 +239,80 @@ pkv_status pkv_decode_attention_static(const pkv_cache_desc *cache, const void *
  */
 pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pairs,
                           int32_t num_pairs, void *k_pool, void *v_pool, void *stream);
+
+/* ------------------------------------------------------------ 8-bit KV cache
+ *
+ * Passage: an 8-bit KV cache is the lever that halves the bytes each decode
+ * step reads ("Contiguous vs Paged KV Cache on RDNA4", section "The order of
+ * the memory levers"; "KV-Cache Optimization & PagedAttention for Long-Context
+ * Agents", introduction). The pages fix no format; this library's is:
+ *
+ *   k_codes, v_codes    [num_blocks][num_kv_heads][block_size][head_dim] uint8
+ *                       one code per element: PKV_INT8 (two's complement,
+ *                       -127..127) or PKV_FP8_E4M3 (OCP E4M3: bias 7, no
+ *                       infinities, largest finite 448)
+ *   k_scales, v_scales  [num_blocks][num_kv_heads][block_size] float
+ *                       one scale per (token, kv head) row
+ *
+ * The cached value of element d of a row is scale * value(code[d]). A row x
+ * of D activations is quantized at append time: a = max_d |x_d| (fp32),
+ * scale = a / Qmax (fp32 division, round to nearest even; Qmax = 127 for
+ * int8, 448 for E4M3), code_d = x_d / scale in fp32 rounded to the nearest
+ * code value (ties to even), saturated to +-Qmax; a = 0 gives scale 0 and
+ * zero codes. Both K and V are stored this way. q, k_new and v_new stay in the
+ * activation dtype (PKV_F16 or PKV_BF16).
+ */
+typedef struct {
+    int32_t num_blocks;    /* physical blocks in each pool, >= 1               */
+    int32_t block_size;    /* tokens per block B: 8, 16 or 32                  */
+    int32_t num_kv_heads;  /* Hk >= 1                                          */
+    int32_t head_dim;      /* D: 128                                           */
+    int32_t code_dtype;    /* PKV_INT8 or PKV_FP8_E4M3                         */
+    int32_t act_dtype;     /* PKV_F16 or PKV_BF16: q, k_new, v_new             */
+} pkv_qcache_desc;
+
+/*
+ * pkv_append_quant — pkv_append for an 8-bit cache: quantizes each new token's
+ * K and V rows and writes codes and scales to slot_mapping[i] (negative
+ * slots are skipped; a slot past the pool sets PKV_DEVERR_SLOT and is
+ * skipped). k_new, v_new: [num_tokens][num_kv_heads][head_dim] in act_dtype,
+ * 16-byte aligned; code pools 16-byte aligned; scale pools 16-byte aligned.
+ * Codes and scales equal the rule above bit for bit.
+ */
+pkv_status pkv_append_quant(const pkv_qcache_desc *cache, const void *k_new, const void *v_new,
+                            const int64_t *slot_mapping, int32_t num_tokens, void *k_codes,
+                            void *v_codes, float *k_scales, float *v_scales, void *stream);
+
+/* Workspace bytes for pkv_decode_attention_quant with num_ctas CTAs (0 = the
+ * default launch). Same contract as pkv_decode_workspace_bytes_ex. */
+size_t pkv_decode_quant_workspace_bytes(const pkv_qcache_desc *cache, int32_t num_q_heads,
+                                        int32_t num_ctas);
+
+/*
+ * pkv_decode_attention_quant — pkv_decode_attention_ex over an 8-bit cache:
+ * out[s][h] = softmax(scale * q K^T) V with K and V the cached values
+ * scale * value(code). q: [num_seqs][num_q_heads][head_dim] in act_dtype.
+ * Same contract as pkv_decode_attention_ex for tables, lengths, out, the
+ * workspace (zero-filled before first use) and options, except that
+ * options->consumer 1 (CUDA-core math) is not available (PKV_ERR_UNSUPPORTED).
+ */
+pkv_status pkv_decode_attention_quant(const pkv_qcache_desc *cache, const void *q,
+                                      int32_t num_seqs, int32_t num_q_heads, const void *k_codes,
+                                      const void *v_codes, const float *k_scales,
+                                      const float *v_scales, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      float scale, void *out, int32_t out_dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream,
+                                      const pkv_decode_options *options);
+
+/*
+ * pkv_block_copy_quant — pkv_block_copy for an 8-bit cache: copies the codes
+ * and the scales of whole blocks. Same pair rules and errors as
+ * pkv_block_copy. Byte-exact.
+ */
+pkv_status pkv_block_copy_quant(const pkv_qcache_desc *cache, const int64_t *src_dst_pairs,
+                                int32_t num_pairs, void *k_codes, void *v_codes, float *k_scales,
+                                float *v_scales, void *stream);
 
 /*
  * pkv_get_error — synchronise `stream`, then read and clear the device error

@@ -14,7 +14,8 @@ import torch
 
 from . import build as _build
 
-PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
+PKV_F32, PKV_F16, PKV_BF16, PKV_INT8, PKV_FP8_E4M3 = 0, 1, 2, 3, 4
+CODE_DTYPES = {"int8": PKV_INT8, "fp8_e4m3": PKV_FP8_E4M3}
 DTYPE_CODE = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
 CODE_DTYPE = {v: k for k, v in DTYPE_CODE.items()}
 
@@ -27,6 +28,12 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32)]
+
+
+class QCacheDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("code_dtype", ctypes.c_int32), ("act_dtype", ctypes.c_int32)]
 
 
 class DecodeOptions(ctypes.Structure):
@@ -70,6 +77,17 @@ def lib():
         L.pkv_decode_attention_ex.restype = i32
         L.pkv_block_copy.argtypes = [dp, vp, i32, vp, vp, vp]
         L.pkv_block_copy.restype = i32
+        qp = ctypes.POINTER(QCacheDesc)
+        L.pkv_append_quant.argtypes = [qp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
+        L.pkv_append_quant.restype = i32
+        L.pkv_decode_quant_workspace_bytes.argtypes = [qp, i32, i32]
+        L.pkv_decode_quant_workspace_bytes.restype = sz
+        L.pkv_decode_attention_quant.argtypes = [qp, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp,
+                                                 ctypes.c_float, vp, i32, vp, sz, vp,
+                                                 ctypes.POINTER(DecodeOptions)]
+        L.pkv_decode_attention_quant.restype = i32
+        L.pkv_block_copy_quant.argtypes = [qp, vp, i32, vp, vp, vp, vp, vp]
+        L.pkv_block_copy_quant.restype = i32
         L.pkv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
         L.pkv_get_error.restype = i32
         L.pkv_status_string.argtypes = [i32]
@@ -238,3 +256,141 @@ def get_error(stream=None) -> int:
     w = ctypes.c_int32(0)
     lib().pkv_get_error(ctypes.byref(w), _stream(stream))
     return int(w.value)
+
+
+# ------------------------------------------------------------------ 8-bit caches
+class QuantCache:
+    """An 8-bit paged KV cache: code pools [NB][Hk][B][D] (uint8) and row-scale
+    pools [NB][Hk][B] (fp32) for K and V, with the activation dtype of q,
+    k_new and v_new. Holds the tensors; the library owns no memory."""
+
+    def __init__(self, k_codes, v_codes, k_scales, v_scales, code: str, act_dtype: torch.dtype):
+        for t in (k_codes, v_codes, k_scales, v_scales):
+            if not t.is_contiguous():
+                raise ValueError("quantized pools must be contiguous")
+        if k_codes.dtype != torch.uint8 or v_codes.shape != k_codes.shape:
+            raise ValueError("code pools must be uint8 and of one shape")
+        NB, Hk, B, D = k_codes.shape
+        if k_scales.dtype != torch.float32 or k_scales.shape != (NB, Hk, B) or \
+                v_scales.shape != k_scales.shape:
+            raise ValueError("scale pools must be float32 [NB][Hk][B]")
+        self.k_codes, self.v_codes, self.k_scales, self.v_scales = k_codes, v_codes, k_scales, v_scales
+        self.code, self.act_dtype = code, act_dtype
+        self.desc = QCacheDesc(NB, B, Hk, D, CODE_DTYPES[code], DTYPE_CODE[act_dtype])
+
+    @classmethod
+    def empty(cls, num_blocks, num_kv_heads, block_size, head_dim, code: str,
+              act_dtype: torch.dtype, device="cuda"):
+        kc = torch.zeros(num_blocks, num_kv_heads, block_size, head_dim, dtype=torch.uint8,
+                         device=device)
+        ks = torch.zeros(num_blocks, num_kv_heads, block_size, dtype=torch.float32, device=device)
+        return cls(kc, kc.clone(), ks, ks.clone(), code, act_dtype)
+
+    def pointers(self):
+        return (self.k_codes.data_ptr(), self.v_codes.data_ptr(), self.k_scales.data_ptr(),
+                self.v_scales.data_ptr())
+
+
+def append_quant(k_new, v_new, slot_mapping, cache: QuantCache, stream=None) -> None:
+    """Quantize k_new/v_new [N][Hk][D] (the cache's activation dtype) into their slots."""
+    k_new, v_new = k_new.contiguous(), v_new.contiguous()
+    sm = slot_mapping.contiguous()
+    assert sm.dtype == torch.int64 and k_new.dtype == cache.act_dtype == v_new.dtype
+    _check(lib().pkv_append_quant(ctypes.byref(cache.desc), _ptr(k_new), _ptr(v_new), _ptr(sm),
+                                  sm.numel(), *cache.pointers(), _stream(stream)))
+
+
+def quant_workspace_bytes(cache: QuantCache, num_q_heads: int, num_ctas: int = 0) -> int:
+    return int(lib().pkv_decode_quant_workspace_bytes(ctypes.byref(cache.desc), num_q_heads,
+                                                      num_ctas))
+
+
+def alloc_quant_workspace(cache: QuantCache, num_q_heads: int, num_ctas: int = 0) -> torch.Tensor:
+    """Zero-filled split-K workspace for pkv_decode_attention_quant."""
+    n = quant_workspace_bytes(cache, num_q_heads, num_ctas)
+    if n == 0:
+        raise PkvError(-1, "workspace size query failed")
+    return torch.zeros(n, dtype=torch.uint8, device=cache.k_codes.device)
+
+
+def decode_attention_quant(q, cache: QuantCache, block_tables, context_lens, scale: float,
+                           out: Optional[torch.Tensor] = None,
+                           out_dtype: Optional[torch.dtype] = None,
+                           workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                           consumer: int = 0, timing_events: Optional[Sequence] = None,
+                           stream=None) -> torch.Tensor:
+    """Paged decode attention over an 8-bit cache."""
+    S, Hq, D = q.shape
+    q = q.contiguous()
+    bt, cl = block_tables.contiguous(), context_lens.contiguous()
+    assert bt.dtype == torch.int32 and cl.dtype == torch.int32 and q.dtype == cache.act_dtype
+    if out is None:
+        out = torch.empty(S, Hq, D, dtype=out_dtype or q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_quant_workspace(cache, Hq, num_ctas)
+    opts = DecodeOptions()
+    opts.num_ctas = num_ctas
+    opts.consumer = consumer
+    if timing_events is not None:
+        for i, ev in enumerate(timing_events):
+            opts.timing_events[i] = None if ev is None else ev.cuda_event
+    _check(lib().pkv_decode_attention_quant(
+        ctypes.byref(cache.desc), _ptr(q), S, Hq, *cache.pointers(), _ptr(bt), bt.shape[1],
+        _ptr(cl), float(scale), _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace),
+        workspace.numel(), _stream(stream), ctypes.byref(opts)))
+    return out
+
+
+class PreparedDecodeQuant:
+    """pkv_decode_attention_quant with its arguments marshalled once (see PreparedDecode)."""
+
+    def __init__(self, q, cache: QuantCache, block_tables, context_lens, scale: float,
+                 out: torch.Tensor, workspace: Optional[torch.Tensor] = None, num_ctas: int = 0):
+        for t in (q, block_tables, context_lens, out):
+            if not t.is_contiguous():
+                raise ValueError("prepared decode needs contiguous tensors")
+        assert q.dtype == cache.act_dtype
+        S, Hq, D = q.shape
+        if workspace is None:
+            workspace = alloc_quant_workspace(cache, Hq, num_ctas)
+        self._keep = (q, cache, block_tables, context_lens, out, workspace)
+        self._opts = DecodeOptions()
+        self._opts.num_ctas = num_ctas
+        self._args = (ctypes.byref(cache.desc), q.data_ptr(), S, Hq, *cache.pointers(),
+                      block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(),
+                      float(scale), out.data_ptr(), DTYPE_CODE[out.dtype], workspace.data_ptr(),
+                      workspace.numel())
+        self._fn = lib().pkv_decode_attention_quant
+        self.out = out
+
+    def __call__(self, stream, timing_events: Optional[Sequence] = None) -> None:
+        opts = self._opts
+        for i in range(2):
+            ev = timing_events[i] if timing_events is not None else None
+            opts.timing_events[i] = None if ev is None else ev.cuda_event
+        _check(self._fn(*self._args, _stream(stream), ctypes.byref(opts)))
+
+
+class PreparedAppendQuant:
+    """pkv_append_quant with its arguments marshalled once (see PreparedDecode)."""
+
+    def __init__(self, k_new, v_new, slot_mapping, cache: QuantCache):
+        for t in (k_new, v_new, slot_mapping):
+            if not t.is_contiguous():
+                raise ValueError("prepared append needs contiguous tensors")
+        assert slot_mapping.dtype == torch.int64 and k_new.dtype == cache.act_dtype
+        self._keep = (k_new, v_new, slot_mapping, cache)
+        self._args = (ctypes.byref(cache.desc), k_new.data_ptr(), v_new.data_ptr(),
+                      slot_mapping.data_ptr(), slot_mapping.numel(), *cache.pointers())
+        self._fn = lib().pkv_append_quant
+
+    def __call__(self, stream) -> None:
+        _check(self._fn(*self._args, _stream(stream)))
+
+
+def block_copy_quant(pairs, cache: QuantCache, stream=None) -> None:
+    """Copy whole blocks (codes and scales) src -> dst; pairs is host data [n][2]."""
+    p = torch.as_tensor(pairs, dtype=torch.int64).reshape(-1, 2).contiguous()
+    assert p.device.type == "cpu", "block-copy pairs are host memory"
+    _check(lib().pkv_block_copy_quant(ctypes.byref(cache.desc), _ptr(p), p.shape[0],
+                                      *cache.pointers(), _stream(stream)))

@@ -1,0 +1,154 @@
+// Quantized KV append: each new token's K and V rows become 8-bit codes with
+// one fp32 scale per (token, kv head) row, written at their slot.
+//
+// The pages name an 8-bit KV cache as the lever that halves each decode's
+// read ("Contiguous vs Paged KV Cache on RDNA4", section "The order of the
+// memory levers"); the format (include/pkv.h, "8-bit KV cache") is this
+// library's reading: scale = max|x| / Qmax and code = x / scale rounded to
+// the nearest int8 or E4M3 value (ties to even), both divisions in fp32 with
+// round to nearest even, saturated to +-Qmax; an all-zero row has scale 0.
+//
+// One warp per (token, kv head) row of D = 128 activations: each lane holds
+// four consecutive elements (one 8-byte load), the row maximum is a warp
+// max-reduction, and the lane writes its four codes as one 32-bit store.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+__device__ __forceinline__ void wait_prior_grid() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_next_grid() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ float act_to_f32(T x);
+template <>
+__device__ __forceinline__ float act_to_f32<__half>(__half x) { return __half2float(x); }
+template <>
+__device__ __forceinline__ float act_to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+
+// One code of x / s (s > 0).
+template <int CODE>
+__device__ __forceinline__ uint32_t encode(float x, float s) {
+    const float v = __fdiv_rn(x, s);
+    if constexpr (CODE == PKV_INT8) {
+        int c = __float2int_rn(v);
+        c = c > 127 ? 127 : (c < -127 ? -127 : c);
+        return (uint32_t)(uint8_t)(int8_t)c;
+    } else {
+        return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+    }
+}
+
+// Quantize the row `src` (D = 128 elements of T) into `codes` and `*scale`.
+template <typename T, int CODE>
+__device__ __forceinline__ void quantize_row(const T *__restrict__ src, uint8_t *__restrict__ codes,
+                                             float *__restrict__ scale, int lane) {
+    constexpr float kQmax = CODE == PKV_INT8 ? 127.f : 448.f;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(src) + lane);
+    const T *e = reinterpret_cast<const T *>(&raw);
+    float x[4], a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        x[i] = act_to_f32<T>(e[i]);
+        a = fmaxf(a, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float s = __fdiv_rn(a, kQmax);
+    uint32_t word = 0;
+    if (a != 0.f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) word |= encode<CODE>(x[i], s) << (8 * i);
+    }
+    reinterpret_cast<uint32_t *>(codes)[lane] = word;
+    if (lane == 0) *scale = s;
+}
+
+// grid-stride over rows (token, kv head); one warp per row
+template <typename T, int CODE>
+__global__ void __launch_bounds__(256) append_quant_kernel(
+    const T *__restrict__ k_new, const T *__restrict__ v_new, const int64_t *__restrict__ slots,
+    int num_tokens, uint8_t *__restrict__ k_codes, uint8_t *__restrict__ v_codes,
+    float *__restrict__ k_scales, float *__restrict__ v_scales, int NB, int Hk, int B,
+    unsigned *err) {
+    constexpr int D = 128;
+    // programmatic serialisation: the previous kernel on the stream completes
+    // before any pool byte is touched; the next one may be scheduled meanwhile
+    allow_next_grid();
+    wait_prior_grid();
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = (int64_t)num_tokens * Hk;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+         r += warps) {
+        const int tok = (int)(r / Hk), g = (int)(r - (int64_t)tok * Hk);
+        const int64_t slot = __ldg(slots + tok);
+        if (slot < 0) continue;
+        const int64_t blk = slot / B;
+        const int off = (int)(slot - blk * B);
+        if (blk >= NB) {
+            if (lane == 0 && g == 0) atomicOr(err, PKV_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t row = (blk * Hk + g) * B + off;   // row of the pool
+        quantize_row<T, CODE>(k_new + r * D, k_codes + row * D, k_scales + row, lane);
+        quantize_row<T, CODE>(v_new + r * D, v_codes + row * D, v_scales + row, lane);
+    }
+}
+
+template <typename T, int CODE>
+cudaError_t launch(const void *k_new, const void *v_new, const int64_t *slots, int num_tokens,
+                   void *k_codes, void *v_codes, float *k_scales, float *v_scales, int NB, int Hk,
+                   int B, unsigned *err, cudaStream_t st) {
+    const int64_t rows = (int64_t)num_tokens * Hk;
+    int64_t blocks = (rows + 7) / 8;
+    if (blocks > 4096) blocks = 4096;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_quant_kernel<T, CODE>, static_cast<const T *>(k_new),
+                              static_cast<const T *>(v_new), slots, num_tokens,
+                              static_cast<uint8_t *>(k_codes), static_cast<uint8_t *>(v_codes),
+                              k_scales, v_scales, NB, Hk, B, err);
+}
+
+}  // namespace
+
+cudaError_t launch_append_quant(int code_dtype, int act_dtype, const void *k_new,
+                                const void *v_new, const int64_t *slots, int num_tokens,
+                                void *k_codes, void *v_codes, float *k_scales, float *v_scales,
+                                int NB, int Hk, int B, unsigned *err, cudaStream_t st) {
+    if (act_dtype == PKV_F16)
+        return code_dtype == PKV_INT8
+                   ? launch<__half, PKV_INT8>(k_new, v_new, slots, num_tokens, k_codes, v_codes,
+                                              k_scales, v_scales, NB, Hk, B, err, st)
+                   : launch<__half, PKV_FP8_E4M3>(k_new, v_new, slots, num_tokens, k_codes,
+                                                  v_codes, k_scales, v_scales, NB, Hk, B, err, st);
+    return code_dtype == PKV_INT8
+               ? launch<__nv_bfloat16, PKV_INT8>(k_new, v_new, slots, num_tokens, k_codes, v_codes,
+                                                 k_scales, v_scales, NB, Hk, B, err, st)
+               : launch<__nv_bfloat16, PKV_FP8_E4M3>(k_new, v_new, slots, num_tokens, k_codes,
+                                                     v_codes, k_scales, v_scales, NB, Hk, B, err,
+                                                     st);
+}
+
+}  // namespace pkv

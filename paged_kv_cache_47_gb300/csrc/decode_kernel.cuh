@@ -38,7 +38,10 @@
 //    __syncthreads or named barrier after the producer/consumer split.
 #pragma once
 
+#include <cuda_fp8.h>
 #include <math_constants.h>
+
+#include <type_traits>
 
 #include "decomp.h"
 #include "device_utils.cuh"
@@ -49,15 +52,25 @@ namespace pkv {
 // ---------------------------------------------------------------------------
 // compile-time shared-memory plan of one kernel variant
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA>
+// T is the activation type (q, k_new / v_new); QK selects the cache format:
+// 0 = T elements, kQuantInt8 / kQuantE4m3 = 8-bit codes with one fp32 scale
+// per (token, kv head) row.
+constexpr int kQuantInt8 = 1;
+constexpr int kQuantE4m3 = 2;
+
+template <typename T, int D, int GMAX, bool MMA, int QK = 0>
 struct SplitCfg {
-    static constexpr int ES = (int)sizeof(T);
+    static constexpr int ES = QK ? 1 : (int)sizeof(T);  // bytes of one cache element
     static constexpr int ROWB = D * ES;              // bytes of one K or V row
+    static constexpr int QROWB = D * (int)sizeof(T); // bytes of one q row
     static constexpr int NP = ROWB / 128;            // 128-byte swizzle planes per row
     static constexpr int PLANE = PKV_TILE_TOKENS * 128;
     static constexpr int KVB = NP * PLANE;           // bytes of one tile of K (or V)
-    static constexpr int QB = ((GMAX * ROWB + 1023) / 1024) * 1024;
-    static constexpr int STAGE = 2 * KVB + QB;       // multiple of 1024
+    static constexpr int SCB = QK ? 1024 : 0;        // K then V scales of the tile (2 x 256 B)
+    static constexpr int QB = ((GMAX * QROWB + 1023) / 1024) * 1024;
+    static constexpr int STAGE = 2 * KVB + SCB + QB; // multiple of 1024
+    // codes converted to 16-bit K and V tiles, one buffer reused every tile
+    static constexpr int CONV = QK ? 2 * (QROWB / 128) * PLANE : 0;
     static constexpr int NTN = GMAX / 8;             // mma n-tiles (MMA only)
     static constexpr int COMB_O = kConsumerWarps * GMAX * D * 4;
     static constexpr int COMB_ML = 2 * kConsumerWarps * GMAX * 4;
@@ -65,15 +78,17 @@ struct SplitCfg {
     static constexpr int SEQ_MAX = (2 * kMaxSeqsPerLaunch + 1) * 4;
     static constexpr int SMEM_LIMIT = 227 * 1024;
     static constexpr int PER_STAGE_EXTRA = (int)sizeof(TileMeta) + 16;  // meta + 2 barriers
-    static constexpr int FIXED = 1024 /*alignment slack*/ + COMB_O + COMB_ML + PBUF + 16 /*comb bars*/
-                                 + SEQ_MAX + 64;
+    static constexpr int FIXED = 1024 /*alignment slack*/ + CONV + COMB_O + COMB_ML + PBUF +
+                                 16 /*comb bars*/ + SEQ_MAX + 64;
     static constexpr int NST_FIT = (SMEM_LIMIT - FIXED) / (STAGE + PER_STAGE_EXTRA);
     static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
     static_assert(NST >= 2, "shared-memory plan leaves fewer than two stages");
     static_assert(ROWB % 128 == 0, "rows must be whole 128-byte planes");
+    static_assert(!QK || MMA, "8-bit caches use the tensor-core math");
 
     // offsets from the 1024-aligned base
-    static constexpr int OFF_META = NST * STAGE;
+    static constexpr int OFF_CONV = NST * STAGE;
+    static constexpr int OFF_META = OFF_CONV + CONV;
     static constexpr int OFF_FULL = OFF_META + NST * (int)sizeof(TileMeta);
     static constexpr int OFF_EMPTY = OFF_FULL + NST * 8;
     static constexpr int OFF_CBAR = OFF_EMPTY + NST * 8;   // comb_full, comb_empty
@@ -169,12 +184,12 @@ __device__ __forceinline__ void lds_vec(uint32_t addr, float (&out)[N]) {
 // ---------------------------------------------------------------------------
 // consumer state
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA>
+template <typename T, int D, int GMAX, bool MMA, int QK = 0>
 struct Consumer;
 
 // CUDA-core math: lane owns EPL = D/32 consecutive elements of head_dim.
 template <typename T, int D, int GMAX>
-struct Consumer<T, D, GMAX, false> {
+struct Consumer<T, D, GMAX, false, 0> {
     static constexpr int EPL = D / 32;
     static constexpr int TB = GMAX <= 2 ? 16 : (GMAX == 4 ? 8 : (GMAX == 8 ? 4 : 2));
     static constexpr int LOGTB = TB == 16 ? 4 : (TB == 8 ? 3 : (TB == 4 ? 2 : 1));
@@ -317,8 +332,20 @@ struct Consumer<T, D, GMAX, false> {
 
 // Tensor-core math: per warp, S^T[16 tokens x 8 heads] = K Q^T and
 // O^T[D x 8 heads] += V^T P^T with mma.sync m16n8k16 (fp32 accumulate).
-template <typename T, int D, int GMAX>
-struct Consumer<T, D, GMAX, true> {
+//
+// 8-bit caches (QK != 0): the math warps first turn their rows of codes into
+// exact fp16 values (convert_rows), so the products run in fp16. Each q head
+// is scaled by a power of two 2^-e (e >= 0) that keeps it below 2^15, and e
+// is folded back into that head's score factor; the scaling is exact. The
+// row scales enter as
+//     score_t = s_k[t] * <q, code_k[t]>,
+//     o = sum_t p_t s_v[t] code_v[t] / sum_t p_t,
+// with s_v[t] / max(s_v of the warp's 16 rows) multiplied into p_t before
+// it is split into fp16 parts (so it stays <= 1), and the running factor
+// sigma (that maximum) carried beside the accumulator, which holds o / sigma.
+template <typename T, int D, int GMAX, int QK>
+struct Consumer<T, D, GMAX, true, QK> {
+    using MT = typename std::conditional<QK != 0, __half, T>::type;  // mma operand type
     static constexpr int NTN = GMAX / 8;
     static constexpr int KS = D / 16;
     uint32_t qb[NTN][KS][2];
@@ -326,8 +353,11 @@ struct Consumer<T, D, GMAX, true> {
     float m[NTN][2], l[NTN][2];
     uint32_t pbuf;  // this warp's P staging buffer (NTN x {hi, lo} x 256 B)
     float scale_log2;
+    float sl2[NTN][2];  // 8-bit caches: score factor of this thread's score heads
+    float sigma;        // 8-bit caches: the accumulator holds o / sigma
 
     __device__ __forceinline__ void reset() {
+        sigma = 0.f;
 #pragma unroll
         for (int nt = 0; nt < NTN; ++nt) {
 #pragma unroll
@@ -342,23 +372,66 @@ struct Consumer<T, D, GMAX, true> {
         }
     }
 
-    __device__ __forceinline__ void load_q(const uint8_t *qslot, int gca, float sl2, int lane) {
-        scale_log2 = sl2;
+    __device__ __forceinline__ void load_q(const uint8_t *qslot, int gca, float sl2_in, int lane) {
+        scale_log2 = sl2_in;
         const int h_in = lane >> 2;        // n index (q head within the n-tile)
         const int k_in = (lane & 3) * 2;   // k index pair
+        if constexpr (QK == 0) {
 #pragma unroll
-        for (int nt = 0; nt < NTN; ++nt) {
-            const int h = nt * 8 + h_in;
-            const uint32_t *row = reinterpret_cast<const uint32_t *>(qslot + h * D * sizeof(T));
+            for (int nt = 0; nt < NTN; ++nt) {
+                const int h = nt * 8 + h_in;
+                const uint32_t *row = reinterpret_cast<const uint32_t *>(qslot + h * D * sizeof(T));
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                qb[nt][ks][0] = (h < gca) ? row[(ks * 16 + k_in) >> 1] : 0u;
-                qb[nt][ks][1] = (h < gca) ? row[(ks * 16 + 8 + k_in) >> 1] : 0u;
+                for (int ks = 0; ks < KS; ++ks) {
+                    qb[nt][ks][0] = (h < gca) ? row[(ks * 16 + k_in) >> 1] : 0u;
+                    qb[nt][ks][1] = (h < gca) ? row[(ks * 16 + 8 + k_in) >> 1] : 0u;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt) {
+                const int h = nt * 8 + h_in;
+                const T *row = reinterpret_cast<const T *>(qslot + h * D * sizeof(T));
+                // the four lanes of head h hold all D of its elements
+                float amax = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int d = ks * 16 + (j >> 1) * 8 + k_in + (j & 1);
+                        const float x = h < gca ? Elem<T>::to_f32(row[d]) : 0.f;
+                        amax = fmaxf(amax, fabsf(x));
+                    }
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                // amax < 2^(F+1); scaling by 2^-e, e = max(0, F - 14), keeps |q| < 2^15
+                const int F = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+                const int e = F > 14 ? F - 14 : 0;
+                const float mul = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int d = ks * 16 + half * 8 + k_in;
+                        const float x0 = h < gca ? Elem<T>::to_f32(row[d]) * mul : 0.f;
+                        const float x1 = h < gca ? Elem<T>::to_f32(row[d + 1]) * mul : 0.f;
+                        __half2 q2 = __floats2half2_rn(x0, x1);
+                        qb[nt][ks][half] = *reinterpret_cast<uint32_t *>(&q2);
+                    }
+                // score heads of this thread: 8nt + 2(lane%4) + hh, whose shift
+                // sits with lanes 4 * (2(lane%4) + hh)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int es = __shfl_sync(0xffffffffu, e, ((lane & 3) * 2 + hh) * 4);
+                    sl2[nt][hh] = scale_log2 * __uint_as_float((uint32_t)(127 + es) << 23);
+                }
             }
         }
     }
 
-    __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int ntok, int warp, int lane) {
+    // ksc / vsc: the tile's K and V row scales (8-bit caches only)
+    __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int ntok, int warp, int lane,
+                                         const float *ksc = nullptr, const float *vsc = nullptr) {
         const int r0 = 16 * warp;
         const int nval = ntok - r0;
         if (nval <= 0) return;
@@ -377,19 +450,37 @@ struct Consumer<T, D, GMAX, true> {
                 ldsm_x4(swz(sK, row, chunk), a0, a1, a2, a3);
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt)
-                    MmaOp<T>::run(s[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+                    MmaOp<MT>::run(s[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
             }
         }
         // ---- online softmax (tokens rA, rB; heads 8nt + 2*(lane%4) + hh)
         const int rA = r0 + (lane >> 2), rB = rA + 8;
         const bool vA = rA < ntok, vB = rB < ntok;
+        // 8-bit caches: row scales of K (into the scores) and V (into p)
+        float ksA = 1.f, ksB = 1.f, fvA = 1.f, fvB = 1.f, ratio = 1.f;
+        if constexpr (QK != 0) {
+            ksA = vA ? ksc[rA] : 0.f;
+            ksB = vB ? ksc[rB] : 0.f;
+            const float vsA = vA ? vsc[rA] : 0.f, vsB = vB ? vsc[rB] : 0.f;
+            float vmax = fmaxf(vsA, vsB);
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
+            if (!(vmax > 0.f)) vmax = 1.f;   // all-zero V rows: p' = 0 whatever vmax is
+            fvA = vsA / vmax;
+            fvB = vsB / vmax;
+            ratio = sigma / vmax;            // the accumulator moves from o/sigma to o/vmax
+            sigma = vmax;
+        }
         float p[NTN][4];
 #pragma unroll
         for (int nt = 0; nt < NTN; ++nt) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const float sa = vA ? s[nt][hh] * scale_log2 : -CUDART_INF_F;
-                const float sb = vB ? s[nt][2 + hh] * scale_log2 : -CUDART_INF_F;
+                const float fa = QK != 0 ? ksA * sl2[nt][hh] : scale_log2;
+                const float fb = QK != 0 ? ksB * sl2[nt][hh] : scale_log2;
+                const float sa = vA ? s[nt][hh] * fa : -CUDART_INF_F;
+                const float sb = vB ? s[nt][2 + hh] * fb : -CUDART_INF_F;
                 float mx = fmaxf(sa, sb);
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -400,10 +491,15 @@ struct Consumer<T, D, GMAX, true> {
                 p[nt][hh] = exp2f(sa - mn);
                 p[nt][2 + hh] = exp2f(sb - mn);
                 l[nt][hh] = l[nt][hh] * alpha + p[nt][hh] + p[nt][2 + hh];
+                const float ar = QK != 0 ? alpha * ratio : alpha;
 #pragma unroll
                 for (int ks = 0; ks < KS; ++ks) {
-                    acc[ks][nt][hh] *= alpha;
-                    acc[ks][nt][2 + hh] *= alpha;
+                    acc[ks][nt][hh] *= ar;
+                    acc[ks][nt][2 + hh] *= ar;
+                }
+                if constexpr (QK != 0) {   // p' = p * s_v / vmax for the PV product
+                    p[nt][hh] *= fvA;
+                    p[nt][2 + hh] *= fvB;
                 }
             }
         }
@@ -414,11 +510,11 @@ struct Consumer<T, D, GMAX, true> {
         for (int nt = 0; nt < NTN; ++nt) {
             const uint32_t hi = pbuf + nt * 512, lo = hi + 256;
             float r00, r01, r10, r11;
-            const uint32_t hA = Elem<T>::pack2(p[nt][0], p[nt][1], r00, r01);
-            const uint32_t hB = Elem<T>::pack2(p[nt][2], p[nt][3], r10, r11);
+            const uint32_t hA = Elem<MT>::pack2(p[nt][0], p[nt][1], r00, r01);
+            const uint32_t hB = Elem<MT>::pack2(p[nt][2], p[nt][3], r10, r11);
             float d0, d1;
-            const uint32_t lA = Elem<T>::pack2(p[nt][0] - r00, p[nt][1] - r01, d0, d1);
-            const uint32_t lB = Elem<T>::pack2(p[nt][2] - r10, p[nt][3] - r11, d0, d1);
+            const uint32_t lA = Elem<MT>::pack2(p[nt][0] - r00, p[nt][1] - r01, d0, d1);
+            const uint32_t lB = Elem<MT>::pack2(p[nt][2] - r10, p[nt][3] - r11, d0, d1);
             const uint32_t offA = (lane >> 2) * 16 + (lane & 3) * 4;
             const uint32_t offB = offA + 8 * 16;
             asm volatile("st.shared.u32 [%0], %1;" ::"r"(hi + offA), "r"(hA) : "memory");
@@ -443,8 +539,8 @@ struct Consumer<T, D, GMAX, true> {
                 ldsm_x4_t(swz(sV, tok, chunk), a0, a1, a2, a3);
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt) {
-                    MmaOp<T>::run(acc[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
-                    MmaOp<T>::run(acc[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                    MmaOp<MT>::run(acc[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                    MmaOp<MT>::run(acc[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
                 }
             }
         }
@@ -467,19 +563,73 @@ struct Consumer<T, D, GMAX, true> {
                     comb_l[warp * GMAX + h] = lt;
                 }
             }
+            const float sg = QK != 0 ? sigma : 1.f;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int h = nt * 8 + (lane & 3) * 2;
                 const int d = mt * 16 + (lane >> 2);
                 float *o = comb_o + (warp * GMAX + h) * D;
-                o[d] = acc[mt][nt][0];
-                o[D + d] = acc[mt][nt][1];
-                o[d + 8] = acc[mt][nt][2];
-                o[D + d + 8] = acc[mt][nt][3];
+                o[d] = acc[mt][nt][0] * sg;
+                o[D + d] = acc[mt][nt][1] * sg;
+                o[d + 8] = acc[mt][nt][2] * sg;
+                o[D + d + 8] = acc[mt][nt][3] * sg;
             }
         }
     }
 };
+
+// ---------------------------------------------------------------------------
+// 8-bit codes -> fp16 (exact: every int8 and E4M3 value is an fp16 value)
+// ---------------------------------------------------------------------------
+// Four codes (lowest address in the low byte) -> two fp16 pairs.
+template <int QK>
+__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    if constexpr (QK == kQuantInt8) {
+        // byte b + 128 placed under the fp16 exponent of 1024 (0x64nn) reads
+        // as 1024 + b + 128; subtracting 1152 leaves b exactly
+        const uint32_t u = w ^ 0x80808080u;
+        uint32_t a, b;
+        asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+        asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
+        __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+        lo = *reinterpret_cast<uint32_t *>(&ha);
+        hi = *reinterpret_cast<uint32_t *>(&hb);
+    } else {
+        const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+        const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+        lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
+        hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
+    }
+}
+
+// Math warp `warp` converts its 16 rows of an 8-bit tile (one 128-byte plane
+// per row, D = 128) into the 16-bit tile layout (two planes per row) that
+// the tensor-core tile step reads. Lanes take whole 16-byte chunks.
+template <int QK>
+__device__ __forceinline__ void convert_rows(uint32_t src, uint32_t dst, int warp, int lane) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int i = lane + 32 * k;
+        const int row = 16 * warp + (i >> 3), ch = i & 7;
+        uint32_t w0, w1, w2, w3;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                     : "r"(swz(src, row, ch)));
+        uint32_t h[8];
+        codes_to_f16<QK>(w0, h[0], h[1]);
+        codes_to_f16<QK>(w1, h[2], h[3]);
+        codes_to_f16<QK>(w2, h[4], h[5]);
+        codes_to_f16<QK>(w3, h[6], h[7]);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst, row, 2 * ch)),
+                     "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst, row, 2 * ch + 1)),
+                     "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                     : "memory");
+    }
+}
 
 // ---------------------------------------------------------------------------
 // log-sum-exp merge of one warp's slice of a unit cut by CTA boundaries
@@ -555,10 +705,10 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
 // ---------------------------------------------------------------------------
 // the split-K kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA>
+template <typename T, int D, int GMAX, bool MMA, int QK>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_split_kernel(const DecodeParams p) {
-    using Cfg = SplitCfg<T, D, GMAX, MMA>;
+    using Cfg = SplitCfg<T, D, GMAX, MMA, QK>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -616,7 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // zero-filled (src-size 0): no address outside the pool is formed
         // and the math warps never see stale or garbage rows.
         constexpr int LA = 8;
-        constexpr int CPR = Cfg::ROWB / 16;          // 16-byte chunks per row
+        constexpr int CPR = Cfg::ROWB / 16;          // 16-byte chunks per K/V row
+        constexpr int CPRQ = Cfg::QROWB / 16;        // 16-byte chunks per q row
         const int pt = tid - kConsumerWarps * 32;     // 0 .. kProducerThreads-1
         const int bpt = PKV_TILE_TOKENS / p.B;        // blocks per tile
         const int tpb = kProducerThreads / bpt;       // producer threads per block
@@ -667,7 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t full = full0 + 8 * stage;
                 const uint32_t sK = sbase + stage * Cfg::STAGE;
                 const uint32_t sV = sK + Cfg::KVB;
-                const uint32_t sQ = sV + Cfg::KVB;
+                const uint32_t sS = sV + Cfg::KVB;           // scales (8-bit caches)
+                const uint32_t sQ = sS + Cfg::SCB;
                 // ---- K and V rows of block jblk of this tile
                 const bool blk_ok = e >= 0 && e < p.NB;
                 if (tb == 0 && jblk * p.B < ntok && !blk_ok) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
@@ -682,11 +834,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     cp_async_16(swz(sK, row, ch), kpool + off, v);
                     cp_async_16(swz(sV, row, ch), vpool + off, v);
                 }
+                if constexpr (QK != 0) {
+                    // the block's B row scales, 4 rows per 16-byte copy; the
+                    // bytes of rows past the context are zeroed, not read
+                    if (tb < p.B / 4) {
+                        const int row = jblk * p.B + 4 * tb;
+                        const int nrow = blk_ok ? min(4, max(0, ntok - row)) : 0;
+                        const size_t so = blk_ok ? ((size_t)e * p.Hk + g) * p.B + 4 * tb : 0;
+                        cp_async_16_n(sS + row * 4, p.ks + so, 4u * nrow);
+                        cp_async_16_n(sS + 256 + row * 4, p.vs + so, 4u * nrow);
+                    }
+                }
                 // ---- q rows of the unit ride along with its first tile
                 if (first) {
                     const uint8_t *qsrc = static_cast<const uint8_t *>(p.q) +
-                                          ((size_t)cur.s * p.Hq + h0) * Cfg::ROWB;
-                    for (int i = pt; i < gca * CPR; i += kProducerThreads)
+                                          ((size_t)cur.s * p.Hq + h0) * Cfg::QROWB;
+                    for (int i = pt; i < gca * CPRQ; i += kProducerThreads)
                         cp_async_16(sQ + i * 16, qsrc + (size_t)i * 16, true);
                 }
                 cp_async_arrive_noinc(full);
@@ -714,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ======================= consumer warps =======================
-    Consumer<T, D, GMAX, MMA> cs;
+    Consumer<T, D, GMAX, MMA, QK> cs;
     if constexpr (MMA) cs.pbuf = sbase + Cfg::OFF_PBUF + warp * Cfg::NTN * 512;
     cs.reset();
     int seg = 0;
@@ -733,9 +896,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sV = sK + Cfg::KVB;
         if (mt.flags & kFirst) {
             cs.reset();
-            cs.load_q(smem + stage * Cfg::STAGE + 2 * Cfg::KVB, mt.gca, p.scale_log2, lane);
+            cs.load_q(smem + stage * Cfg::STAGE + 2 * Cfg::KVB + Cfg::SCB, mt.gca, p.scale_log2,
+                      lane);
         }
-        cs.tile(sK, sV, mt.ntok, warp, lane);
+        if constexpr (QK != 0) {
+            // this warp's 16 rows of codes -> fp16, then the 16-bit tile step
+            const uint32_t cK = sbase + Cfg::OFF_CONV, cV = cK + Cfg::CONV / 2;
+            convert_rows<QK>(sK, cK, warp, lane);
+            convert_rows<QK>(sV, cV, warp, lane);
+            __syncwarp();
+            const float *ksc = reinterpret_cast<const float *>(smem + stage * Cfg::STAGE +
+                                                               2 * Cfg::KVB);
+            cs.tile(cK, cV, mt.ntok, warp, lane, ksc, ksc + PKV_TILE_TOKENS);
+        } else {
+            cs.tile(sK, sV, mt.ntok, warp, lane);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);
 
@@ -807,16 +982,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host-side launch of one variant
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA>
+template <typename T, int D, int GMAX, bool MMA, int QK = 0>
 struct SplitVariant {
-    using Cfg = SplitCfg<T, D, GMAX, MMA>;
+    using Cfg = SplitCfg<T, D, GMAX, MMA, QK>;
 
     static cudaError_t prepare(int dev) {
         static bool done[64] = {false};
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!done[dev]) {
             const size_t smem = Cfg::smem_bytes(kMaxSeqsPerLaunch);
-            cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, GMAX, MMA>,
+            cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, GMAX, MMA, QK>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem);
             if (e != cudaSuccess) return e;
@@ -840,7 +1015,7 @@ struct SplitVariant {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA>, p);
+        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA, QK>, p);
     }
 
     // occupancy of this variant on the current device (queried once per device)
@@ -852,7 +1027,7 @@ struct SplitVariant {
         if (prepare(dev) != cudaSuccess) return 0;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &n, decode_split_kernel<T, D, GMAX, MMA>, kThreads,
+                &n, decode_split_kernel<T, D, GMAX, MMA, QK>, kThreads,
                 Cfg::smem_bytes(kMaxSeqsPerLaunch)) != cudaSuccess)
             return 0;
         cached[dev] = n;

@@ -105,6 +105,14 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, bool 
                  : "memory");
 }
 
+// 16-byte copy of which only the first `nbytes` (0..16) are read; the rest of
+// the destination is zeroed.
+__device__ __forceinline__ void cp_async_16_n(uint32_t dst, const void *src, uint32_t nbytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(nbytes)
+                 : "memory");
+}
+
 // One arrival on `bar` once every cp.async this thread issued so far has
 // landed (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

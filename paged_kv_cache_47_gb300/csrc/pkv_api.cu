@@ -71,6 +71,22 @@ pkv_status check_cache(const pkv_cache_desc *c) {
     return PKV_OK;
 }
 
+pkv_status check_qcache(const pkv_qcache_desc *c) {
+    if (!c) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
+    if (c->code_dtype != PKV_INT8 && c->code_dtype != PKV_FP8_E4M3)
+        return fail(PKV_ERR_UNSUPPORTED, "code_dtype %d (supported: PKV_INT8, PKV_FP8_E4M3)",
+                    c->code_dtype);
+    if (c->act_dtype != PKV_F16 && c->act_dtype != PKV_BF16)
+        return fail(PKV_ERR_UNSUPPORTED, "act_dtype %d (supported: PKV_F16, PKV_BF16)", c->act_dtype);
+    if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32)
+        return fail(PKV_ERR_UNSUPPORTED, "block_size %d (supported: 8, 16, 32)", c->block_size);
+    if (c->head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (8-bit caches support 128)", c->head_dim);
+    if (c->num_kv_heads < 1) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads %d", c->num_kv_heads);
+    if (c->num_blocks < 1) return fail(PKV_ERR_INVALID_ARG, "num_blocks %d", c->num_blocks);
+    return PKV_OK;
+}
+
 // ---------------------------------------------------------------- decode plan
 struct Plan {
     int G, GC, NC, U;
@@ -79,17 +95,17 @@ struct Plan {
     const pkv::DecodeVariant *variant;
 };
 
-pkv_status make_plan(const pkv_cache_desc *c, int Hq, const pkv_decode_options *o, Plan *pl) {
-    if (Hq < 1 || Hq % c->num_kv_heads != 0)
+// Head grouping and math path shared by every decode entry point.
+pkv_status plan_groups(int Hk, int Hq, const pkv_decode_options *o, bool half, Plan *pl) {
+    if (Hq < 1 || Hq % Hk != 0)
         return fail(PKV_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
-                    Hq, c->num_kv_heads);
+                    Hq, Hk);
     const int consumer = o ? o->consumer : 0;
     if (consumer < 0 || consumer > 2) return fail(PKV_ERR_INVALID_ARG, "consumer %d", consumer);
-    pl->G = Hq / c->num_kv_heads;
+    pl->G = Hq / Hk;
     pl->GC = pl->G < pkv::kMaxHeadsPerUnit ? pl->G : pkv::kMaxHeadsPerUnit;
     pl->NC = (pl->G + pl->GC - 1) / pl->GC;
-    pl->U = c->num_kv_heads * pl->NC;
-    const bool half = c->dtype != PKV_F32;
+    pl->U = Hk * pl->NC;
     if (consumer == 2 && !half)
         return fail(PKV_ERR_UNSUPPORTED, "tensor-core math needs fp16 or bf16 K/V");
     // 16-bit K/V go to the tensor cores whatever the group size: with one
@@ -103,10 +119,27 @@ pkv_status make_plan(const pkv_cache_desc *c, int Hq, const pkv_decode_options *
         while (g < pl->GC) g <<= 1;
         pl->gmax = g;
     }
+    return PKV_OK;
+}
+
+pkv_status make_plan(const pkv_cache_desc *c, int Hq, const pkv_decode_options *o, Plan *pl) {
+    pkv_status st = plan_groups(c->num_kv_heads, Hq, o, c->dtype != PKV_F32, pl);
+    if (st != PKV_OK) return st;
     const int D = c->head_dim;
     pl->variant = c->dtype == PKV_F32   ? pkv::find_variant_f32(D, pl->gmax, pl->mma)
                   : c->dtype == PKV_F16 ? pkv::find_variant_f16(D, pl->gmax, pl->mma)
                                         : pkv::find_variant_bf16(D, pl->gmax, pl->mma);
+    if (!pl->variant) return fail(PKV_ERR_UNSUPPORTED, "no kernel variant for this shape");
+    return PKV_OK;
+}
+
+pkv_status make_plan_quant(const pkv_qcache_desc *c, int Hq, const pkv_decode_options *o,
+                           Plan *pl) {
+    if (o && o->consumer == 1)
+        return fail(PKV_ERR_UNSUPPORTED, "8-bit caches use the tensor-core math (consumer 1 given)");
+    pkv_status st = plan_groups(c->num_kv_heads, Hq, o, true, pl);
+    if (st != PKV_OK) return st;
+    pl->variant = pkv::find_variant_quant(c->code_dtype, c->act_dtype, c->head_dim, pl->gmax);
     if (!pl->variant) return fail(PKV_ERR_UNSUPPORTED, "no kernel variant for this shape");
     return PKV_OK;
 }
@@ -169,6 +202,42 @@ cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t s) {
     return cudaEventRecord(ev, s);
 }
 
+// Validate whole-block copy pairs on the host and launch the copies of
+// block_bytes per block in both pools (batches of kCopyPairsPerLaunch).
+pkv_status copy_blocks(int NB, const int64_t *pairs, int n, void *k_pool, void *v_pool,
+                       size_t block_bytes, cudaStream_t stream) {
+    if (n < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs %d", n);
+    if (n == 0) return PKV_OK;
+    if (!pairs || !k_pool || !v_pool) return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16))
+        return fail(PKV_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+    std::unordered_set<int64_t> srcs, dsts;
+    for (int i = 0; i < n; ++i) {
+        const int64_t s = pairs[2 * i], d = pairs[2 * i + 1];
+        if (s < 0 || s >= NB || d < 0 || d >= NB)
+            return fail(PKV_ERR_INVALID_ARG, "pair %d (%lld -> %lld) outside [0, %d)", i,
+                        (long long)s, (long long)d, NB);
+        if (!dsts.insert(d).second)
+            return fail(PKV_ERR_INVALID_ARG, "block %lld is the destination of two pairs", (long long)d);
+        srcs.insert(s);
+    }
+    for (int64_t d : dsts)
+        if (srcs.count(d))
+            return fail(PKV_ERR_INVALID_ARG, "block %lld is both a source and a destination",
+                        (long long)d);
+    for (int base = 0; base < n; base += pkv::kCopyPairsPerLaunch) {
+        pkv::CopyPairs cp;
+        const int m = n - base < pkv::kCopyPairsPerLaunch ? n - base : pkv::kCopyPairsPerLaunch;
+        for (int i = 0; i < m; ++i) {
+            cp.src[i] = pairs[2 * (base + i)];
+            cp.dst[i] = pairs[2 * (base + i) + 1];
+        }
+        cudaError_t e = pkv::launch_block_copy(cp, m, k_pool, v_pool, block_bytes, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
+    }
+    return PKV_OK;
+}
+
 }  // namespace
 
 namespace pkv {
@@ -224,41 +293,28 @@ pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pa
                           int32_t num_pairs, void *k_pool, void *v_pool, void *stream) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
-    if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs %d", num_pairs);
-    if (num_pairs == 0) return PKV_OK;
-    if (!src_dst_pairs || !k_pool || !v_pool)
-        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
-    if (!aligned(k_pool, 16) || !aligned(v_pool, 16))
-        return fail(PKV_ERR_INVALID_ARG, "pools must be 16-byte aligned");
-    std::unordered_set<int64_t> srcs, dsts;
-    for (int i = 0; i < num_pairs; ++i) {
-        const int64_t s = src_dst_pairs[2 * i], d = src_dst_pairs[2 * i + 1];
-        if (s < 0 || s >= cache->num_blocks || d < 0 || d >= cache->num_blocks)
-            return fail(PKV_ERR_INVALID_ARG, "pair %d (%lld -> %lld) outside [0, %d)", i,
-                        (long long)s, (long long)d, cache->num_blocks);
-        if (!dsts.insert(d).second)
-            return fail(PKV_ERR_INVALID_ARG, "block %lld is the destination of two pairs", (long long)d);
-        srcs.insert(s);
-    }
-    for (int64_t d : dsts)
-        if (srcs.count(d))
-            return fail(PKV_ERR_INVALID_ARG, "block %lld is both a source and a destination",
-                        (long long)d);
     const size_t block_bytes = (size_t)cache->num_kv_heads * cache->block_size * cache->head_dim *
                                elem_bytes(cache->dtype);
-    for (int base = 0; base < num_pairs; base += pkv::kCopyPairsPerLaunch) {
-        pkv::CopyPairs cp;
-        const int n = num_pairs - base < pkv::kCopyPairsPerLaunch ? num_pairs - base
-                                                                 : pkv::kCopyPairsPerLaunch;
-        for (int i = 0; i < n; ++i) {
-            cp.src[i] = src_dst_pairs[2 * (base + i)];
-            cp.dst[i] = src_dst_pairs[2 * (base + i) + 1];
-        }
-        cudaError_t e = pkv::launch_block_copy(cp, n, k_pool, v_pool, block_bytes,
-                                               static_cast<cudaStream_t>(stream));
-        if (e != cudaSuccess) return cuda_fail(e, "block copy launch");
-    }
-    return PKV_OK;
+    return copy_blocks(cache->num_blocks, src_dst_pairs, num_pairs, k_pool, v_pool, block_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_block_copy_quant(const pkv_qcache_desc *cache, const int64_t *src_dst_pairs,
+                                int32_t num_pairs, void *k_codes, void *v_codes, float *k_scales,
+                                float *v_scales, void *stream) {
+    pkv_status st = check_qcache(cache);
+    if (st != PKV_OK) return st;
+    if (num_pairs > 0 && (!k_scales || !v_scales))
+        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (num_pairs > 0 && (!aligned(k_scales, 16) || !aligned(v_scales, 16)))
+        return fail(PKV_ERR_INVALID_ARG, "scale pools must be 16-byte aligned");
+    const size_t rows = (size_t)cache->num_kv_heads * cache->block_size;
+    // pairs are checked by the first call; the second cannot fail on them
+    if ((st = copy_blocks(cache->num_blocks, src_dst_pairs, num_pairs, k_codes, v_codes,
+                          rows * cache->head_dim, static_cast<cudaStream_t>(stream))) != PKV_OK)
+        return st;
+    return copy_blocks(cache->num_blocks, src_dst_pairs, num_pairs, k_scales, v_scales,
+                       rows * sizeof(float), static_cast<cudaStream_t>(stream));
 }
 
 size_t pkv_decode_workspace_bytes_ex(const pkv_cache_desc *cache, int32_t num_q_heads,
@@ -281,6 +337,118 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc *cache, int32_t num_seqs,
     return pkv_decode_workspace_bytes_ex(cache, num_q_heads, 0);
 }
 
+}  // extern "C"
+
+namespace {
+
+// What one decode call reads and writes, whatever the cache format.
+struct DecodeArgs {
+    int NB, B, Hk, D;
+    int q_es;                        // bytes of one q element
+    const void *q;
+    int S, Hq;
+    const void *kp, *vp;
+    const float *ks, *vs;            // row scales (8-bit caches) or NULL
+    const int32_t *tables;
+    int M;
+    const int32_t *lens;
+    float scale;
+    void *out;
+    int out_dtype;
+    void *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+    const pkv_decode_options *opts;
+};
+
+// Host checks shared by the decode entry points (after the cache descriptor).
+pkv_status check_decode_args(const DecodeArgs &a) {
+    if (a.S < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d", a.S);
+    if (!valid_dtype(a.out_dtype)) return fail(PKV_ERR_UNSUPPORTED, "out_dtype %d", a.out_dtype);
+    if (a.M < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", a.M);
+    if (!isfinite(a.scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+    return PKV_OK;
+}
+
+pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
+    if (a.S == 0) return PKV_OK;
+    if (!a.q || !a.kp || !a.vp || !a.tables || !a.lens || !a.out)
+        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (!aligned(a.q, 16) || !aligned(a.kp, 16) || !aligned(a.vp, 16) ||
+        !aligned(a.out, elem_bytes(a.out_dtype)) || !aligned(a.tables, 4) || !aligned(a.lens, 4))
+        return fail(PKV_ERR_INVALID_ARG, "q and the pools must be 16-byte aligned");
+    // flattened tile count must fit in int32
+    const int64_t max_tiles_per_unit =
+        ((int64_t)a.M * a.B + PKV_TILE_TOKENS - 1) / PKV_TILE_TOKENS;
+    const int64_t chunk_seqs = a.S < pkv::kMaxSeqsPerLaunch ? a.S : pkv::kMaxSeqsPerLaunch;
+    if (chunk_seqs * pl.U * max_tiles_per_unit >= (int64_t)INT32_MAX)
+        return fail(PKV_ERR_UNSUPPORTED, "batch x context too large for one launch");
+
+    int C = a.opts ? a.opts->num_ctas : 0;
+    pkv_status st;
+    if (C < 0 || C > PKV_MAX_DECODE_CTAS)
+        return fail(PKV_ERR_INVALID_ARG, "num_ctas %d outside [0, %d]", C, PKV_MAX_DECODE_CTAS);
+    if (C == 0 && (st = default_ctas(pl, &C)) != PKV_OK) return st;
+    const size_t need = workspace_for(C, pl.GC, a.D);
+    if (C > 1 && (!a.ws || a.ws_bytes < need))
+        return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                    a.ws ? a.ws_bytes : (size_t)0);
+    if (a.ws && !aligned(a.ws, 16))
+        return fail(PKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+
+    unsigned *err = nullptr;
+    if ((st = device_error_ptr(&err)) != PKV_OK) return st;
+
+    const int oes = elem_bytes(a.out_dtype);
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    if (a.opts)
+        for (int i = 0; i < 2; ++i) ev[i] = static_cast<cudaEvent_t>(a.opts->timing_events[i]);
+
+    for (int s0 = 0; s0 < a.S; s0 += pkv::kMaxSeqsPerLaunch) {
+        const int S = a.S - s0 < pkv::kMaxSeqsPerLaunch ? a.S - s0 : pkv::kMaxSeqsPerLaunch;
+        pkv::DecodeParams p;
+        p.q = static_cast<const uint8_t *>(a.q) + (size_t)s0 * a.Hq * a.D * a.q_es;
+        p.out = static_cast<uint8_t *>(a.out) + (size_t)s0 * a.Hq * a.D * oes;
+        p.out_dtype = a.out_dtype;
+        p.block_tables = a.tables + (size_t)s0 * a.M;
+        p.context_lens = a.lens + s0;
+        p.M = a.M;
+        p.S = S;
+        p.Hq = a.Hq;
+        p.Hk = a.Hk;
+        p.G = pl.G;
+        p.NC = pl.NC;
+        p.GC = pl.GC;
+        p.U = pl.U;
+        p.B = a.B;
+        p.NB = a.NB;
+        p.scale_log2 = a.scale * 1.4426950408889634f;
+        p.ws_cnt = static_cast<unsigned *>(a.ws);
+        p.ws_o = a.ws ? reinterpret_cast<float *>(static_cast<uint8_t *>(a.ws) + kCounterBytes)
+                      : nullptr;
+        p.ws_lse = a.ws ? p.ws_o + (size_t)C * 2 * pl.GC * a.D : nullptr;
+        p.C = C;
+        p.err = err;
+        p.kp = a.kp;
+        p.vp = a.vp;
+        p.ks = a.ks;
+        p.vs = a.vs;
+        const bool first = s0 == 0;
+        cudaError_t e;
+        if (first && ev[0] && (e = record_timing_event(ev[0], a.stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+        if ((e = pl.variant->launch(p, a.stream)) != cudaSuccess)
+            return cuda_fail(e, "split-K decode launch");
+        if (first && ev[1] && (e = record_timing_event(ev[1], a.stream)) != cudaSuccess)
+            return cuda_fail(e, "cudaEventRecord");
+    }
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, int32_t num_seqs,
                                    int32_t num_q_heads, const void *k_pool, const void *v_pool,
                                    const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -289,86 +457,74 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
                                    void *stream, const pkv_decode_options *options) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
-    if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d", num_seqs);
-    if (!valid_dtype(out_dtype)) return fail(PKV_ERR_UNSUPPORTED, "out_dtype %d", out_dtype);
-    if (max_blocks_per_seq < 1)
-        return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", max_blocks_per_seq);
-    if (!isfinite(scale)) return fail(PKV_ERR_INVALID_ARG, "scale is not finite");
+    DecodeArgs a{cache->num_blocks, cache->block_size, cache->num_kv_heads, cache->head_dim,
+                 elem_bytes(cache->dtype), q, num_seqs, num_q_heads, k_pool, v_pool, nullptr,
+                 nullptr, block_tables, max_blocks_per_seq, context_lens, scale, out, out_dtype,
+                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream), options};
+    if ((st = check_decode_args(a)) != PKV_OK) return st;
     Plan pl;
     if ((st = make_plan(cache, num_q_heads, options, &pl)) != PKV_OK) return st;
-    if (num_seqs == 0) return PKV_OK;
-    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out)
+    return run_decode(pl, a);
+}
+
+pkv_status pkv_decode_attention_quant(const pkv_qcache_desc *cache, const void *q,
+                                      int32_t num_seqs, int32_t num_q_heads, const void *k_codes,
+                                      const void *v_codes, const float *k_scales,
+                                      const float *v_scales, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                      float scale, void *out, int32_t out_dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream,
+                                      const pkv_decode_options *options) {
+    pkv_status st = check_qcache(cache);
+    if (st != PKV_OK) return st;
+    DecodeArgs a{cache->num_blocks, cache->block_size, cache->num_kv_heads, cache->head_dim,
+                 elem_bytes(cache->act_dtype), q, num_seqs, num_q_heads, k_codes, v_codes,
+                 k_scales, v_scales, block_tables, max_blocks_per_seq, context_lens, scale, out,
+                 out_dtype, workspace, workspace_bytes, static_cast<cudaStream_t>(stream), options};
+    if ((st = check_decode_args(a)) != PKV_OK) return st;
+    Plan pl;
+    if ((st = make_plan_quant(cache, num_q_heads, options, &pl)) != PKV_OK) return st;
+    if (num_seqs > 0 && (!k_scales || !v_scales))
         return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
-    if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(v_pool, 16) ||
-        !aligned(out, elem_bytes(out_dtype)) || !aligned(block_tables, 4) ||
-        !aligned(context_lens, 4))
-        return fail(PKV_ERR_INVALID_ARG, "q and the pools must be 16-byte aligned");
-    // flattened tile count must fit in int32
-    const int64_t max_tiles_per_unit =
-        ((int64_t)max_blocks_per_seq * cache->block_size + PKV_TILE_TOKENS - 1) / PKV_TILE_TOKENS;
-    const int64_t chunk_seqs = num_seqs < pkv::kMaxSeqsPerLaunch ? num_seqs : pkv::kMaxSeqsPerLaunch;
-    if (chunk_seqs * pl.U * max_tiles_per_unit >= (int64_t)INT32_MAX)
-        return fail(PKV_ERR_UNSUPPORTED, "batch x context too large for one launch");
+    if (!aligned(k_scales, 16) || !aligned(v_scales, 16))
+        return fail(PKV_ERR_INVALID_ARG, "scale pools must be 16-byte aligned");
+    return run_decode(pl, a);
+}
 
-    int C = options ? options->num_ctas : 0;
-    if (C < 0 || C > PKV_MAX_DECODE_CTAS)
-        return fail(PKV_ERR_INVALID_ARG, "num_ctas %d outside [0, %d]", C, PKV_MAX_DECODE_CTAS);
-    if (C == 0 && (st = default_ctas(pl, &C)) != PKV_OK) return st;
-    const size_t need = workspace_for(C, pl.GC, cache->head_dim);
-    if (C > 1 && (!workspace || workspace_bytes < need))
-        return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
-                    workspace ? workspace_bytes : (size_t)0);
-    if (workspace && !aligned(workspace, 16))
-        return fail(PKV_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+size_t pkv_decode_quant_workspace_bytes(const pkv_qcache_desc *cache, int32_t num_q_heads,
+                                        int32_t num_ctas) {
+    if (check_qcache(cache) != PKV_OK) return 0;
+    if (num_q_heads < 1 || num_q_heads % cache->num_kv_heads != 0 || num_ctas < 0 ||
+        num_ctas > PKV_MAX_DECODE_CTAS)
+        return 0;
+    int C = num_ctas;
+    if (C == 0 && max_default_ctas(&C) != PKV_OK) return 0;
+    const int G = num_q_heads / cache->num_kv_heads;
+    const int GC = G < pkv::kMaxHeadsPerUnit ? G : pkv::kMaxHeadsPerUnit;
+    return workspace_for(C, GC, cache->head_dim);
+}
 
+pkv_status pkv_append_quant(const pkv_qcache_desc *cache, const void *k_new, const void *v_new,
+                            const int64_t *slot_mapping, int32_t num_tokens, void *k_codes,
+                            void *v_codes, float *k_scales, float *v_scales, void *stream) {
+    pkv_status st = check_qcache(cache);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales)
+        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_codes, 16) ||
+        !aligned(v_codes, 16) || !aligned(k_scales, 16) || !aligned(v_scales, 16) ||
+        !aligned(slot_mapping, 8))
+        return fail(PKV_ERR_INVALID_ARG, "pointers must be 16-byte aligned (slot_mapping 8)");
     unsigned *err = nullptr;
     if ((st = device_error_ptr(&err)) != PKV_OK) return st;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int es = elem_bytes(cache->dtype);
-    const int oes = elem_bytes(out_dtype);
-    const int D = cache->head_dim;
-    cudaEvent_t ev[2] = {nullptr, nullptr};
-    if (options)
-        for (int i = 0; i < 2; ++i) ev[i] = static_cast<cudaEvent_t>(options->timing_events[i]);
-
-    for (int s0 = 0; s0 < num_seqs; s0 += pkv::kMaxSeqsPerLaunch) {
-        const int S = num_seqs - s0 < pkv::kMaxSeqsPerLaunch ? num_seqs - s0 : pkv::kMaxSeqsPerLaunch;
-        pkv::DecodeParams p;
-        p.q = static_cast<const uint8_t *>(q) + (size_t)s0 * num_q_heads * D * es;
-        p.out = static_cast<uint8_t *>(out) + (size_t)s0 * num_q_heads * D * oes;
-        p.out_dtype = out_dtype;
-        p.block_tables = block_tables + (size_t)s0 * max_blocks_per_seq;
-        p.context_lens = context_lens + s0;
-        p.M = max_blocks_per_seq;
-        p.S = S;
-        p.Hq = num_q_heads;
-        p.Hk = cache->num_kv_heads;
-        p.G = pl.G;
-        p.NC = pl.NC;
-        p.GC = pl.GC;
-        p.U = pl.U;
-        p.B = cache->block_size;
-        p.NB = cache->num_blocks;
-        p.scale_log2 = scale * 1.4426950408889634f;
-        p.ws_cnt = static_cast<unsigned *>(workspace);
-        p.ws_o = workspace ? reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
-                                                       kCounterBytes)
-                           : nullptr;
-        p.ws_lse = workspace ? p.ws_o + (size_t)C * 2 * pl.GC * D : nullptr;
-        p.C = C;
-        p.err = err;
-        p.kp = k_pool;
-        p.vp = v_pool;
-        const bool first = s0 == 0;
-        cudaError_t e;
-        if (first && ev[0] && (e = record_timing_event(ev[0], s)) != cudaSuccess)
-            return cuda_fail(e, "cudaEventRecord");
-        if ((e = pl.variant->launch(p, s)) != cudaSuccess)
-            return cuda_fail(e, "split-K decode launch");
-        if (first && ev[1] && (e = record_timing_event(ev[1], s)) != cudaSuccess)
-            return cuda_fail(e, "cudaEventRecord");
-    }
+    cudaError_t e = pkv::launch_append_quant(cache->code_dtype, cache->act_dtype, k_new, v_new,
+                                             slot_mapping, num_tokens, k_codes, v_codes, k_scales,
+                                             v_scales, cache->num_blocks, cache->num_kv_heads,
+                                             cache->block_size, err,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "quantized append launch");
     return PKV_OK;
 }
 

@@ -55,7 +55,8 @@ struct DecodeParams {
                                 //                copy per owning warp
     int C;                      // CTAs of the split-K launch
     unsigned *err;              // device error word
-    const void *kp, *vp;        // pools [NB][Hk][B][D]
+    const void *kp, *vp;        // pools [NB][Hk][B][D] (elements, or 8-bit codes)
+    const float *ks, *vs;       // 8-bit caches: row scales [NB][Hk][B]; else unused
 };
 
 using SplitLaunchFn = cudaError_t (*)(const DecodeParams &, cudaStream_t);
@@ -72,6 +73,9 @@ struct DecodeVariant {
 const DecodeVariant *find_variant_f32(int D, int gmax, bool mma);
 const DecodeVariant *find_variant_f16(int D, int gmax, bool mma);
 const DecodeVariant *find_variant_bf16(int D, int gmax, bool mma);
+// 8-bit caches (decode_quant.cu): code_dtype PKV_INT8 / PKV_FP8_E4M3, q in
+// act_dtype PKV_F16 / PKV_BF16, tensor-core math, D = 128, gmax 8 or 16.
+const DecodeVariant *find_variant_quant(int code_dtype, int act_dtype, int D, int gmax);
 
 // Zero pkv_decode_attention_static's scratch on the current device (after a
 // timed-out wait may have left arrival counters set).
@@ -83,6 +87,12 @@ pkv_status set_last_error(pkv_status st, const char *fmt, ...);
 cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
                           const int64_t *slot_mapping, int num_tokens, void *k_pool, void *v_pool,
                           int NB, int Hk, int B, int D, unsigned *err, cudaStream_t st);
+
+// 8-bit caches (append_quant.cu): D = 128.
+cudaError_t launch_append_quant(int code_dtype, int act_dtype, const void *k_new,
+                                const void *v_new, const int64_t *slots, int num_tokens,
+                                void *k_codes, void *v_codes, float *k_scales, float *v_scales,
+                                int NB, int Hk, int B, unsigned *err, cudaStream_t st);
 
 constexpr int kCopyPairsPerLaunch = 128;
 struct CopyPairs {

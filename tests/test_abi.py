@@ -96,6 +96,45 @@ def test_decode_rejects_bad_arguments(L):
     assert _decode(L, d, q=8) == -1                        # misaligned q
 
 
+def _qdesc(nb=8, b=16, hk=2, d=128, code=binding.PKV_INT8, act=binding.PKV_BF16):
+    return binding.QCacheDesc(nb, b, hk, d, code, act)
+
+
+def _qdecode(L, desc, S=1, Hq=4, q=16, kc=16, vc=16, ks=16, vs=16, opts=None):
+    return L.pkv_decode_attention_quant(ctypes.byref(desc), q, S, Hq, kc, vc, ks, vs, 16, 4, 16,
+                                        1.0, 16, 2, 16, 1 << 30, None,
+                                        ctypes.byref(opts) if opts is not None else None)
+
+
+def test_quant_calls_reject_bad_arguments(L):
+    assert _qdecode(L, _qdesc(code=binding.PKV_BF16)) == -2        # not a code dtype
+    assert _qdecode(L, _qdesc(act=binding.PKV_F32)) == -2          # activations 16-bit only
+    assert _qdecode(L, _qdesc(d=64)) == -2                         # head_dim 128 only
+    assert _qdecode(L, _qdesc(b=12)) == -2
+    assert _qdecode(L, _qdesc(), Hq=3) == -1
+    o = binding.DecodeOptions()
+    o.consumer = 1
+    assert _qdecode(L, _qdesc(), opts=o) == -2                    # CUDA-core math: not for codes
+    assert _qdecode(L, _qdesc(), ks=None) == -1
+    assert _qdecode(L, _qdesc(), vs=8) == -1                       # misaligned scales
+    assert _qdecode(L, _qdesc(), S=0) == 0
+    d = _qdesc()
+    assert L.pkv_append_quant(ctypes.byref(d), 16, 16, 16, 1, 16, 16, None, 16, None) == -1
+    assert L.pkv_append_quant(ctypes.byref(d), 16, 16, 16, 1, 16, 16, 8, 16, None) == -1
+    assert L.pkv_append_quant(ctypes.byref(d), 16, 16, 16, 0, 16, 16, 16, 16, None) == 0
+    p = torch.tensor([[0, 8]], dtype=torch.int64)
+    assert L.pkv_block_copy_quant(ctypes.byref(d), p.data_ptr(), 1, 16, 16, 16, 16, None) == -1
+    assert L.pkv_block_copy_quant(ctypes.byref(d), p.data_ptr(), 1, 16, 16, None, 16, None) == -1
+
+
+def test_quant_workspace_formula(L):
+    d = _qdesc(hk=8)
+    cnt = 4096 * 16
+    assert L.pkv_decode_quant_workspace_bytes(ctypes.byref(d), 32, 10) == cnt + 10 * 2 * 4 * 132 * 4
+    assert L.pkv_decode_quant_workspace_bytes(ctypes.byref(d), 33, 10) == 0
+    assert L.pkv_decode_quant_workspace_bytes(ctypes.byref(_qdesc(d=64)), 32, 10) == 0
+
+
 def test_block_copy_rejects_bad_pairs(L):
     d = _desc(nb=10)
 

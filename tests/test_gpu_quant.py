@@ -1,0 +1,220 @@
+"""Parity of the 8-bit KV cache path (pkv_append_quant, pkv_decode_attention_quant,
+pkv_block_copy_quant) against the CPU oracle.
+
+Each side quantizes the same drawn activations itself: the oracle in C on
+the CPU, the library through pkv_append_quant on the GPU. Codes and scales
+must then match bit for bit (both take the rounding decisions in fp32), and
+the decode over the two caches must match within max-abs 2e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from paged_kv_cache_47_gb300 import binding, build, workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+KINDS = ["int8", "fp8_e4m3"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    binding.lib()
+    yield
+
+
+def _empty_pools(NB, Hk, B, D, device):
+    """Code pools full of 0x7F (E4M3 NaN, int8 127) and NaN scales: entries no
+    append writes must never reach an output."""
+    kc = torch.full((NB, Hk, B, D), 0x7F, dtype=torch.uint8, device=device)
+    ks = torch.full((NB, Hk, B), float("nan"), dtype=torch.float32, device=device)
+    return kc, kc.clone(), ks, ks.clone()
+
+
+def _token_rows(st, vals):
+    """Every context token's K/V activation row and slot, after the step's
+    append (the appended token's row comes from k_new / v_new)."""
+    kp, vp = vals["k_pool"].clone(), vals["v_pool"].clone()
+    oracle.append(vals["k_new"], vals["v_new"], st.slot_mapping, kp, vp)
+    B = kp.shape[2]
+    slots = []
+    for s, L in enumerate(st.context_lens.tolist()):
+        row = st.block_tables[s]
+        slots += [int(row[t // B]) * B + t % B for t in range(L)]
+    sl = torch.tensor(slots, dtype=torch.int64)
+    blk, off = sl // B, sl % B
+    return kp[blk, :, off].contiguous(), vp[blk, :, off].contiguous(), sl
+
+
+def build_caches(kind, st, vals):
+    """The same quantized cache built by the oracle (CPU) and the library (GPU)."""
+    NB, Hk, B, D = vals["k_pool"].shape
+    kr, vr, sl = _token_rows(st, vals)
+    ref = _empty_pools(NB, Hk, B, D, "cpu")
+    oracle.append_quant(kind, kr, vr, sl, *ref)
+    gpu = binding.QuantCache(*_empty_pools(NB, Hk, B, D, "cuda"), kind, kr.dtype)
+    binding.append_quant(kr.cuda(), vr.cuda(), sl.cuda(), gpu)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    return ref, gpu
+
+
+def assert_same_cache(ref, gpu):
+    kc, vc, ks, vs = ref
+    assert torch.equal(gpu.k_codes.cpu(), kc) and torch.equal(gpu.v_codes.cpu(), vc)
+    # scales bit for bit, NaN sentinels included
+    assert torch.equal(gpu.k_scales.cpu().view(torch.int32), ks.view(torch.int32))
+    assert torch.equal(gpu.v_scales.cpu().view(torch.int32), vs.view(torch.int32))
+
+
+def decode_both(kind, st, vals, ref, gpu, num_ctas=0, seq_ids=None):
+    scale = 1.0 / math.sqrt(vals["q"].shape[2])
+    out = binding.decode_attention_quant(vals["q"].cuda(), gpu, st.block_tables.cuda(),
+                                         st.context_lens.cuda(), scale, out_dtype=torch.float32,
+                                         num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    got = out.double().cpu().numpy()
+    want = oracle.decode_quant(kind, vals["q"], *ref, st.block_tables, st.context_lens, scale,
+                               seq_ids=seq_ids)
+    if seq_ids is not None:
+        got = got[list(seq_ids)]
+    return got, want
+
+
+def assert_close(got, want, what=""):
+    assert np.all(np.isfinite(got)), f"non-finite output {what}"
+    err = float(np.max(np.abs(got - want))) if got.size else 0.0
+    assert err <= TOL, f"max abs err {err:.3e} > {TOL} {what}"
+
+
+RAGGED = [1, 2, 15, 16, 17, 63, 64, 65, 127, 129, 300, 1000]
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_append_quant_is_bit_exact(kind, dtype):
+    spec = W.WorkloadSpec("q", len(RAGGED), 32, 8, 128, 16, dtype, 1.0)
+    st, vals = W.make_workload(spec, seed=51, lengths=RAGGED)
+    ref, gpu = build_caches(kind, st, vals)
+    assert_same_cache(ref, gpu)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_append_quant_ties_and_zero_rows(kind):
+    # rows whose largest element makes the scale exactly 1, holding exact
+    # rounding ties, and an all-zero row
+    qmax = 127.0 if kind == "int8" else 448.0
+    if kind == "int8":
+        ties = np.arange(-120.5, 120.5, 1.0)
+    else:
+        v = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+        m = (v[1:] + v[:-1]) / 2
+        ties = np.concatenate([m, -m])
+    D = 128
+    rows = []
+    for i in range(0, len(ties), D - 1):
+        r = np.zeros(D)
+        chunk = ties[i:i + D - 1]
+        r[0] = qmax
+        r[1:1 + len(chunk)] = chunk
+        rows.append(r)
+    rows.append(np.zeros(D))
+    x = torch.tensor(np.stack(rows), dtype=torch.float32).to(torch.float16)
+    assert torch.equal(x.double(), torch.tensor(np.stack(rows)))   # all exact in fp16
+    n = x.shape[0]
+    kn = x.reshape(n, 1, D)
+    vn = -kn
+    sl = torch.arange(n, dtype=torch.int64)
+    NB = (n + 15) // 16
+    ref = _empty_pools(NB, 1, 16, D, "cpu")
+    oracle.append_quant(kind, kn, vn, sl, *ref)
+    gpu = binding.QuantCache(*_empty_pools(NB, 1, 16, D, "cuda"), kind, torch.float16)
+    binding.append_quant(kn.cuda(), vn.cuda(), sl.cuda(), gpu)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    assert_same_cache(ref, gpu)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("dtype,Hq,Hk,B", [("bf16", 32, 8, 16), ("f16", 8, 8, 16),
+                                           ("bf16", 64, 8, 8), ("f16", 40, 2, 32),
+                                           ("bf16", 16, 8, 16)])
+def test_decode_quant_matches_oracle(kind, dtype, Hq, Hk, B):
+    spec = W.WorkloadSpec("q", len(RAGGED), Hq, Hk, 128, B, dtype, 1.0)
+    st, vals = W.make_workload(spec, seed=52, lengths=RAGGED)
+    ref, gpu = build_caches(kind, st, vals)
+    got, want = decode_both(kind, st, vals, ref, gpu, num_ctas=9)
+    assert_close(got, want, f"{kind} {dtype} {Hq}/{Hk} B{B}")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("num_ctas", [0, 1, 3, 64, 600])
+def test_decode_quant_ctas(kind, num_ctas):
+    spec = W.WorkloadSpec("q", len(RAGGED), 32, 8, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=53, lengths=RAGGED)
+    ref, gpu = build_caches(kind, st, vals)
+    got, want = decode_both(kind, st, vals, ref, gpu, num_ctas=num_ctas)
+    assert_close(got, want, f"ctas={num_ctas}")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_decode_quant_large_values(kind):
+    # activations far outside the fp16 range of q and of p * scale: the kernel
+    # scales q heads by powers of two and normalises the V scales per tile
+    spec = W.WorkloadSpec("q", 4, 16, 4, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=54, lengths=[70, 300, 1, 129])
+    vals = dict(vals)
+    big = torch.tensor(1e7, dtype=torch.float32)      # V scales ~2e5: p * s_v > fp16 max
+    vals["q"] = (vals["q"].float() * 1e5).to(torch.bfloat16)   # |q| > fp16 max
+    vals["k_pool"] = (vals["k_pool"].float() * 1e-4).to(torch.bfloat16)
+    vals["k_new"] = (vals["k_new"].float() * 1e-4).to(torch.bfloat16)
+    vals["v_pool"] = (vals["v_pool"].float() * big).to(torch.bfloat16)
+    vals["v_new"] = (vals["v_new"].float() * big).to(torch.bfloat16)
+    ref, gpu = build_caches(kind, st, vals)
+    got, want = decode_both(kind, st, vals, ref, gpu, num_ctas=5)
+    rel = np.max(np.abs(got - want)) / np.max(np.abs(want))
+    assert np.all(np.isfinite(got)) and rel < 1e-4, rel
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_decode_quant_llama_workload_sampled(kind):
+    st, vals = W.make_workload(1, seed=0)
+    ref, gpu = build_caches(kind, st, vals)
+    ids = [0, 7, 21, 40, 63]
+    got, want = decode_both(kind, st, vals, ref, gpu, seq_ids=ids)
+    assert_close(got, want, "llama workload")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_block_copy_quant_is_byte_exact(kind):
+    spec = W.WorkloadSpec("q", 3, 8, 2, 128, 16, "f16", 1.0, pool_ratio=2.0)
+    st, vals = W.make_workload(spec, seed=55, lengths=[40, 17, 90])
+    ref, gpu = build_caches(kind, st, vals)
+    NB = gpu.k_codes.shape[0]
+    free = sorted(set(range(NB)) - set(st.block_tables[st.block_tables >= 0].tolist()))
+    assert len(free) >= 2
+    used = st.block_tables[0, :2].tolist()
+    pairs = [[used[0], free[0]], [used[1], free[1]]]
+    binding.block_copy_quant(pairs, gpu)
+    torch.cuda.synchronize()
+    for src, dst in pairs:
+        for t in (gpu.k_codes, gpu.v_codes):
+            assert torch.equal(t[dst].cpu(), t[src].cpu())
+        for t in (gpu.k_scales, gpu.v_scales):
+            assert torch.equal(t[dst].cpu().view(torch.int32), t[src].cpu().view(torch.int32))
+    with pytest.raises(binding.PkvError):
+        binding.block_copy_quant([[used[0], free[0]], [used[1], free[0]]], gpu)
+
+
+def test_append_quant_out_of_pool_slot_sets_error_word():
+    gpu = binding.QuantCache.empty(2, 1, 16, 128, "int8", torch.float16)
+    kn = torch.randn(2, 1, 128, device="cuda").to(torch.float16)
+    binding.get_error()
+    binding.append_quant(kn, kn, torch.tensor([0, 2 * 16], device="cuda"), gpu)
+    assert binding.get_error() == binding.DEVERR_SLOT
