@@ -604,24 +604,32 @@ __device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t 
     }
 }
 
-// Math warp `warp` converts its 16 rows of an 8-bit tile (one 128-byte plane
-// per row, D = 128) into the 16-bit tile layout (two planes per row) that
-// the tensor-core tile step reads. Lanes take whole 16-byte chunks.
+// Math warp `warp` converts its 16 rows of the 8-bit K and V tiles (one
+// 128-byte plane per row, D = 128) into the 16-bit tile layout (two planes
+// per row) that the tensor-core tile step reads. Lanes take whole 16-byte
+// chunks; all eight loads are issued before any conversion or store.
 template <int QK>
-__device__ __forceinline__ void convert_rows(uint32_t src, uint32_t dst, int warp, int lane) {
+__device__ __forceinline__ void convert_rows(uint32_t srcK, uint32_t srcV, uint32_t dstK,
+                                             uint32_t dstV, int warp, int lane) {
+    uint32_t w[8][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int i = lane + 32 * k;
+    for (int k = 0; k < 8; ++k) {
+        const int i = lane + 32 * (k & 3);
         const int row = 16 * warp + (i >> 3), ch = i & 7;
-        uint32_t w0, w1, w2, w3;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
-                     : "r"(swz(src, row, ch)));
+                     : "=r"(w[k][0]), "=r"(w[k][1]), "=r"(w[k][2]), "=r"(w[k][3])
+                     : "r"(swz(k < 4 ? srcK : srcV, row, ch)));
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = lane + 32 * (k & 3);
+        const int row = 16 * warp + (i >> 3), ch = i & 7;
+        const uint32_t dst = k < 4 ? dstK : dstV;
         uint32_t h[8];
-        codes_to_f16<QK>(w0, h[0], h[1]);
-        codes_to_f16<QK>(w1, h[2], h[3]);
-        codes_to_f16<QK>(w2, h[4], h[5]);
-        codes_to_f16<QK>(w3, h[6], h[7]);
+        codes_to_f16<QK>(w[k][0], h[0], h[1]);
+        codes_to_f16<QK>(w[k][1], h[2], h[3]);
+        codes_to_f16<QK>(w[k][2], h[4], h[5]);
+        codes_to_f16<QK>(w[k][3], h[6], h[7]);
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst, row, 2 * ch)),
                      "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
                      : "memory");
@@ -792,6 +800,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pkv_cursor_next(la, seq_len, p.S, p.U);
             }
         }
+        // This thread's chunks sit at the same places in every tile: row of
+        // the tile, swizzled shared-memory offset and byte offset inside the
+        // (block, kv head) chunk of the pool, computed once.
+        constexpr int NCH = CPR / 2;                  // K (and V) chunks per thread per tile
+        int crow[NCH];
+        uint32_t soff[NCH], goff[NCH];
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+            const int idx = tb + c * tpb;             // chunk within the block
+            const int rb = idx / CPR, ch = idx - (idx / CPR) * CPR;
+            crow[c] = jblk * p.B + rb;
+            soff[c] = swz(0u, crow[c], ch);
+            goff[c] = (uint32_t)(rb * Cfg::ROWB + ch * 16);
+        }
+        const size_t blk_stride = (size_t)p.Hk * p.B * Cfg::ROWB;   // bytes per pool block
+        // unit values, refreshed at each segment's first tile
+        int h0 = 0, gca = 0;
+        size_t head_off = 0, head_rows = 0;
         bool ok = true;
         for (int it0 = 0; it0 < n_my && ok; it0 += LA) {
 #pragma unroll
@@ -811,10 +837,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int ntok = min(PKV_TILE_TOKENS, cur.L - cur.ti * PKV_TILE_TOKENS);
                 const bool first = (it == 0) || (cur.ti == 0);
-                const int g = cur.u / p.NC;
-                const int chunk = cur.u - g * p.NC;
-                const int h0 = g * p.G + chunk * p.GC;
-                const int gca = min(p.GC, p.G - chunk * p.GC);
+                if (first) {
+                    const int g = p.NC == 1 ? cur.u : cur.u / p.NC;
+                    const int chunk = cur.u - g * p.NC;
+                    h0 = g * p.G + chunk * p.GC;
+                    gca = min(p.GC, p.G - chunk * p.GC);
+                    head_rows = (size_t)g * p.B;               // rows before kv head g in a block
+                    head_off = head_rows * Cfg::ROWB;
+                }
                 const uint32_t full = full0 + 8 * stage;
                 const uint32_t sK = sbase + stage * Cfg::STAGE;
                 const uint32_t sV = sK + Cfg::KVB;
@@ -823,16 +853,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- K and V rows of block jblk of this tile
                 const bool blk_ok = e >= 0 && e < p.NB;
                 if (tb == 0 && jblk * p.B < ntok && !blk_ok) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
-                const size_t blk_base = blk_ok ? ((size_t)e * p.Hk + g) * p.B * Cfg::ROWB : 0;
+                const size_t blk_base = blk_ok ? (size_t)e * blk_stride + head_off : 0;
 #pragma unroll
-                for (int c = 0; c < CPR / 2; ++c) {
-                    const int idx = tb + c * tpb;            // chunk within the block
-                    const int rb = idx / CPR, ch = idx - (idx / CPR) * CPR;
-                    const int row = jblk * p.B + rb;         // row of the tile
-                    const bool v = blk_ok && row < ntok;
-                    const size_t off = v ? blk_base + (size_t)rb * Cfg::ROWB + ch * 16 : 0;
-                    cp_async_16(swz(sK, row, ch), kpool + off, v);
-                    cp_async_16(swz(sV, row, ch), vpool + off, v);
+                for (int c = 0; c < NCH; ++c) {
+                    const bool v = blk_ok && crow[c] < ntok;
+                    const size_t off = v ? blk_base + goff[c] : 0;
+                    cp_async_16(sK + soff[c], kpool + off, v);
+                    cp_async_16(sV + soff[c], vpool + off, v);
                 }
                 if constexpr (QK != 0) {
                     // the block's B row scales, 4 rows per 16-byte copy; the
@@ -840,7 +867,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (tb < p.B / 4) {
                         const int row = jblk * p.B + 4 * tb;
                         const int nrow = blk_ok ? min(4, max(0, ntok - row)) : 0;
-                        const size_t so = blk_ok ? ((size_t)e * p.Hk + g) * p.B + 4 * tb : 0;
+                        const size_t so =
+                            blk_ok ? (size_t)e * p.Hk * p.B + head_rows + 4 * tb : 0;
                         cp_async_16_n(sS + row * 4, p.ks + so, 4u * nrow);
                         cp_async_16_n(sS + 256 + row * 4, p.vs + so, 4u * nrow);
                     }
@@ -902,8 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (QK != 0) {
             // this warp's 16 rows of codes -> fp16, then the 16-bit tile step
             const uint32_t cK = sbase + Cfg::OFF_CONV, cV = cK + Cfg::CONV / 2;
-            convert_rows<QK>(sK, cK, warp, lane);
-            convert_rows<QK>(sV, cV, warp, lane);
+            convert_rows<QK>(sK, sV, cK, cV, warp, lane);
             __syncwarp();
             const float *ksc = reinterpret_cast<const float *>(smem + stage * Cfg::STAGE +
                                                                2 * Cfg::KVB);
