@@ -276,6 +276,37 @@ def time_oracle(st, spec, h, target_s, seq_ids=None):
     return nbytes * reps / spent / 1e9, sum(lens) * reps / spent, spent, reps
 
 
+# ------------------------------------------------------------------ block manager
+def time_block_manager(st, spec, steps=200):
+    """Host cost of the block manager's part of a decode step for this
+    workload: one new token for every sequence (pkv_bm_append) and the
+    decode tables of the whole batch (pkv_bm_block_tables)."""
+    from paged_kv_cache_47_gb300 import binding
+
+    S = st.context_lens.numel()
+    B = spec.block_size
+    need = sum(-(-(int(L) + steps) // B) for L in st.context_lens.tolist())
+    bm = binding.BlockManager(need + 8, B)
+    for s, L in enumerate(st.context_lens.tolist()):
+        bm.add_sequence(s)
+        bm.append(s, int(L) - 1)
+    M = -(-(int(st.context_lens.max()) + steps) // B)
+    ids = list(range(S))
+    ones = [1] * S
+    t_app = t_tab = 0.0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        bm.append_batch(ids, ones)
+        t1 = time.perf_counter()
+        bm.block_tables(ids, M)
+        t_tab += time.perf_counter() - t1
+        t_app += t1 - t0
+    return {"sequences": S, "append_us_per_step": round(1e6 * t_app / steps, 2),
+            "tables_us_per_step": round(1e6 * t_tab / steps, 2),
+            "note": "host, through the Python binding: one pkv_bm_append_batch and one "
+                    "pkv_bm_block_tables call per step"}
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     world, rank, local = dist_env()
@@ -592,6 +623,7 @@ def run_ours(args):
                      "avg_launch_ms": round(split_avg, 5),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
         "other_kernels": side or None,
+        "block_manager": time_block_manager(st, spec) if rank == 0 else None,
         "gpu_launches": (2 + (1 if cow is not None else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),

@@ -65,7 +65,9 @@ typedef enum {
     PKV_ERR_CUDA = -3,          /* a CUDA runtime call or launch failed        */
     PKV_ERR_OUT_OF_RANGE = -4,  /* the device error word was non-zero          */
     PKV_ERR_TIMEOUT = -5,       /* a bounded on-chip wait gave up              */
-    PKV_ERR_WORKSPACE = -6      /* workspace missing or too small              */
+    PKV_ERR_WORKSPACE = -6,     /* workspace missing or too small              */
+    PKV_ERR_NO_BLOCKS = -7      /* block manager: not enough free blocks; the
+                                   call changed nothing                        */
 } pkv_status;
 
 /* Bits of the device error word (see pkv_get_error). */

@@ -394,3 +394,149 @@ def block_copy_quant(pairs, cache: QuantCache, stream=None) -> None:
     assert p.device.type == "cpu", "block-copy pairs are host memory"
     _check(lib().pkv_block_copy_quant(ctypes.byref(cache.desc), _ptr(p), p.shape[0],
                                       *cache.pointers(), _stream(stream)))
+
+
+# ------------------------------------------------------------------ block manager
+class BmStats(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("free_blocks", ctypes.c_int32),
+                ("shared_blocks", ctypes.c_int32), ("prefix_entries", ctypes.c_int32),
+                ("sequences", ctypes.c_int64), ("tokens", ctypes.c_int64)]
+
+
+def _bm_lib():
+    L = lib()
+    if not getattr(L, "_bm_ready", False):
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.pkv_bm_create.argtypes = [i32, i32, ctypes.POINTER(vp)]
+        L.pkv_bm_create.restype = i32
+        L.pkv_bm_destroy.argtypes = [vp]
+        L.pkv_bm_destroy.restype = None
+        L.pkv_bm_add_sequence.argtypes = [vp, i64, vp, i32, vp]
+        L.pkv_bm_add_sequence.restype = i32
+        L.pkv_bm_append.argtypes = [vp, i64, i32, vp, vp, i32, ctypes.POINTER(i32)]
+        L.pkv_bm_append.restype = i32
+        L.pkv_bm_append_batch.argtypes = [vp, vp, vp, i32, vp, vp, i32, ctypes.POINTER(i32),
+                                          ctypes.POINTER(i32)]
+        L.pkv_bm_append_batch.restype = i32
+        L.pkv_bm_fork.argtypes = [vp, i64, i64]
+        L.pkv_bm_fork.restype = i32
+        L.pkv_bm_free_sequence.argtypes = [vp, i64]
+        L.pkv_bm_free_sequence.restype = i32
+        L.pkv_bm_block_tables.argtypes = [vp, vp, i32, i32, vp, vp]
+        L.pkv_bm_block_tables.restype = i32
+        L.pkv_bm_stats_get.argtypes = [vp, ctypes.POINTER(BmStats)]
+        L.pkv_bm_stats_get.restype = i32
+        L.pkv_bm_refcount.argtypes = [vp, i32]
+        L.pkv_bm_refcount.restype = i32
+        L.pkv_bm_simulate_admission.argtypes = [i32, i32, vp, i32, i32, ctypes.POINTER(i32),
+                                                ctypes.POINTER(ctypes.c_double)]
+        L.pkv_bm_simulate_admission.restype = i32
+        L._bm_ready = True
+    return L
+
+
+class NoBlocks(PkvError):
+    """The block manager has too few free blocks; the call changed nothing."""
+
+
+def _bm_check(status: int):
+    if status == -7:
+        raise NoBlocks(status, lib().pkv_last_error_message().decode())
+    _check(status)
+
+
+class BlockManager:
+    """Host block manager of a paged KV cache (libpkv's pkv_bm_* calls)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        L = _bm_lib()
+        h = ctypes.c_void_p()
+        _bm_check(L.pkv_bm_create(num_blocks, block_size, ctypes.byref(h)))
+        self._h, self._L = h, L
+        self.block_size = block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._L.pkv_bm_destroy(h)
+            self._h = None
+
+    def add_sequence(self, seq: int, prefix_hashes=()) -> list:
+        hs = (ctypes.c_uint64 * max(1, len(prefix_hashes)))(*[int(x) & (2 ** 64 - 1)
+                                                              for x in prefix_hashes])
+        hits = (ctypes.c_uint8 * max(1, len(prefix_hashes)))()
+        _bm_check(self._L.pkv_bm_add_sequence(self._h, seq, hs, len(prefix_hashes), hits))
+        return [bool(hits[i]) for i in range(len(prefix_hashes))]
+
+    def append(self, seq: int, n: int):
+        """Slots of n new tokens and the (src, dst) copies to run first."""
+        slots = (ctypes.c_int64 * max(1, n))()
+        pairs = (ctypes.c_int64 * 2)()
+        nc = ctypes.c_int32(0)
+        _bm_check(self._L.pkv_bm_append(self._h, seq, n, slots, pairs, 1, ctypes.byref(nc)))
+        return [slots[i] for i in range(n)], [(pairs[2 * i], pairs[2 * i + 1])
+                                               for i in range(nc.value)]
+
+    def append_batch(self, seq_ids, num_tokens):
+        """Slots (all sequences back to back) and copies of one step; raises on
+        failure after the sequences before the failing one were applied."""
+        ids = torch.as_tensor(list(seq_ids), dtype=torch.int64)
+        nt = torch.as_tensor(list(num_tokens), dtype=torch.int32)
+        total = int(nt.sum()) if len(nt) else 0
+        slots = torch.empty(max(1, total), dtype=torch.int64)
+        pairs = torch.empty(max(1, len(ids)), 2, dtype=torch.int64)
+        nc, nd = ctypes.c_int32(0), ctypes.c_int32(0)
+        _bm_check(self._L.pkv_bm_append_batch(self._h, ids.data_ptr(), nt.data_ptr(), len(ids),
+                                              slots.data_ptr(), pairs.data_ptr(), len(ids),
+                                              ctypes.byref(nc), ctypes.byref(nd)))
+        return slots[:total], pairs[:nc.value]
+
+    def fork(self, parent: int, child: int) -> None:
+        _bm_check(self._L.pkv_bm_fork(self._h, parent, child))
+
+    def free_sequence(self, seq: int) -> None:
+        _bm_check(self._L.pkv_bm_free_sequence(self._h, seq))
+
+    def block_tables(self, seq_ids, max_blocks_per_seq: int):
+        """(block_tables [S][M] int32, context_lens [S] int32) as CPU tensors."""
+        ids = torch.as_tensor(list(seq_ids), dtype=torch.int64)
+        tables = torch.empty(len(ids), max_blocks_per_seq, dtype=torch.int32)
+        lens = torch.empty(len(ids), dtype=torch.int32)
+        _bm_check(self._L.pkv_bm_block_tables(self._h, ids.data_ptr(), len(ids),
+                                              max_blocks_per_seq, tables.data_ptr(),
+                                              lens.data_ptr()))
+        return tables, lens
+
+    def table(self, seq: int) -> list:
+        width = max(1, self.stats().num_blocks)
+        while True:
+            try:
+                t, _ = self.block_tables([seq], width)
+            except PkvError:
+                if width >= 1 << 24:
+                    raise
+                width *= 4      # a prefix can repeat a block, so a table may exceed the pool
+                continue
+            return [int(b) for b in t[0].tolist() if b >= 0]
+
+    def stats(self) -> BmStats:
+        st = BmStats()
+        _bm_check(self._L.pkv_bm_stats_get(self._h, ctypes.byref(st)))
+        return st
+
+    def refcount(self, block: int) -> int:
+        return int(self._L.pkv_bm_refcount(self._h, block))
+
+    def num_free(self) -> int:
+        return int(self.stats().free_blocks)
+
+
+def simulate_admission(num_blocks: int, block_size: int, context_lens, reserve_tokens: int = 0):
+    """(admitted, utilisation) of requests admitted in order into a pool."""
+    L = _bm_lib()
+    cl = torch.as_tensor(list(context_lens), dtype=torch.int32)
+    adm = ctypes.c_int32(0)
+    u = ctypes.c_double(0.0)
+    _bm_check(L.pkv_bm_simulate_admission(num_blocks, block_size, cl.data_ptr(), len(cl),
+                                          reserve_tokens, ctypes.byref(adm), ctypes.byref(u)))
+    return int(adm.value), float(u.value)

@@ -1,6 +1,7 @@
 """Build libpkv.so in-tree with nvcc for sm_103a.
 
-Each .cu translation unit compiles in its own nvcc process (in parallel), then
+Each .cu translation unit (and each host-only .cpp unit, such as the block
+manager) compiles in its own nvcc process (in parallel), then
 one link step produces paged_kv_cache_47_gb300/_build/libpkv.so, which links
 the shared CUDA runtime (the same libcudart.so.13 PyTorch loads).
 """
@@ -33,12 +34,12 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(
-        os.path.join(CSRC, "*.cuh")) + [os.path.join(INCLUDE, "pkv.h"), __file__]
+        os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
 def is_stale() -> bool:

@@ -261,6 +261,7 @@ const char *pkv_status_string(pkv_status s) {
         case PKV_ERR_OUT_OF_RANGE: return "device-side value out of range";
         case PKV_ERR_TIMEOUT: return "on-chip wait timed out";
         case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_NO_BLOCKS: return "not enough free blocks";
     }
     return "unknown status";
 }

@@ -12,7 +12,7 @@ import torch
 from paged_kv_cache_47_gb300 import binding, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pkv.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("pkv.h", "pkv_block_manager.h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,9 +22,11 @@ def L():
 
 
 def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", src)))
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(L):
@@ -39,7 +41,7 @@ def test_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
         assert L.pkv_status_string(code) not in (b"", b"unknown status")
     assert L.pkv_status_string(-99) == b"unknown status"
 
