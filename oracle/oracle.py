@@ -46,6 +46,9 @@ def lib():
         L.oracle_e4m3_decode.restype = ctypes.c_double
         L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         L.oracle_e4m3_encode.restype = i32
+        L.oracle_decode_flat.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, i32, i32, i32p,
+                                         i32p, ctypes.c_double, vp]
+        L.oracle_decode_flat.restype = i32
         L.oracle_set_num_threads.argtypes = [i32]
         L.oracle_set_num_threads.restype = None
         _lib = L
@@ -169,4 +172,24 @@ def decode_quant(kind: str, q, k_codes, v_codes, k_scales, v_scales, block_table
                                    float(scale), out.ctypes.data)
     if rc != 0:
         raise ValueError(f"oracle_decode_quant failed with status {rc}")
+    return out
+
+
+# ------------------------------------------------------------------ flat spans
+def decode_flat(q, k_flat, v_flat, slots, context_lens, scale: float) -> np.ndarray:
+    """fp64 attention output [S][Hq][D]; sequence s reads span slots[s] of
+    k_flat / v_flat [num_slots][capacity][Hk][D] (token-major)."""
+    q, kf, vf = _cpu(q), _cpu(k_flat), _cpu(v_flat)
+    sl = _cpu(torch.as_tensor(slots)).to(torch.int32)
+    cl = _cpu(context_lens).to(torch.int32)
+    assert q.dtype == kf.dtype == vf.dtype and kf.shape == vf.shape
+    S, Hq, D = q.shape
+    NS, cap, Hk, D2 = kf.shape
+    assert D2 == D
+    out = np.zeros((S, Hq, D), dtype=np.float64)
+    rc = lib().oracle_decode_flat(q.data_ptr(), _CODES[q.dtype], S, Hq, Hk, D, kf.data_ptr(),
+                                  vf.data_ptr(), NS, cap, sl.data_ptr(), cl.data_ptr(),
+                                  float(scale), out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_decode_flat failed with status {rc}")
     return out

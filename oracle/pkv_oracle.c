@@ -41,6 +41,12 @@
  *   oracle_append_quant, oracle_decode_quant
  *                      The same append and decode over an 8-bit quantized
  *                      cache (see "quantized KV" below).
+ *   oracle_decode_flat The same attention over K/V that sit in one flat span
+ *                      per sequence instead of blocks: the alternative that
+ *                      keeps each sequence's cache contiguous in virtual
+ *                      memory and commits physical pages on demand
+ *                      ("Contiguous vs Paged KV Cache on RDNA4", section "Why
+ *                      the single-user verdict flipped", on vAttention).
  *
  * Element decoding (fp16 / bf16 / fp32 -> double) follows the IEEE-754
  * binary16 and bfloat16 bit layouts directly; it does not use any library
@@ -424,6 +430,55 @@ int oracle_decode_quant(const void *q, int act_dtype, int S, int Hq, int Hk, int
         int rc = decode_one_quant(q, act_dtype, Hq, Hk, B, D, kind, k_codes, v_codes, k_scales,
                                   v_scales, NB, block_tables + (size_t)s * M, M, context_lens[s],
                                   scale, s, g, out);
+        if (rc != 0) {
+#pragma omp critical
+            status = rc;
+        }
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------- flat spans
+ * Sequence s's cache is one span [capacity][Hk][D] (token-major: the rows of
+ * all kv heads of token t are adjacent) at slot slots[s] of k_flat / v_flat
+ * [num_slots][capacity][Hk][D]. Token t of kv head g is row (t * Hk + g) of
+ * the span; no block table is involved. */
+int oracle_decode_flat(const void *q, int dtype, int S, int Hq, int Hk, int D,
+                       const void *k_flat, const void *v_flat, int num_slots, int capacity,
+                       const int32_t *slots, const int32_t *context_lens, double scale,
+                       double *out) {
+    if (!q || !k_flat || !v_flat || !slots || !context_lens || !out) return -1;
+    if (S < 0 || Hq <= 0 || Hk <= 0 || Hq % Hk != 0 || D <= 0 || capacity <= 0) return -1;
+    if (dtype < 0 || dtype > 2) return -1;
+    int status = 0;
+    long units = (long)S * Hk;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long u = 0; u < units; ++u) {
+        int s = (int)(u / Hk), g = (int)(u % Hk);
+        int L = context_lens[s], slot = slots[s];
+        int rc = 0;
+        if (slot < 0 || slot >= num_slots || L < 0 || L > capacity) {
+            rc = -2;
+        } else if (L == 0) {
+            zero_rows(Hq, Hk, D, s, g, out);
+        } else {
+            double *Kc = (double *)malloc(sizeof(double) * (size_t)L * D);
+            double *Vc = (double *)malloc(sizeof(double) * (size_t)L * D);
+            if (!Kc || !Vc) {
+                rc = -1;
+            } else {
+                for (int t = 0; t < L; ++t) {
+                    size_t row = (((size_t)slot * capacity + t) * Hk + g) * D;
+                    for (int d = 0; d < D; ++d) {
+                        Kc[(size_t)t * D + d] = load_elem(k_flat, dtype, row + d);
+                        Vc[(size_t)t * D + d] = load_elem(v_flat, dtype, row + d);
+                    }
+                }
+                rc = attend(q, dtype, Hq, Hk, D, L, Kc, Vc, scale, s, g, out);
+            }
+            free(Kc);
+            free(Vc);
+        }
         if (rc != 0) {
 #pragma omp critical
             status = rc;
