@@ -432,6 +432,63 @@ class PoolsQ:
                                          c.v_scales.clone(), c.code, c.act_dtype))
 
 
+class PoolsFlat:
+    """One resident copy of a flat cache: one virtual span per sequence, its
+    physical chunks mapped as it grows (pkv_flat_*)."""
+
+    def __init__(self, fc, st):
+        self.fc, self.st = fc, st
+
+    @classmethod
+    def fill(cls, st, vals, dev):
+        """Every context row before the step's append, copied into the flat
+        spans (slot s = sequence s) by the library's flat append."""
+        from paged_kv_cache_47_gb300 import binding
+        NB, Hk, B, D = vals["k_pool"].shape
+        lens = st.context_lens.tolist()
+        cap = -(-max(lens) // 64) * 64
+        fc = binding.FlatCache(len(lens), cap, Hk, D, vals["q"].dtype)
+        slots, pos, src = [], [], []
+        for s, L in enumerate(lens):
+            fc.reserve(s, L)
+            row = st.block_tables[s].tolist()
+            for t in range(L - 1):
+                slots.append(s)
+                pos.append(t)
+                src.append(row[t // B] * B + t % B)
+        sl = torch.tensor(src, dtype=torch.int64, device=dev)
+        kr = vals["k_pool"][sl // B, :, sl % B].contiguous()
+        vr = vals["v_pool"][sl // B, :, sl % B].contiguous()
+        fc.append(kr, vr, torch.tensor(slots, dtype=torch.int32, device=dev),
+                  torch.tensor(pos, dtype=torch.int32, device=dev))
+        torch.cuda.synchronize()
+        return cls(fc, st)
+
+    def workspace(self, Hq):
+        return self.fc.workspace(Hq)
+
+    def prepared(self, q, kn, vn, slots, tables, lens, scale, out, ws, consumer=0):
+        S = q.shape[0]
+        seq = torch.arange(S, dtype=torch.int32, device=q.device)
+        # the appended token sits at position L - 1 (the workload's lengths are fixed)
+        pos = (self.st.context_lens - 1).to(torch.int32).to(q.device)
+        fc = self.fc
+
+        def app(stream):
+            fc.append(kn, vn, seq, pos, stream=stream)
+
+        def dec(stream, timing_events=None):
+            fc.decode_attention(q, seq, lens, scale, out=out, workspace=ws,
+                                timing_events=timing_events, stream=stream)
+        return app, dec
+
+    def cow(self, pairs, stream):
+        raise RuntimeError("flat spans share no blocks: no copy-on-write")
+
+    def clone(self):
+        raise RuntimeError("clone a flat cache by filling a new one")
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args):
     from paged_kv_cache_47_gb300 import binding, build
@@ -464,11 +521,19 @@ def run_ours(args):
     slots = st.slot_mapping.to(dev)
     S, Hq, D = vals["q"].shape
     # three resident copies of the cache so every step reads a cold L2
-    base = PoolsQ.fill(args.kv_quant, st, vals, dev) if args.kv_quant else \
-        Pools16(vals["k_pool"], vals["v_pool"])
-    if args.kv_quant:
-        del vals["k_pool"], vals["v_pool"]      # the activations are in the 8-bit cache now
-    copies = [base] + [base.clone() for _ in range(args.copies - 1)]
+    if args.flat:
+        if cow is not None:
+            raise SystemExit("--flat: flat spans share no blocks (no copy-on-write workloads)")
+        if args.kv_quant:
+            raise SystemExit("--flat and --kv-quant are separate paths")
+        copies = [PoolsFlat.fill(st, vals, dev) for _ in range(args.copies)]
+        del vals["k_pool"], vals["v_pool"]      # the rows are in the flat spans now
+    else:
+        base = PoolsQ.fill(args.kv_quant, st, vals, dev) if args.kv_quant else \
+            Pools16(vals["k_pool"], vals["v_pool"])
+        if args.kv_quant:
+            del vals["k_pool"], vals["v_pool"]      # the activations are in the 8-bit cache now
+        copies = [base] + [base.clone() for _ in range(args.copies - 1)]
     outs = [torch.empty(S, Hq, D, dtype=vals["q"].dtype, device=dev) for _ in copies]
     wss = [c.workspace(Hq) for c in copies]
     row_bytes = cache_row_bytes(spec, args.kv_quant)
@@ -600,6 +665,11 @@ def run_ours(args):
         "dtype": args.kv_quant or spec.dtype,
         "data": "synthetic (seeded N(0,1) values, random block tables)",
         "config": {**workload_config(spec, st),
+                   **({"kv_cache": "flat spans: one virtual range per sequence, physical "
+                                   "chunks mapped on demand (pkv_flat_*)",
+                       "flat_committed_bytes_per_copy": int(copies[0].fc.info().committed_bytes),
+                       "kv_bytes_per_copy": int(st.context_lens.sum()) * 2 * spec.num_kv_heads *
+                                            row_bytes} if args.flat else {}),
                    **({"kv_cache": f"{args.kv_quant} codes + fp32 row scales "
                                    f"({row_bytes} B per token and kv head for K, same for V); "
                                    f"{spec.dtype} activations; fp16 tensor-core math"}
@@ -721,6 +791,8 @@ def main():
     ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size")
     ap.add_argument("--dtype", choices=["f32", "f16", "bf16"], default=None,
                     help="override the workload's K/V dtype")
+    ap.add_argument("--flat", action="store_true",
+                    help="flat per-sequence spans in virtual memory instead of a paged pool")
     ap.add_argument("--kv-quant", choices=["int8", "fp8_e4m3"], default=None,
                     help="8-bit KV cache (codes + fp32 row scales) instead of the workload's dtype")
     ap.add_argument("--consumer", type=int, default=0,

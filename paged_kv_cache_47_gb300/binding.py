@@ -540,3 +540,108 @@ def simulate_admission(num_blocks: int, block_size: int, context_lens, reserve_t
     _bm_check(L.pkv_bm_simulate_admission(num_blocks, block_size, cl.data_ptr(), len(cl),
                                           reserve_tokens, ctypes.byref(adm), ctypes.byref(u)))
     return int(adm.value), float(u.value)
+
+
+# ------------------------------------------------------------------ flat spans
+class FlatInfo(ctypes.Structure):
+    _fields_ = [("k_base", ctypes.c_void_p), ("slot_stride", ctypes.c_size_t),
+                ("v_offset", ctypes.c_size_t), ("granularity", ctypes.c_size_t),
+                ("committed_bytes", ctypes.c_size_t), ("committed_tokens", ctypes.c_void_p)]
+
+
+def _flat_lib():
+    L = lib()
+    if not getattr(L, "_flat_ready", False):
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.pkv_flat_create.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(vp)]
+        L.pkv_flat_create.restype = i32
+        L.pkv_flat_destroy.argtypes = [vp]
+        L.pkv_flat_destroy.restype = None
+        L.pkv_flat_reserve.argtypes = [vp, i32, i32]
+        L.pkv_flat_reserve.restype = i32
+        L.pkv_flat_release.argtypes = [vp, i32]
+        L.pkv_flat_release.restype = i32
+        L.pkv_flat_get_info.argtypes = [vp, ctypes.POINTER(FlatInfo)]
+        L.pkv_flat_get_info.restype = i32
+        L.pkv_flat_append.argtypes = [vp, vp, vp, vp, vp, i32, vp]
+        L.pkv_flat_append.restype = i32
+        L.pkv_flat_decode_workspace_bytes.argtypes = [vp, i32, i32]
+        L.pkv_flat_decode_workspace_bytes.restype = sz
+        L.pkv_decode_attention_flat.argtypes = [vp, vp, i32, i32, vp, vp, ctypes.c_float, vp, i32,
+                                                vp, sz, vp, ctypes.POINTER(DecodeOptions)]
+        L.pkv_decode_attention_flat.restype = i32
+        L._flat_ready = True
+    return L
+
+
+class FlatCache:
+    """A KV cache kept contiguous in virtual memory (libpkv's pkv_flat_* calls):
+    num_slots sequence slots of capacity tokens, physical chunks mapped as
+    slots grow."""
+
+    def __init__(self, num_slots: int, capacity: int, num_kv_heads: int, head_dim: int,
+                 dtype: torch.dtype):
+        L = _flat_lib()
+        h = ctypes.c_void_p()
+        _check(L.pkv_flat_create(num_slots, capacity, num_kv_heads, head_dim, DTYPE_CODE[dtype],
+                                 ctypes.byref(h)))
+        self._h, self._L = h, L
+        self.num_slots, self.capacity = num_slots, capacity
+        self.num_kv_heads, self.head_dim, self.dtype = num_kv_heads, head_dim, dtype
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._L.pkv_flat_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def reserve(self, slot: int, tokens: int) -> None:
+        _check(self._L.pkv_flat_reserve(self._h, slot, tokens))
+
+    def release(self, slot: int) -> None:
+        _check(self._L.pkv_flat_release(self._h, slot))
+
+    def info(self) -> FlatInfo:
+        inf = FlatInfo()
+        _check(self._L.pkv_flat_get_info(self._h, ctypes.byref(inf)))
+        return inf
+
+    def append(self, k_new, v_new, slots, positions, stream=None) -> None:
+        """k_new/v_new [N][Hk][D] (device); slots/positions int32 [N] (device)."""
+        k_new, v_new = k_new.contiguous(), v_new.contiguous()
+        sl, pos = slots.contiguous(), positions.contiguous()
+        assert sl.dtype == torch.int32 and pos.dtype == torch.int32 and k_new.dtype == self.dtype
+        _check(self._L.pkv_flat_append(self._h, _ptr(k_new), _ptr(v_new), _ptr(sl), _ptr(pos),
+                                       sl.numel(), _stream(stream)))
+
+    def workspace(self, num_q_heads: int, num_ctas: int = 0) -> torch.Tensor:
+        n = int(self._L.pkv_flat_decode_workspace_bytes(self._h, num_q_heads, num_ctas))
+        if n == 0:
+            raise PkvError(-1, "workspace size query failed")
+        return torch.zeros(n, dtype=torch.uint8, device="cuda")
+
+    def decode_attention(self, q, slots, context_lens, scale: float,
+                         out: Optional[torch.Tensor] = None,
+                         out_dtype: Optional[torch.dtype] = None,
+                         workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                         timing_events: Optional[Sequence] = None, stream=None) -> torch.Tensor:
+        S, Hq, D = q.shape
+        q = q.contiguous()
+        sl, cl = slots.contiguous(), context_lens.contiguous()
+        assert sl.dtype == torch.int32 and cl.dtype == torch.int32 and q.dtype == self.dtype
+        if out is None:
+            out = torch.empty(S, Hq, D, dtype=out_dtype or q.dtype, device=q.device)
+        if workspace is None:
+            workspace = self.workspace(Hq, num_ctas)
+        opts = DecodeOptions()
+        opts.num_ctas = num_ctas
+        if timing_events is not None:
+            for i, ev in enumerate(timing_events):
+                opts.timing_events[i] = None if ev is None else ev.cuda_event
+        _check(self._L.pkv_decode_attention_flat(
+            self._h, _ptr(q), S, Hq, _ptr(sl), _ptr(cl), float(scale), _ptr(out),
+            DTYPE_CODE[out.dtype], _ptr(workspace), workspace.numel(), _stream(stream),
+            ctypes.byref(opts)))
+        return out

@@ -107,13 +107,26 @@ struct SplitCfg {
 // seq_len[s]   = context length clamped to [0, M*B] (a clamp flags the error word)
 // seq_prefix[s]= U * sum_{s'<s} ceil(seq_len[s'] / 64), seq_prefix[S] = NT
 // Ends with __syncthreads(); all threads of the block must call it.
+template <bool FLAT>
 __device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq_prefix,
                                                  int *seq_len, bool report) {
     const int tid = threadIdx.x;
     const int max_len = p.M * p.B;
     for (int s = tid; s < p.S; s += blockDim.x) {
         int bad = 0;
-        int L = pkv_clamp_len(p.context_lens[s], max_len, &bad);
+        int L;
+        if constexpr (FLAT) {
+            // a flat span holds at most the tokens its slot has memory for
+            const int slot = p.slots[s];
+            if (slot < 0 || slot >= p.NB) {
+                if (report) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+                L = 0;
+            } else {
+                L = pkv_clamp_len(p.context_lens[s], min(max_len, p.committed[slot]), &bad);
+            }
+        } else {
+            L = pkv_clamp_len(p.context_lens[s], max_len, &bad);
+        }
         if (bad && report) atomicOr(p.err, PKV_DEVERR_CONTEXT);
         seq_len[s] = L;
     }
@@ -713,7 +726,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
 // ---------------------------------------------------------------------------
 // the split-K kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA, int QK>
+template <typename T, int D, int GMAX, bool MMA, int QK, bool FLAT>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_split_kernel(const DecodeParams p) {
     using Cfg = SplitCfg<T, D, GMAX, MMA, QK>;
@@ -747,7 +760,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // inputs may come from the previous kernel on the stream (launched with
     // programmatic serialisation): wait for it before reading any of them
     grid_dependency_wait();
-    build_seq_arrays(p, seq_prefix, seq_len, cta == 0);
+    build_seq_arrays<FLAT>(p, seq_prefix, seq_len, cta == 0);
 
     // zero-length sequences: zeros, written by CTA s % C
     for (int s = 0; s < p.S; ++s) {
@@ -782,13 +795,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jblk = pt / tpb;
         const int tb = pt - jblk * tpb;
         const uint8_t *kpool = static_cast<const uint8_t *>(p.kp);
-        const uint8_t *vpool = static_cast<const uint8_t *>(p.vp);
+        const uint8_t *vpool = FLAT ? kpool + p.v_off : static_cast<const uint8_t *>(p.vp);
         PkvCursor cur, la;
         pkv_cursor_at(cur, t_begin, seq_prefix, seq_len, p.S);
         la = cur;
+        // per tile: the physical block of this thread's rows, or (flat
+        // spans) the sequence's slot
         auto load_entry = [&](const PkvCursor &c) -> int {
             const int ntok = min(PKV_TILE_TOKENS, c.L - c.ti * PKV_TILE_TOKENS);
             if (jblk * p.B >= ntok) return -1;
+            if constexpr (FLAT) return __ldg(p.slots + c.s);
             return __ldg(p.block_tables + (size_t)c.s * p.M + c.ti * bpt + jblk);
         };
         int ent[LA];
@@ -812,7 +828,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rb = idx / CPR, ch = idx - (idx / CPR) * CPR;
             crow[c] = jblk * p.B + rb;
             soff[c] = swz(0u, crow[c], ch);
-            goff[c] = (uint32_t)(rb * Cfg::ROWB + ch * 16);
+            // paged: row rb of a (block, kv head) chunk; flat: row crow of the
+            // tile, Hk rows apart per token
+            goff[c] = FLAT ? (uint32_t)(crow[c] * p.Hk * Cfg::ROWB + ch * 16)
+                           : (uint32_t)(rb * Cfg::ROWB + ch * 16);
         }
         const size_t blk_stride = (size_t)p.Hk * p.B * Cfg::ROWB;   // bytes per pool block
         // unit values, refreshed at each segment's first tile
@@ -843,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     h0 = g * p.G + chunk * p.GC;
                     gca = min(p.GC, p.G - chunk * p.GC);
                     head_rows = (size_t)g * p.B;               // rows before kv head g in a block
-                    head_off = head_rows * Cfg::ROWB;
+                    head_off = FLAT ? (size_t)g * Cfg::ROWB : head_rows * Cfg::ROWB;
                 }
                 const uint32_t full = full0 + 8 * stage;
                 const uint32_t sK = sbase + stage * Cfg::STAGE;
@@ -853,7 +872,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- K and V rows of block jblk of this tile
                 const bool blk_ok = e >= 0 && e < p.NB;
                 if (tb == 0 && jblk * p.B < ntok && !blk_ok) atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
-                const size_t blk_base = blk_ok ? (size_t)e * blk_stride + head_off : 0;
+                size_t blk_base = 0;
+                if (blk_ok) {
+                    blk_base = FLAT ? (size_t)e * p.slot_stride +
+                                          (size_t)cur.ti * PKV_TILE_TOKENS * p.Hk * Cfg::ROWB +
+                                          head_off
+                                    : (size_t)e * blk_stride + head_off;
+                }
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     const bool v = blk_ok && crow[c] < ntok;
@@ -1009,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // host-side launch of one variant
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA, int QK = 0>
+template <typename T, int D, int GMAX, bool MMA, int QK = 0, bool FLAT = false>
 struct SplitVariant {
     using Cfg = SplitCfg<T, D, GMAX, MMA, QK>;
 
@@ -1018,7 +1043,7 @@ struct SplitVariant {
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!done[dev]) {
             const size_t smem = Cfg::smem_bytes(kMaxSeqsPerLaunch);
-            cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, GMAX, MMA, QK>,
+            cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, GMAX, MMA, QK, FLAT>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem);
             if (e != cudaSuccess) return e;
@@ -1042,7 +1067,7 @@ struct SplitVariant {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA, QK>, p);
+        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT>, p);
     }
 
     // occupancy of this variant on the current device (queried once per device)
@@ -1054,7 +1079,7 @@ struct SplitVariant {
         if (prepare(dev) != cudaSuccess) return 0;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &n, decode_split_kernel<T, D, GMAX, MMA, QK>, kThreads,
+                &n, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT>, kThreads,
                 Cfg::smem_bytes(kMaxSeqsPerLaunch)) != cudaSuccess)
             return 0;
         cached[dev] = n;

@@ -241,6 +241,8 @@ pkv_status copy_blocks(int NB, const int64_t *pairs, int n, void *k_pool, void *
 }  // namespace
 
 namespace pkv {
+pkv_status device_error_word(unsigned **out) { return device_error_ptr(out); }
+
 pkv_status set_last_error(pkv_status st, const char *fmt, ...) {
     va_list ap;
     va_start(ap, fmt);
@@ -360,6 +362,10 @@ struct DecodeArgs {
     size_t ws_bytes;
     cudaStream_t stream;
     const pkv_decode_options *opts;
+    // flat spans (tables is then NULL): see DecodeParams
+    const int32_t *slots = nullptr;
+    const int32_t *committed = nullptr;
+    size_t slot_stride = 0, v_off = 0;
 };
 
 // Host checks shared by the decode entry points (after the cache descriptor).
@@ -373,10 +379,11 @@ pkv_status check_decode_args(const DecodeArgs &a) {
 
 pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
     if (a.S == 0) return PKV_OK;
-    if (!a.q || !a.kp || !a.vp || !a.tables || !a.lens || !a.out)
+    if (!a.q || !a.kp || !a.vp || (!a.tables && !a.slots) || !a.lens || !a.out)
         return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
     if (!aligned(a.q, 16) || !aligned(a.kp, 16) || !aligned(a.vp, 16) ||
-        !aligned(a.out, elem_bytes(a.out_dtype)) || !aligned(a.tables, 4) || !aligned(a.lens, 4))
+        !aligned(a.out, elem_bytes(a.out_dtype)) || !aligned(a.tables, 4) ||
+        !aligned(a.slots, 4) || !aligned(a.lens, 4))
         return fail(PKV_ERR_INVALID_ARG, "q and the pools must be 16-byte aligned");
     // flattened tile count must fit in int32
     const int64_t max_tiles_per_unit =
@@ -411,7 +418,11 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
         p.q = static_cast<const uint8_t *>(a.q) + (size_t)s0 * a.Hq * a.D * a.q_es;
         p.out = static_cast<uint8_t *>(a.out) + (size_t)s0 * a.Hq * a.D * oes;
         p.out_dtype = a.out_dtype;
-        p.block_tables = a.tables + (size_t)s0 * a.M;
+        p.block_tables = a.tables ? a.tables + (size_t)s0 * a.M : nullptr;
+        p.slots = a.slots ? a.slots + s0 : nullptr;
+        p.committed = a.committed;
+        p.slot_stride = a.slot_stride;
+        p.v_off = a.v_off;
         p.context_lens = a.lens + s0;
         p.M = a.M;
         p.S = S;
@@ -562,3 +573,39 @@ pkv_status pkv_get_error(int32_t *device_error_word, void *stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- flat spans
+namespace pkv {
+
+pkv_status decode_flat(const FlatGeom &g, const void *q, int32_t S, int32_t Hq,
+                       const int32_t *slots, const int32_t *lens, float scale, void *out,
+                       int32_t out_dtype, void *ws, size_t ws_bytes, cudaStream_t stream,
+                       const pkv_decode_options *o) {
+    if (o && o->consumer == 1)
+        return fail(PKV_ERR_UNSUPPORTED, "flat spans use the tensor-core math (consumer 1 given)");
+    DecodeArgs a{g.num_slots, kFlatRowsPerGroup, g.Hk, g.D, elem_bytes(g.dtype), q, S, Hq,
+                 g.k_base, g.k_base, nullptr, nullptr, nullptr,
+                 g.capacity / kFlatRowsPerGroup, lens, scale, out, out_dtype, ws, ws_bytes,
+                 stream, o};
+    a.slots = slots;
+    a.committed = g.committed;
+    a.slot_stride = g.slot_stride;
+    a.v_off = g.v_off;
+    pkv_status st = check_decode_args(a);
+    if (st != PKV_OK) return st;
+    Plan pl;
+    if ((st = plan_groups(g.Hk, Hq, o, true, &pl)) != PKV_OK) return st;
+    pl.variant = find_variant_flat(g.dtype, g.D, pl.gmax);
+    if (!pl.variant) return fail(PKV_ERR_UNSUPPORTED, "no kernel variant for this shape");
+    return run_decode(pl, a);
+}
+
+size_t flat_workspace_bytes(const FlatGeom &g, int32_t Hq, int32_t num_ctas) {
+    if (Hq < 1 || Hq % g.Hk != 0 || num_ctas < 0 || num_ctas > PKV_MAX_DECODE_CTAS) return 0;
+    int C = num_ctas;
+    if (C == 0 && max_default_ctas(&C) != PKV_OK) return 0;
+    const int G = Hq / g.Hk;
+    return workspace_for(C, G < kMaxHeadsPerUnit ? G : kMaxHeadsPerUnit, g.D);
+}
+
+}  // namespace pkv

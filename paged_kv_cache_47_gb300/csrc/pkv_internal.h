@@ -57,6 +57,13 @@ struct DecodeParams {
     unsigned *err;              // device error word
     const void *kp, *vp;        // pools [NB][Hk][B][D] (elements, or 8-bit codes)
     const float *ks, *vs;       // 8-bit caches: row scales [NB][Hk][B]; else unused
+    // Flat spans (decode over one contiguous span per sequence instead of
+    // blocks): kp is K of slot 0, slot i starts slot_stride bytes further, V
+    // sits v_off bytes after K, and token t of kv head g is row t * Hk + g.
+    // NB is then the number of slots and M * B the span capacity in tokens.
+    const int32_t *slots;       // [S] batch entry -> slot (flat spans only)
+    const int32_t *committed;   // [NB] tokens of each slot backed by memory
+    size_t slot_stride, v_off;
 };
 
 using SplitLaunchFn = cudaError_t (*)(const DecodeParams &, cudaStream_t);
@@ -76,6 +83,27 @@ const DecodeVariant *find_variant_bf16(int D, int gmax, bool mma);
 // 8-bit caches (decode_quant.cu): code_dtype PKV_INT8 / PKV_FP8_E4M3, q in
 // act_dtype PKV_F16 / PKV_BF16, tensor-core math, D = 128, gmax 8 or 16.
 const DecodeVariant *find_variant_quant(int code_dtype, int act_dtype, int D, int gmax);
+// Flat spans (decode_flat.cu): fp16 / bf16, tensor-core math, D 64 or 128, gmax 8 or 16.
+const DecodeVariant *find_variant_flat(int dtype, int D, int gmax);
+
+// Flat spans (flat_cache.cu owns the memory; pkv_api.cu runs the decode).
+// The split kernel's producer splits a tile's rows into groups as it splits
+// them into pool blocks; flat spans use groups of this many rows.
+constexpr int kFlatRowsPerGroup = 16;
+struct FlatGeom {
+    const void *k_base;          // K span of slot 0
+    size_t slot_stride, v_off;   // bytes
+    const int32_t *committed;    // device [num_slots]
+    int32_t num_slots, capacity, Hk, D, dtype;
+};
+pkv_status decode_flat(const FlatGeom &g, const void *q, int32_t S, int32_t Hq,
+                       const int32_t *slots, const int32_t *lens, float scale, void *out,
+                       int32_t out_dtype, void *ws, size_t ws_bytes, cudaStream_t stream,
+                       const pkv_decode_options *o);
+size_t flat_workspace_bytes(const FlatGeom &g, int32_t Hq, int32_t num_ctas);
+
+// The device error word of the current device (PKV_DEVERR_* bits).
+pkv_status device_error_word(unsigned **out);
 
 // Zero pkv_decode_attention_static's scratch on the current device (after a
 // timed-out wait may have left arrival counters set).

@@ -12,7 +12,7 @@ import torch
 from paged_kv_cache_47_gb300 import binding, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = [os.path.join(ROOT, "include", h) for h in ("pkv.h", "pkv_block_manager.h")]
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("pkv.h", "pkv_block_manager.h", "pkv_flat.h")]
 
 
 @pytest.fixture(scope="module")
