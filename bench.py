@@ -489,6 +489,40 @@ class PoolsFlat:
         raise RuntimeError("clone a flat cache by filling a new one")
 
 
+class PoolsPrefix(Pools16):
+    """A 16-bit paged cache decoded prefix-aware: all sequences form one group
+    sharing the prefix blocks they still hold in common."""
+
+    def __init__(self, kp, vp, shared_blocks):
+        super().__init__(kp, vp)
+        self.shared_blocks = shared_blocks
+
+    def clone(self):
+        return PoolsPrefix(self.kp.clone(), self.vp.clone(), self.shared_blocks)
+
+    def workspace(self, Hq):
+        return None        # sized per call shape in prepared()
+
+    def prepared(self, q, kn, vn, slots, tables, lens, scale, out, ws, consumer=0):
+        from paged_kv_cache_47_gb300 import binding
+        S = q.shape[0]
+        gos, gpb = [0] * S, [self.shared_blocks]
+        n = binding.prefix_workspace_bytes(self.kp, S, q.shape[1], tables.shape[1], gos, gpb)
+        pws = torch.zeros(n, dtype=torch.uint8, device=q.device)
+        app = binding.PreparedAppend(kn, vn, slots, self.kp, self.vp)
+        kp, vp = self.kp, self.vp
+
+        def dec(stream, timing_events=None):
+            s = stream if stream is not None else torch.cuda.current_stream()
+            if timing_events is not None:
+                timing_events[0].record(s)
+            binding.decode_attention_prefix(q, kp, vp, tables, lens, scale, gos, gpb, out=out,
+                                            workspace=pws, stream=s)
+            if timing_events is not None:
+                timing_events[1].record(s)
+        return app, dec
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args):
     from paged_kv_cache_47_gb300 import binding, build
@@ -512,6 +546,9 @@ def run_ours(args):
     if args.dtype:
         from dataclasses import replace
         spec = replace(spec, dtype=args.dtype)
+    if args.suffix_hi is not None:
+        from dataclasses import replace
+        spec = replace(spec, suffix_hi=args.suffix_hi)
     st = W.make_structure(spec, args.seed)
     scale = 1.0 / math.sqrt(spec.head_dim)
     vals = W.make_values(st, args.seed, device=dev)
@@ -521,7 +558,15 @@ def run_ours(args):
     slots = st.slot_mapping.to(dev)
     S, Hq, D = vals["q"].shape
     # three resident copies of the cache so every step reads a cold L2
-    if args.flat:
+    if args.prefix_aware:
+        if not spec.shared_prefix:
+            raise SystemExit("--prefix-aware needs a workload with a shared prefix")
+        # after the step's copy-on-write every sequence but one holds a private
+        # copy of the last prefix block, so the group shares the blocks before it
+        shared = spec.shared_prefix // spec.block_size - (1 if cow is not None else 0)
+        base = PoolsPrefix(vals["k_pool"], vals["v_pool"], shared)
+        copies = [base] + [base.clone() for _ in range(args.copies - 1)]
+    elif args.flat:
         if cow is not None:
             raise SystemExit("--flat: flat spans share no blocks (no copy-on-write workloads)")
         if args.kv_quant:
@@ -665,6 +710,10 @@ def run_ours(args):
         "dtype": args.kv_quant or spec.dtype,
         "data": "synthetic (seeded N(0,1) values, random block tables)",
         "config": {**workload_config(spec, st),
+                   **({"decode": "prefix-aware: the shared prefix decoded once for all "
+                                 "sharers' heads, suffixes apart, log-sum-exp merge "
+                                 "(pkv_decode_attention_prefix; 5 launches)"}
+                      if args.prefix_aware else {}),
                    **({"kv_cache": "flat spans: one virtual range per sequence, physical "
                                    "chunks mapped on demand (pkv_flat_*)",
                        "flat_committed_bytes_per_copy": int(copies[0].fc.info().committed_bytes),
@@ -694,7 +743,10 @@ def run_ours(args):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
         "other_kernels": side or None,
         "block_manager": time_block_manager(st, spec) if rank == 0 else None,
-        "gpu_launches": (2 + (1 if cow is not None else 0)) * args.steps,
+        # append + decode (+ copy-on-write); the prefix-aware decode is five
+        # launches: q gather, suffix tables, prefix decode, suffix decode, merge
+        "gpu_launches": (1 + (5 if args.prefix_aware else 1) + (1 if cow is not None else 0))
+                        * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
         "host_enqueue_s": round(enqueue_s, 4),
@@ -791,6 +843,10 @@ def main():
     ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size")
     ap.add_argument("--dtype", choices=["f32", "f16", "bf16"], default=None,
                     help="override the workload's K/V dtype")
+    ap.add_argument("--prefix-aware", action="store_true",
+                    help="decode shared prefixes once per group of sharers (shared-prefix workload)")
+    ap.add_argument("--suffix-hi", type=int, default=None,
+                    help="override the shared-prefix workload's largest private suffix")
     ap.add_argument("--flat", action="store_true",
                     help="flat per-sequence spans in virtual memory instead of a paged pool")
     ap.add_argument("--kv-quant", choices=["int8", "fp8_e4m3"], default=None,

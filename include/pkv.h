@@ -175,6 +175,11 @@ typedef struct {
                                 first 1024 sequences (NULL = not recorded);
                                 under stream capture they become event-record
                                 nodes */
+    float *lse_out;          /* optional device [num_seqs][num_q_heads] fp32:
+                                log2 of the softmax denominator of each head,
+                                log2 sum_t exp(scale <q, k_t>) (-inf for an
+                                empty context), to merge partial attentions
+                                computed apart; NULL = not written          */
 } pkv_decode_options;
 
 /* Workspace bytes for pkv_decode_attention_ex with options->num_ctas = num_ctas
@@ -241,6 +246,50 @@ pkv_status pkv_decode_attention_static(const pkv_cache_desc *cache, const void *
  */
 pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pairs,
                           int32_t num_pairs, void *k_pool, void *v_pool, void *stream);
+
+/* ------------------------------------------------------- prefix-aware decode
+ *
+ * Passage: identical prompt prefixes are stored once and shared by every
+ * request holding them ("KV-Cache Optimization & PagedAttention for
+ * Long-Context Agents", section "Key KV-Cache Optimization Principles", item
+ * 3). pkv_decode_attention_prefix also reads them once per group of sharers:
+ * the prefix is attended for all sharers' query heads together (up to 16
+ * heads per pass of the decode kernel), each sequence's private suffix on its
+ * own, and the two partial attentions are merged by log-sum-exp. The result
+ * is the plain decode's, up to rounding.
+ */
+typedef struct {
+    int32_t num_groups;
+    const int32_t *group_of_seq;         /* host [num_seqs]: group id, or -1     */
+    const int32_t *group_prefix_blocks;  /* host [num_groups]: shared leading
+                                            table entries (>= 1); every member's
+                                            table holds the same ids there and
+                                            its length is at least that many
+                                            blocks (a shorter one sets
+                                            PKV_DEVERR_CONTEXT)                */
+} pkv_prefix_groups;
+
+/* Workspace bytes of pkv_decode_attention_prefix (0 on invalid arguments). */
+size_t pkv_decode_prefix_workspace_bytes(const pkv_cache_desc *cache, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                         const pkv_prefix_groups *groups, int32_t num_ctas);
+
+/*
+ * pkv_decode_attention_ex for sequences that share prefixes: same inputs and
+ * output, plus the group description. workspace: at least
+ * pkv_decode_prefix_workspace_bytes, zero-filled before its first use. The
+ * call enqueues a few kernels and copies its small index arrays from the host
+ * (so it is not capturable in a CUDA graph). options: num_ctas and consumer
+ * apply to each decode; timing_events and lse_out are ignored.
+ */
+pkv_status pkv_decode_attention_prefix(const pkv_cache_desc *cache, const void *q,
+                                       int32_t num_seqs, int32_t num_q_heads, const void *k_pool,
+                                       const void *v_pool, const int32_t *block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                       float scale, const pkv_prefix_groups *groups, void *out,
+                                       int32_t out_dtype, void *workspace,
+                                       size_t workspace_bytes, void *stream,
+                                       const pkv_decode_options *options);
 
 /* ------------------------------------------------------------ 8-bit KV cache
  *

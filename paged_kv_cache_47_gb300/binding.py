@@ -38,7 +38,12 @@ class QCacheDesc(ctypes.Structure):
 
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int32), ("consumer", ctypes.c_int32),
-                ("timing_events", ctypes.c_void_p * 2)]
+                ("timing_events", ctypes.c_void_p * 2), ("lse_out", ctypes.c_void_p)]
+
+
+class PrefixGroups(ctypes.Structure):
+    _fields_ = [("num_groups", ctypes.c_int32), ("group_of_seq", ctypes.c_void_p),
+                ("group_prefix_blocks", ctypes.c_void_p)]
 
 
 class PkvError(RuntimeError):
@@ -88,6 +93,14 @@ def lib():
         L.pkv_decode_attention_quant.restype = i32
         L.pkv_block_copy_quant.argtypes = [qp, vp, i32, vp, vp, vp, vp, vp]
         L.pkv_block_copy_quant.restype = i32
+        L.pkv_decode_prefix_workspace_bytes.argtypes = [dp, i32, i32, i32,
+                                                        ctypes.POINTER(PrefixGroups), i32]
+        L.pkv_decode_prefix_workspace_bytes.restype = sz
+        L.pkv_decode_attention_prefix.argtypes = [dp, vp, i32, i32, vp, vp, vp, i32, vp,
+                                                  ctypes.c_float, ctypes.POINTER(PrefixGroups),
+                                                  vp, i32, vp, sz, vp,
+                                                  ctypes.POINTER(DecodeOptions)]
+        L.pkv_decode_attention_prefix.restype = i32
         L.pkv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
         L.pkv_get_error.restype = i32
         L.pkv_status_string.argtypes = [i32]
@@ -157,7 +170,7 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
                      out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
                      workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
                      consumer: int = 0, timing_events: Optional[Sequence] = None,
-                     stream=None) -> torch.Tensor:
+                     stream=None, lse_out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Paged decode attention: out[s][h] = softmax(scale q K^T) V over context_lens[s] tokens."""
     desc = _pools(k_pool, v_pool)
     S, Hq, D = q.shape
@@ -175,6 +188,9 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
     if timing_events is not None:
         for i, ev in enumerate(timing_events):
             opts.timing_events[i] = None if ev is None else ev.cuda_event
+    if lse_out is not None:
+        assert lse_out.dtype == torch.float32 and lse_out.shape == (S, Hq) and lse_out.is_contiguous()
+        opts.lse_out = lse_out.data_ptr()
     _check(lib().pkv_decode_attention_ex(
         ctypes.byref(desc), _ptr(q), S, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(bt), bt.shape[1],
         _ptr(cl), float(scale), _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace),
@@ -645,3 +661,53 @@ class FlatCache:
             DTYPE_CODE[out.dtype], _ptr(workspace), workspace.numel(), _stream(stream),
             ctypes.byref(opts)))
         return out
+
+
+# ------------------------------------------------------------------ prefix-aware decode
+class _Groups:
+    """Host arrays of a prefix-group description, kept alive with the struct."""
+
+    def __init__(self, group_of_seq, group_prefix_blocks):
+        self.gos = torch.as_tensor(list(group_of_seq), dtype=torch.int32).contiguous()
+        self.gpb = torch.as_tensor(list(group_prefix_blocks), dtype=torch.int32).contiguous()
+        self.st = PrefixGroups(len(self.gpb), self.gos.data_ptr() if len(self.gos) else None,
+                               self.gpb.data_ptr() if len(self.gpb) else None)
+
+
+def prefix_workspace_bytes(k_pool, num_seqs, num_q_heads, max_blocks_per_seq, group_of_seq,
+                           group_prefix_blocks, num_ctas: int = 0) -> int:
+    g = _Groups(group_of_seq, group_prefix_blocks)
+    desc = cache_desc(k_pool)
+    return int(lib().pkv_decode_prefix_workspace_bytes(ctypes.byref(desc), num_seqs, num_q_heads,
+                                                       max_blocks_per_seq, ctypes.byref(g.st),
+                                                       num_ctas))
+
+
+def decode_attention_prefix(q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                            group_of_seq, group_prefix_blocks,
+                            out: Optional[torch.Tensor] = None,
+                            out_dtype: Optional[torch.dtype] = None,
+                            workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                            stream=None) -> torch.Tensor:
+    """Decode where the sequences of each group share their first
+    group_prefix_blocks[g] table entries (group_of_seq[s] = g, or -1)."""
+    desc = _pools(k_pool, v_pool)
+    S, Hq, D = q.shape
+    q = q.contiguous()
+    bt, cl = block_tables.contiguous(), context_lens.contiguous()
+    g = _Groups(group_of_seq, group_prefix_blocks)
+    if out is None:
+        out = torch.empty(S, Hq, D, dtype=out_dtype or q.dtype, device=q.device)
+    if workspace is None:
+        n = prefix_workspace_bytes(k_pool, S, Hq, bt.shape[1], group_of_seq, group_prefix_blocks,
+                                   num_ctas)
+        if n == 0:
+            raise PkvError(-1, lib().pkv_last_error_message().decode())
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    opts = DecodeOptions()
+    opts.num_ctas = num_ctas
+    _check(lib().pkv_decode_attention_prefix(
+        ctypes.byref(desc), _ptr(q), S, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(bt), bt.shape[1],
+        _ptr(cl), float(scale), ctypes.byref(g.st), _ptr(out), DTYPE_CODE[out.dtype],
+        _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts)))
+    return out

@@ -718,6 +718,8 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
                 const int j = idx / D, d = idx - (idx / D) * D;
                 store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype,
                           O[k] / W[k]);
+                if (p.lse_out && d == 0)
+                    p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + j] = Mx[k] + log2f(W[k]);
             }
         }
     }
@@ -767,6 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (seq_len[s] == 0 && s % C == cta) {
             for (int i = tid; i < p.Hq * D; i += kThreads)
                 store_out(p.out, (size_t)s * p.Hq * D + i, p.out_dtype, 0.f);
+            if (p.lse_out)
+                for (int h = tid; h < p.Hq; h += kThreads)
+                    p.lse_out[(size_t)s * p.Hq + h] = -CUDART_INF_F;
         }
     }
 
@@ -992,6 +997,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float o = O / Ls;
                 if (whole) {
                     store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype, o);
+                    if (p.lse_out && d == 0)
+                        p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + j] = M + log2f(Ls);
                 } else {
                     p.ws_o[(size_t)(base + j) * D + d] = o;
                     // lane 0 holds one element of every head in the slice:

@@ -420,6 +420,7 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
         p.out_dtype = a.out_dtype;
         p.block_tables = a.tables ? a.tables + (size_t)s0 * a.M : nullptr;
         p.slots = a.slots ? a.slots + s0 : nullptr;
+        p.lse_out = a.opts && a.opts->lse_out ? a.opts->lse_out + (size_t)s0 * a.Hq : nullptr;
         p.committed = a.committed;
         p.slot_stride = a.slot_stride;
         p.v_off = a.v_off;

@@ -61,6 +61,7 @@ struct DecodeParams {
     // blocks): kp is K of slot 0, slot i starts slot_stride bytes further, V
     // sits v_off bytes after K, and token t of kv head g is row t * Hk + g.
     // NB is then the number of slots and M * B the span capacity in tokens.
+    float *lse_out;             // optional [S][Hq]: log2 sum_t exp(scaled score)
     const int32_t *slots;       // [S] batch entry -> slot (flat spans only)
     const int32_t *committed;   // [NB] tokens of each slot backed by memory
     size_t slot_stride, v_off;
