@@ -58,27 +58,38 @@ namespace pkv {
 constexpr int kQuantInt8 = 1;
 constexpr int kQuantE4m3 = 2;
 
+// 8-bit variants with one mma n-tile take 128-token tiles and eight math
+// warps: an 8-bit tile carries half the bytes of a 16-bit one, so twice the
+// tokens keep the producer's per-tile cost and the math warps' per-tile
+// latency below the time HBM takes to deliver it. Every other variant takes
+// 64-token tiles and four math warps.
+constexpr bool big_tiles(int QK, int GMAX) { return QK != 0 && GMAX == 8; }
+constexpr int tile_tokens(int QK, int GMAX) { return big_tiles(QK, GMAX) ? 128 : PKV_TILE_TOKENS; }
+constexpr int math_warps(int QK, int GMAX) { return big_tiles(QK, GMAX) ? 8 : kConsumerWarps; }
+constexpr int kernel_threads(int QK, int GMAX) { return 32 * (math_warps(QK, GMAX) + kProducerWarps); }
+
 template <typename T, int D, int GMAX, bool MMA, int QK = 0>
 struct SplitCfg {
     static constexpr int ES = QK ? 1 : (int)sizeof(T);  // bytes of one cache element
     static constexpr int ROWB = D * ES;              // bytes of one K or V row
     static constexpr int QROWB = D * (int)sizeof(T); // bytes of one q row
     static constexpr int NP = ROWB / 128;            // 128-byte swizzle planes per row
-    static constexpr int PLANE = PKV_TILE_TOKENS * 128;
+    static constexpr int TT = tile_tokens(QK, GMAX);   // tokens per tile
+    static constexpr int CW = math_warps(QK, GMAX);    // math warps
+    static constexpr int THREADS = kernel_threads(QK, GMAX);
+    static constexpr int PLANE = TT * 128;
     static constexpr int KVB = NP * PLANE;           // bytes of one tile of K (or V)
     static constexpr int SCB = QK ? 1024 : 0;        // K then V scales of the tile (2 x 256 B)
     static constexpr int QB = ((GMAX * QROWB + 1023) / 1024) * 1024;
     static constexpr int STAGE = 2 * KVB + SCB + QB; // multiple of 1024
-    // codes converted to 16-bit K and V tiles, one buffer reused every tile
-    static constexpr int CONV = QK ? 2 * (QROWB / 128) * PLANE : 0;
     static constexpr int NTN = GMAX / 8;             // mma n-tiles (MMA only)
-    static constexpr int COMB_O = kConsumerWarps * GMAX * D * 4;
-    static constexpr int COMB_ML = 2 * kConsumerWarps * GMAX * 4;
-    static constexpr int PBUF = MMA ? kConsumerWarps * NTN * 2 * 256 : 0;
+    static constexpr int COMB_O = CW * GMAX * D * 4;
+    static constexpr int COMB_ML = 2 * CW * GMAX * 4;
+    static constexpr int PBUF = MMA ? CW * NTN * 2 * 256 : 0;
     static constexpr int SEQ_MAX = (2 * kMaxSeqsPerLaunch + 1) * 4;
     static constexpr int SMEM_LIMIT = 227 * 1024;
     static constexpr int PER_STAGE_EXTRA = (int)sizeof(TileMeta) + 16;  // meta + 2 barriers
-    static constexpr int FIXED = 1024 /*alignment slack*/ + CONV + COMB_O + COMB_ML + PBUF +
+    static constexpr int FIXED = 1024 /*alignment slack*/ + COMB_O + COMB_ML + PBUF +
                                  16 /*comb bars*/ + SEQ_MAX + 64;
     static constexpr int NST_FIT = (SMEM_LIMIT - FIXED) / (STAGE + PER_STAGE_EXTRA);
     static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
@@ -87,15 +98,14 @@ struct SplitCfg {
     static_assert(!QK || MMA, "8-bit caches use the tensor-core math");
 
     // offsets from the 1024-aligned base
-    static constexpr int OFF_CONV = NST * STAGE;
-    static constexpr int OFF_META = OFF_CONV + CONV;
+    static constexpr int OFF_META = NST * STAGE;
     static constexpr int OFF_FULL = OFF_META + NST * (int)sizeof(TileMeta);
     static constexpr int OFF_EMPTY = OFF_FULL + NST * 8;
     static constexpr int OFF_CBAR = OFF_EMPTY + NST * 8;   // comb_full, comb_empty
     static constexpr int OFF_COMB_O = OFF_CBAR + 16;
     static constexpr int OFF_COMB_M = OFF_COMB_O + COMB_O;
-    static constexpr int OFF_COMB_L = OFF_COMB_M + kConsumerWarps * GMAX * 4;
-    static constexpr int OFF_PBUF = OFF_COMB_L + kConsumerWarps * GMAX * 4;
+    static constexpr int OFF_COMB_L = OFF_COMB_M + CW * GMAX * 4;
+    static constexpr int OFF_PBUF = OFF_COMB_L + CW * GMAX * 4;
     static constexpr int OFF_SEQ = OFF_PBUF + PBUF;
 
     static size_t smem_bytes(int S) { return 1024 + OFF_SEQ + (size_t)(2 * S + 1) * 4; }
@@ -107,7 +117,7 @@ struct SplitCfg {
 // seq_len[s]   = context length clamped to [0, M*B] (a clamp flags the error word)
 // seq_prefix[s]= U * sum_{s'<s} ceil(seq_len[s'] / 64), seq_prefix[S] = NT
 // Ends with __syncthreads(); all threads of the block must call it.
-template <bool FLAT>
+template <bool FLAT, int TT>
 __device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq_prefix,
                                                  int *seq_len, bool report) {
     const int tid = threadIdx.x;
@@ -136,7 +146,7 @@ __device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq
         int running = 0;
         for (int base = 0; base < p.S; base += 32) {
             const int s = base + lane;
-            const int n = (s < p.S) ? pkv_tiles_of_len(seq_len[s]) * p.U : 0;
+            const int n = (s < p.S) ? pkv_tiles_of_len(seq_len[s], TT) * p.U : 0;
             int incl = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -154,9 +164,10 @@ __device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq
 // Swizzled shared-memory address of 16-byte chunk `chunk` (0..8*NP-1) of row r
 // in a tile stored as NP planes of [64 rows][128 bytes] with a 128-byte
 // XOR swizzle (chunk index XOR row%8 within each 1024-byte atom).
+template <int TT = PKV_TILE_TOKENS>
 __device__ __forceinline__ uint32_t swz(uint32_t base, int r, int chunk) {
     const int pl = chunk >> 3, c = chunk & 7;
-    return base + pl * (PKV_TILE_TOKENS * 128) + r * 128 + ((c ^ (r & 7)) << 4);
+    return base + pl * (TT * 128) + r * 128 + ((c ^ (r & 7)) << 4);
 }
 
 // ---------------------------------------------------------------------------
@@ -191,6 +202,32 @@ __device__ __forceinline__ void lds_vec(uint32_t addr, float (&out)[N]) {
             out[2 * i] = Elem<T>::to_f32(h[0]);
             out[2 * i + 1] = Elem<T>::to_f32(h[1]);
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 8-bit codes -> fp16 (exact: every int8 and E4M3 value is an fp16 value)
+// ---------------------------------------------------------------------------
+// Four codes (lowest address in the low byte) -> two fp16 pairs.
+template <int QK>
+__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    if constexpr (QK == kQuantInt8) {
+        // byte b + 128 placed under the fp16 exponent of 1024 (0x64nn) reads
+        // as 1024 + b + 128; subtracting 1152 leaves b exactly
+        const uint32_t u = w ^ 0x80808080u;
+        uint32_t a, b;
+        asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+        asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
+        __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+        lo = *reinterpret_cast<uint32_t *>(&ha);
+        hi = *reinterpret_cast<uint32_t *>(&hb);
+    } else {
+        const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
+        const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
+        lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
+        hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
     }
 }
 
@@ -346,11 +383,21 @@ struct Consumer<T, D, GMAX, false, 0> {
 // Tensor-core math: per warp, S^T[16 tokens x 8 heads] = K Q^T and
 // O^T[D x 8 heads] += V^T P^T with mma.sync m16n8k16 (fp32 accumulate).
 //
-// 8-bit caches (QK != 0): the math warps first turn their rows of codes into
-// exact fp16 values (convert_rows), so the products run in fp16. Each q head
-// is scaled by a power of two 2^-e (e >= 0) that keeps it below 2^15, and e
-// is folded back into that head's score factor; the scaling is exact. The
-// row scales enter as
+// 8-bit caches (QK != 0): codes go from shared memory straight into the mma
+// fragments as exact fp16 values (every int8 and E4M3 value is one), with no
+// 16-bit copy of the tile. Two index permutations make each thread's codes
+// whole 16-byte chunks:
+//  - S^T = K Q^T sums over d, so d may be renumbered in K and q alike: lane
+//    (g, t) = (lane / 4, lane % 4) takes bytes [32t, 32t + 32) of K rows g and
+//    g + 8, and k-step ks, k index {2t, 2t+1, 2t+8, 2t+9} stands for element
+//    32t + 4ks + {0, 1, 2, 3}; load_q puts q in the same order.
+//  - in O^T = V^T P^T the rows of O^T are d: row 16mt + g of m-tile mt stands
+//    for element 16g + 2mt and row 16mt + g + 8 for 16g + 2mt + 1, so lane
+//    (g, t) takes bytes [16g, 16g + 16) of V rows 2t, 2t+1, 2t+8, 2t+9 (the
+//    tokens of its fragment); write_comb puts d back in order.
+// Each q head is scaled by a power of two 2^-e (e >= 0) that keeps it below
+// 2^15, and e is folded back into that head's score factor; the scaling is
+// exact. The row scales enter as
 //     score_t = s_k[t] * <q, code_k[t]>,
 //     o = sum_t p_t s_v[t] code_v[t] / sum_t p_t,
 // with s_v[t] / max(s_v of the warp's 16 rows) multiplied into p_t before
@@ -359,6 +406,7 @@ struct Consumer<T, D, GMAX, false, 0> {
 template <typename T, int D, int GMAX, int QK>
 struct Consumer<T, D, GMAX, true, QK> {
     using MT = typename std::conditional<QK != 0, __half, T>::type;  // mma operand type
+    static constexpr int TT = tile_tokens(QK, GMAX);                  // rows of a tile
     static constexpr int NTN = GMAX / 8;
     static constexpr int KS = D / 16;
     uint32_t qb[NTN][KS][2];
@@ -411,7 +459,7 @@ struct Consumer<T, D, GMAX, true, QK> {
                 for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        const int d = ks * 16 + (j >> 1) * 8 + k_in + (j & 1);
+                        const int d = 32 * (lane & 3) + 4 * ks + j;   // renumbered d
                         const float x = h < gca ? Elem<T>::to_f32(row[d]) : 0.f;
                         amax = fmaxf(amax, fabsf(x));
                     }
@@ -425,7 +473,8 @@ struct Consumer<T, D, GMAX, true, QK> {
                 for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        const int d = ks * 16 + half * 8 + k_in;
+                        // k indices {2t, 2t+1} (half 0), {2t+8, 2t+9} (half 1)
+                        const int d = 32 * (lane & 3) + 4 * ks + 2 * half;
                         const float x0 = h < gca ? Elem<T>::to_f32(row[d]) * mul : 0.f;
                         const float x1 = h < gca ? Elem<T>::to_f32(row[d + 1]) * mul : 0.f;
                         __half2 q2 = __floats2half2_rn(x0, x1);
@@ -442,30 +491,58 @@ struct Consumer<T, D, GMAX, true, QK> {
         }
     }
 
-    // ksc / vsc: the tile's K and V row scales (8-bit caches only)
+    // 8-bit caches: sK / sV hold codes, ksc / vsc the tile's row scales
     __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int ntok, int warp, int lane,
                                          const float *ksc = nullptr, const float *vsc = nullptr) {
         const int r0 = 16 * warp;
         const int nval = ntok - r0;
         if (nval <= 0) return;
+        const int g = lane >> 2, t = lane & 3;
+        // 8-bit caches: all of this lane's codes of the tile, K then V, are
+        // loaded before any is used (16-byte chunks; a quarter-warp's eight
+        // chunks fall in distinct bank groups under the swizzle)
+        uint32_t kw[2][8], vw[4][4];
+        if constexpr (QK != 0) {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    lds_u32x4(swz<TT>(sK, r0 + g + 8 * rr, 2 * t + c), kw[rr][4 * c], kw[rr][4 * c + 1],
+                              kw[rr][4 * c + 2], kw[rr][4 * c + 3]);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                lds_u32x4(swz<TT>(sV, r0 + 2 * t + (k & 1) + 8 * (k >> 1), g), vw[k][0], vw[k][1],
+                          vw[k][2], vw[k][3]);
+        }
         // ---- S^T = K Q^T
         float s[NTN][4];
 #pragma unroll
         for (int nt = 0; nt < NTN; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
-        {
+        if constexpr (QK != 0) {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                codes_to_f16<QK>(kw[0][ks], a0, a2);   // row g:     k 2t, 2t+1 | 2t+8, 2t+9
+                codes_to_f16<QK>(kw[1][ks], a1, a3);   // row g + 8
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt)
+                    MmaOp<MT>::run(s[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+            }
+        } else {
             const int row = r0 + (lane & 15);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int chunk = ks * 2 + (lane >> 4);
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4(swz(sK, row, chunk), a0, a1, a2, a3);
+                ldsm_x4(swz<TT>(sK, row, chunk), a0, a1, a2, a3);
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt)
                     MmaOp<MT>::run(s[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
             }
         }
+
         // ---- online softmax (tokens rA, rB; heads 8nt + 2*(lane%4) + hh)
         const int rA = r0 + (lane >> 2), rB = rA + 8;
         const bool vA = rA < ntok, vB = rB < ntok;
@@ -543,13 +620,34 @@ struct Consumer<T, D, GMAX, true, QK> {
             ldsm_x2_t(lo + (lane & 15) * 16, bl[nt][0], bl[nt][1]);
         }
         // ---- O^T += V^T P^T
-        {
+        if constexpr (QK != 0) {
+            // m-tile mt: rows g / g + 8 are elements 16g + 2mt / + 1, i.e.
+            // byte 2mt / 2mt + 1 of the chunk; k = tokens 2t, 2t+1 (vw[0], vw[1])
+            // and 2t+8, 2t+9 (vw[2], vw[3]), paired byte-wise
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    const int mt = 2 * i + hb;
+                    const uint32_t sel = hb ? 0x7362u : 0x5140u;
+                    uint32_t z01, z23, a0, a1, a2, a3;
+                    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(z01) : "r"(vw[0][i]), "r"(vw[1][i]), "r"(sel));
+                    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(z23) : "r"(vw[2][i]), "r"(vw[3][i]), "r"(sel));
+                    codes_to_f16<QK>(z01, a0, a1);
+                    codes_to_f16<QK>(z23, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < NTN; ++nt) {
+                        MmaOp<MT>::run(acc[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
+                        MmaOp<MT>::run(acc[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
+                    }
+                }
+        } else {
             const int tok = r0 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int chunk = mt * 2 + ((lane >> 3) & 1);
                 uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(swz(sV, tok, chunk), a0, a1, a2, a3);
+                ldsm_x4_t(swz<TT>(sV, tok, chunk), a0, a1, a2, a3);
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt) {
                     MmaOp<MT>::run(acc[mt][nt], a0, a1, a2, a3, bh[nt][0], bh[nt][1]);
@@ -580,77 +678,18 @@ struct Consumer<T, D, GMAX, true, QK> {
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int h = nt * 8 + (lane & 3) * 2;
-                const int d = mt * 16 + (lane >> 2);
+                // rows g and g + 8 of m-tile mt hold elements d and d + dd
+                const int d = QK != 0 ? 16 * (lane >> 2) + 2 * mt : mt * 16 + (lane >> 2);
+                const int dd = QK != 0 ? 1 : 8;
                 float *o = comb_o + (warp * GMAX + h) * D;
                 o[d] = acc[mt][nt][0] * sg;
                 o[D + d] = acc[mt][nt][1] * sg;
-                o[d + 8] = acc[mt][nt][2] * sg;
-                o[D + d + 8] = acc[mt][nt][3] * sg;
+                o[d + dd] = acc[mt][nt][2] * sg;
+                o[D + d + dd] = acc[mt][nt][3] * sg;
             }
         }
     }
 };
-
-// ---------------------------------------------------------------------------
-// 8-bit codes -> fp16 (exact: every int8 and E4M3 value is an fp16 value)
-// ---------------------------------------------------------------------------
-// Four codes (lowest address in the low byte) -> two fp16 pairs.
-template <int QK>
-__device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    if constexpr (QK == kQuantInt8) {
-        // byte b + 128 placed under the fp16 exponent of 1024 (0x64nn) reads
-        // as 1024 + b + 128; subtracting 1152 leaves b exactly
-        const uint32_t u = w ^ 0x80808080u;
-        uint32_t a, b;
-        asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
-        asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
-        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-        __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
-        __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
-        lo = *reinterpret_cast<uint32_t *>(&ha);
-        hi = *reinterpret_cast<uint32_t *>(&hb);
-    } else {
-        const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
-        const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
-        lo = (uint32_t)a.x | ((uint32_t)a.y << 16);
-        hi = (uint32_t)b.x | ((uint32_t)b.y << 16);
-    }
-}
-
-// Math warp `warp` converts its 16 rows of the 8-bit K and V tiles (one
-// 128-byte plane per row, D = 128) into the 16-bit tile layout (two planes
-// per row) that the tensor-core tile step reads. Lanes take whole 16-byte
-// chunks; all eight loads are issued before any conversion or store.
-template <int QK>
-__device__ __forceinline__ void convert_rows(uint32_t srcK, uint32_t srcV, uint32_t dstK,
-                                             uint32_t dstV, int warp, int lane) {
-    uint32_t w[8][4];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int i = lane + 32 * (k & 3);
-        const int row = 16 * warp + (i >> 3), ch = i & 7;
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[k][0]), "=r"(w[k][1]), "=r"(w[k][2]), "=r"(w[k][3])
-                     : "r"(swz(k < 4 ? srcK : srcV, row, ch)));
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const int i = lane + 32 * (k & 3);
-        const int row = 16 * warp + (i >> 3), ch = i & 7;
-        const uint32_t dst = k < 4 ? dstK : dstV;
-        uint32_t h[8];
-        codes_to_f16<QK>(w[k][0], h[0], h[1]);
-        codes_to_f16<QK>(w[k][1], h[2], h[3]);
-        codes_to_f16<QK>(w[k][2], h[4], h[5]);
-        codes_to_f16<QK>(w[k][3], h[6], h[7]);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst, row, 2 * ch)),
-                     "r"(h[0]), "r"(h[1]), "r"(h[2]), "r"(h[3])
-                     : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(swz(dst, row, 2 * ch + 1)),
-                     "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                     : "memory");
-    }
-}
 
 // ---------------------------------------------------------------------------
 // log-sum-exp merge of one warp's slice of a unit cut by CTA boundaries
@@ -668,7 +707,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
     // the lane's elements are idx = warp*32 + lane + 128k, k < EPL, taken in
     // chunks of KC: all loads of one partial for a chunk are issued before
     // any of them is used, and at most KC elements are live at a time
-    constexpr int EPL = (GMAX * D + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+    constexpr int EPL = (GMAX * D + kMergeSlices * 32 - 1) / (kMergeSlices * 32);
     constexpr int KC = EPL < 8 ? EPL : 8;
     const int C = p.C;
     const int n_el = mt.gca * D;
@@ -676,7 +715,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
     const int slot_first = pkv_partial_slot(c_first, C, NT, mt.tu);
 #pragma unroll 1
     for (int k0 = 0; k0 < EPL; k0 += KC) {
-        if (warp * 32 + k0 * kConsumerWarps * 32 >= n_el) break;
+        if (warp * 32 + k0 * kMergeSlices * 32 >= n_el) break;
         float Mx[KC], W[KC], O[KC];
 #pragma unroll
         for (int k = 0; k < KC; ++k) {
@@ -690,19 +729,19 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
             const int slot = c * 2 + (c == c_first ? slot_first : 0);
             // lane h < gca fetches this warp's copy of head h's lse
             const float lse_h =
-                lane < mt.gca ? __ldcg(p.ws_lse + (slot * kConsumerWarps + warp) * p.GC + lane)
+                lane < mt.gca ? __ldcg(p.ws_lse + (slot * kMergeSlices + warp) * p.GC + lane)
                               : 0.f;
             float o[KC];
 #pragma unroll
             for (int k = 0; k < KC; ++k) {
-                const int idx = warp * 32 + lane + (k0 + k) * kConsumerWarps * 32;
+                const int idx = warp * 32 + lane + (k0 + k) * kMergeSlices * 32;
                 const int j = idx / D, d = idx - (idx / D) * D;
                 o[k] = idx < n_el ? __ldcg(p.ws_o + (size_t)(slot * p.GC + j) * D + d) : 0.f;
             }
 #pragma unroll
             for (int k = 0; k < KC; ++k) {
                 // head of element k0 + k: the same for every lane of the warp
-                const int j = (warp * 32 + (k0 + k) * kConsumerWarps * 32) / D;
+                const int j = (warp * 32 + (k0 + k) * kMergeSlices * 32) / D;
                 const float lse = __shfl_sync(0xffffffffu, lse_h, j & 31);
                 const float mn = fmaxf(Mx[k], lse);
                 const float a = exp2f(Mx[k] - mn), w = exp2f(lse - mn);
@@ -713,7 +752,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
         }
 #pragma unroll
         for (int k = 0; k < KC; ++k) {
-            const int idx = warp * 32 + lane + (k0 + k) * kConsumerWarps * 32;
+            const int idx = warp * 32 + lane + (k0 + k) * kMergeSlices * 32;
             if (idx < n_el) {
                 const int j = idx / D, d = idx - (idx / D) * D;
                 store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype,
@@ -729,7 +768,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
 // the split-K kernel
 // ---------------------------------------------------------------------------
 template <typename T, int D, int GMAX, bool MMA, int QK, bool FLAT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     decode_split_kernel(const DecodeParams p) {
     using Cfg = SplitCfg<T, D, GMAX, MMA, QK>;
     extern __shared__ uint8_t smem_raw[];
@@ -753,24 +792,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < Cfg::NST; ++i) {
             mbar_init(full0 + 8 * i, kProducerThreads + 1);
-            mbar_init(empty0 + 8 * i, kConsumerWarps);
+            mbar_init(empty0 + 8 * i, Cfg::CW);
         }
-        mbar_init(comb_full, kConsumerWarps);
-        mbar_init(comb_empty, kConsumerWarps);
+        mbar_init(comb_full, Cfg::CW);
+        mbar_init(comb_empty, Cfg::CW);
         fence_mbarrier_init();
     }
     // inputs may come from the previous kernel on the stream (launched with
     // programmatic serialisation): wait for it before reading any of them
     grid_dependency_wait();
-    build_seq_arrays<FLAT>(p, seq_prefix, seq_len, cta == 0);
+    build_seq_arrays<FLAT, Cfg::TT>(p, seq_prefix, seq_len, cta == 0);
 
     // zero-length sequences: zeros, written by CTA s % C
     for (int s = 0; s < p.S; ++s) {
         if (seq_len[s] == 0 && s % C == cta) {
-            for (int i = tid; i < p.Hq * D; i += kThreads)
+            for (int i = tid; i < p.Hq * D; i += Cfg::THREADS)
                 store_out(p.out, (size_t)s * p.Hq * D + i, p.out_dtype, 0.f);
             if (p.lse_out)
-                for (int h = tid; h < p.Hq; h += kThreads)
+                for (int h = tid; h < p.Hq; h += Cfg::THREADS)
                     p.lse_out[(size_t)s * p.Hq + h] = -CUDART_INF_F;
         }
     }
@@ -781,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dependents_launch();   // the next kernel on the stream may start its launch now
     if (n_my <= 0) return;
 
-    if (warp >= kConsumerWarps) {
+    if (warp >= Cfg::CW) {
         // ======================= producer warps =======================
         // 128 threads gather each tile with 16-byte cp.async copies straight
         // into the swizzled stage layout. Thread pt copies one physical block
@@ -794,20 +833,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int LA = 8;
         constexpr int CPR = Cfg::ROWB / 16;          // 16-byte chunks per K/V row
         constexpr int CPRQ = Cfg::QROWB / 16;        // 16-byte chunks per q row
-        const int pt = tid - kConsumerWarps * 32;     // 0 .. kProducerThreads-1
-        const int bpt = PKV_TILE_TOKENS / p.B;        // blocks per tile
+        const int pt = tid - Cfg::CW * 32;            // 0 .. kProducerThreads-1
+        const int bpt = Cfg::TT / p.B;                // blocks per tile
         const int tpb = kProducerThreads / bpt;       // producer threads per block
         const int jblk = pt / tpb;
         const int tb = pt - jblk * tpb;
         const uint8_t *kpool = static_cast<const uint8_t *>(p.kp);
         const uint8_t *vpool = FLAT ? kpool + p.v_off : static_cast<const uint8_t *>(p.vp);
         PkvCursor cur, la;
-        pkv_cursor_at(cur, t_begin, seq_prefix, seq_len, p.S);
+        pkv_cursor_at(cur, t_begin, seq_prefix, seq_len, p.S, Cfg::TT);
         la = cur;
         // per tile: the physical block of this thread's rows, or (flat
         // spans) the sequence's slot
         auto load_entry = [&](const PkvCursor &c) -> int {
-            const int ntok = min(PKV_TILE_TOKENS, c.L - c.ti * PKV_TILE_TOKENS);
+            const int ntok = min(Cfg::TT, c.L - c.ti * Cfg::TT);
             if (jblk * p.B >= ntok) return -1;
             if constexpr (FLAT) return __ldg(p.slots + c.s);
             return __ldg(p.block_tables + (size_t)c.s * p.M + c.ti * bpt + jblk);
@@ -818,13 +857,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ent[k] = -1;
             if (k < n_my) {
                 ent[k] = load_entry(la);
-                pkv_cursor_next(la, seq_len, p.S, p.U);
+                pkv_cursor_next(la, seq_len, p.S, p.U, Cfg::TT);
             }
         }
         // This thread's chunks sit at the same places in every tile: row of
         // the tile, swizzled shared-memory offset and byte offset inside the
         // (block, kv head) chunk of the pool, computed once.
-        constexpr int NCH = CPR / 2;                  // K (and V) chunks per thread per tile
+        constexpr int NCH = Cfg::TT * CPR / kProducerThreads;   // K (and V) chunks per thread per tile
         int crow[NCH];
         uint32_t soff[NCH], goff[NCH];
 #pragma unroll
@@ -832,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = tb + c * tpb;             // chunk within the block
             const int rb = idx / CPR, ch = idx - (idx / CPR) * CPR;
             crow[c] = jblk * p.B + rb;
-            soff[c] = swz(0u, crow[c], ch);
+            soff[c] = swz<Cfg::TT>(0u, crow[c], ch);
             // paged: row rb of a (block, kv head) chunk; flat: row crow of the
             // tile, Hk rows apart per token
             goff[c] = FLAT ? (uint32_t)(crow[c] * p.Hk * Cfg::ROWB + ch * 16)
@@ -851,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int e = ent[k];
                 if (it + LA < n_my) {
                     ent[k] = load_entry(la);
-                    pkv_cursor_next(la, seq_len, p.S, p.U);
+                    pkv_cursor_next(la, seq_len, p.S, p.U, Cfg::TT);
                 }
                 const int stage = it % Cfg::NST;
                 const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
@@ -859,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const int ntok = min(PKV_TILE_TOKENS, cur.L - cur.ti * PKV_TILE_TOKENS);
+                const int ntok = min(Cfg::TT, cur.L - cur.ti * Cfg::TT);
                 const bool first = (it == 0) || (cur.ti == 0);
                 if (first) {
                     const int g = p.NC == 1 ? cur.u : cur.u / p.NC;
@@ -880,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 size_t blk_base = 0;
                 if (blk_ok) {
                     blk_base = FLAT ? (size_t)e * p.slot_stride +
-                                          (size_t)cur.ti * PKV_TILE_TOKENS * p.Hk * Cfg::ROWB +
+                                          (size_t)cur.ti * Cfg::TT * p.Hk * Cfg::ROWB +
                                           head_off
                                     : (size_t)e * blk_stride + head_off;
                 }
@@ -900,7 +939,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const size_t so =
                             blk_ok ? (size_t)e * p.Hk * p.B + head_rows + 4 * tb : 0;
                         cp_async_16_n(sS + row * 4, p.ks + so, 4u * nrow);
-                        cp_async_16_n(sS + 256 + row * 4, p.vs + so, 4u * nrow);
+                        cp_async_16_n(sS + Cfg::TT * 4 + row * 4, p.vs + so, 4u * nrow);
                     }
                 }
                 // ---- q rows of the unit ride along with its first tile
@@ -927,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     meta[stage] = mt;
                     mbar_arrive(full);   // release: the record is visible with the data
                 }
-                pkv_cursor_next(cur, seq_len, p.S, p.U);
+                pkv_cursor_next(cur, seq_len, p.S, p.U, Cfg::TT);
             }
         }
         cp_async_wait_all();   // this thread's copies land before it exits
@@ -958,13 +997,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       lane);
         }
         if constexpr (QK != 0) {
-            // this warp's 16 rows of codes -> fp16, then the 16-bit tile step
-            const uint32_t cK = sbase + Cfg::OFF_CONV, cV = cK + Cfg::CONV / 2;
-            convert_rows<QK>(sK, sV, cK, cV, warp, lane);
-            __syncwarp();
+            // the tile step reads this warp's 16 rows of codes straight into registers
             const float *ksc = reinterpret_cast<const float *>(smem + stage * Cfg::STAGE +
                                                                2 * Cfg::KVB);
-            cs.tile(cK, cV, mt.ntok, warp, lane, ksc, ksc + PKV_TILE_TOKENS);
+            cs.tile(sK, sV, mt.ntok, warp, lane, ksc, ksc + Cfg::TT);
         } else {
             cs.tile(sK, sV, mt.ntok, warp, lane);
         }
@@ -972,7 +1008,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);
 
         if (mt.flags & kLast) {
-            // combine the four warps' softmax states for this segment
+            // combine the math warps' softmax states for this segment
             if (!mbar_wait(comb_empty, ((uint32_t)seg & 1u) ^ 1u, p.err)) return;
             cs.write_comb(comb_o, comb_m, comb_l, warp, lane);
             __syncwarp();
@@ -980,16 +1016,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(comb_full, (uint32_t)seg & 1u, p.err)) return;
             const int base = (cta * 2 + mt.slot) * p.GC;
             const bool whole = (mt.flags & kWhole) != 0;
-            // warp `warp` owns the elements idx = warp*32 + lane + 128k of the
-            // unit's gca x D outputs (head j = idx / D, element d = idx % D)
-            for (int idx = warp * 32 + lane; idx < mt.gca * D; idx += kConsumerWarps * 32) {
+            // warp `warp` < kMergeSlices owns the elements idx = warp*32 +
+            // lane + 128k of the unit's gca x D outputs (head j = idx / D,
+            // element d = idx % D); further math warps only feed the combine
+            const int idx0 = warp < kMergeSlices ? warp * 32 + lane : mt.gca * D;
+            for (int idx = idx0; idx < mt.gca * D; idx += kMergeSlices * 32) {
                 const int j = idx / D, d = idx - (idx / D) * D;
                 float M = -CUDART_INF_F;
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * GMAX + j]);
+                for (int w = 0; w < Cfg::CW; ++w) M = fmaxf(M, comb_m[w * GMAX + j]);
                 float Ls = 0.f, O = 0.f;
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
+                for (int w = 0; w < Cfg::CW; ++w) {
                     const float wt = exp2f(comb_m[w * GMAX + j] - M);
                     Ls = fmaf(wt, comb_l[w * GMAX + j], Ls);
                     O = fmaf(wt, comb_o[(w * GMAX + j) * D + d], O);
@@ -1004,11 +1042,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // lane 0 holds one element of every head in the slice:
                     // it writes the slice's copy of the head's lse
                     if (lane == 0)
-                        p.ws_lse[((cta * 2 + mt.slot) * kConsumerWarps + warp) * p.GC + j] =
+                        p.ws_lse[((cta * 2 + mt.slot) * kMergeSlices + warp) * p.GC + j] =
                             M + log2f(Ls);
                 }
             }
-            if (!whole && warp * 32 < mt.gca * D) pend[n_pend++] = mt;
+            if (!whole && warp < kMergeSlices && warp * 32 < mt.gca * D) pend[n_pend++] = mt;
             __syncwarp();
             if (lane == 0) mbar_arrive(comb_empty);
             ++seg;
@@ -1024,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
         fence_acq_rel_gpu();
         for (int i = 0; i < n_pend; ++i)
-            prev[i] = atomicAdd(p.ws_cnt + pkv_owner(pend[i].tu, C, NT) * kConsumerWarps + warp, 1u);
+            prev[i] = atomicAdd(p.ws_cnt + pkv_owner(pend[i].tu, C, NT) * kMergeSlices + warp, 1u);
         fence_acq_rel_gpu();
     }
     __syncwarp();
@@ -1032,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileMeta &mt = pend[i];
         const int c_first = pkv_owner(mt.tu, C, NT);
         if ((int)__shfl_sync(0xffffffffu, prev[i], 0) + 1 == pkv_unit_parts(mt.tu, mt.nu, C, NT)) {
-            if (lane == 0) p.ws_cnt[c_first * kConsumerWarps + warp] = 0u;   // for the next call
+            if (lane == 0) p.ws_cnt[c_first * kMergeSlices + warp] = 0u;   // for the next call
             merge_slice<D, GMAX>(p, mt, c_first, warp, lane, NT);
         }
     }
@@ -1066,7 +1104,7 @@ struct SplitVariant {
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)p.C);
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(Cfg::THREADS);
         cfg.dynamicSmemBytes = Cfg::smem_bytes(p.S);
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
@@ -1086,7 +1124,7 @@ struct SplitVariant {
         if (prepare(dev) != cudaSuccess) return 0;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &n, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT>, kThreads,
+                &n, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT>, Cfg::THREADS,
                 Cfg::smem_bytes(kMaxSeqsPerLaunch)) != cudaSuccess)
             return 0;
         cached[dev] = n;

@@ -52,7 +52,9 @@ PKV_HD bool pkv_cta_empty(int c, int C, int64_t NT) {
     return pkv_split(c, C, NT) == pkv_split(c + 1, C, NT);
 }
 
-PKV_HD int pkv_tiles_of_len(int L) { return (L + PKV_TILE_TOKENS - 1) / PKV_TILE_TOKENS; }
+// Tiles of a unit of L tokens; tt is the tile size (PKV_TILE_TOKENS unless a
+// kernel variant uses larger tiles).
+PKV_HD int pkv_tiles_of_len(int L, int tt = PKV_TILE_TOKENS) { return (L + tt - 1) / tt; }
 
 PKV_HD int pkv_partial_slot(int c, int C, int64_t NT, int64_t unit_start) {
     return unit_start > pkv_split(c, C, NT) ? 1 : 0;
@@ -92,10 +94,10 @@ struct PkvCursor {
 };
 
 PKV_HD void pkv_cursor_at(PkvCursor &c, int64_t tau, const int *seq_prefix, const int *seq_len,
-                          int S) {
+                          int S, int tt = PKV_TILE_TOKENS) {
     c.s = pkv_find_seq(seq_prefix, S, tau);
     c.L = seq_len[c.s];
-    c.n = pkv_tiles_of_len(c.L);
+    c.n = pkv_tiles_of_len(c.L, tt);
     const int off = (int)(tau - seq_prefix[c.s]);
     c.u = off / c.n;
     c.ti = off - c.u * c.n;
@@ -103,7 +105,8 @@ PKV_HD void pkv_cursor_at(PkvCursor &c, int64_t tau, const int *seq_prefix, cons
 
 // The next tile in flat order, skipping sequences with no tiles. Past the
 // last tile c.s becomes S and the other fields are left as they were.
-PKV_HD void pkv_cursor_next(PkvCursor &c, const int *seq_len, int S, int U) {
+PKV_HD void pkv_cursor_next(PkvCursor &c, const int *seq_len, int S, int U,
+                            int tt = PKV_TILE_TOKENS) {
     if (++c.ti < c.n) return;
     c.ti = 0;
     if (++c.u < U) return;
@@ -113,6 +116,6 @@ PKV_HD void pkv_cursor_next(PkvCursor &c, const int *seq_len, int S, int U) {
     } while (c.s < S && seq_len[c.s] == 0);
     if (c.s < S) {
         c.L = seq_len[c.s];
-        c.n = pkv_tiles_of_len(c.L);
+        c.n = pkv_tiles_of_len(c.L, tt);
     }
 }

@@ -176,9 +176,9 @@ pkv_status default_ctas(const Plan &pl, int *C) {
 // that no launch's partials ever land where a launch with more CTAs keeps its
 // counters), then [C][2][GC][D] partial outputs, then [C][2][4][GC] partial
 // log2-sum-exp2 values (one copy per math warp)
-constexpr size_t kCounterBytes = (size_t)PKV_MAX_DECODE_CTAS * pkv::kConsumerWarps * sizeof(unsigned);
+constexpr size_t kCounterBytes = (size_t)PKV_MAX_DECODE_CTAS * pkv::kMergeSlices * sizeof(unsigned);
 size_t workspace_for(int C, int GC, int D) {
-    const size_t W = pkv::kConsumerWarps;
+    const size_t W = pkv::kMergeSlices;
     return kCounterBytes + (size_t)C * 2 * GC * (D + W) * sizeof(float);
 }
 

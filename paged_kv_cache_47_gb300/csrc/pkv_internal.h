@@ -10,6 +10,7 @@
 namespace pkv {
 
 constexpr int kConsumerWarps = 4;                  // math warps of the split-K kernel
+constexpr int kMergeSlices = 4;                    // workspace slices of a cut unit's partial
 constexpr int kProducerWarps = 4;                  // gather (cp.async) warps
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
@@ -45,13 +46,13 @@ struct DecodeParams {
     float scale_log2;           // scale * log2(e)
     // Split-K workspace. A unit cut by CTA boundaries is indexed by its first
     // owner c_first (a CTA starts at most one unit that runs past its range).
-    // Math warp w of each CTA holding a partial owns a fixed slice of the
-    // unit's (head, d) elements: it writes that slice, then counts itself in
-    // ws_cnt[c_first][w]; the warp that arrives last merges the slice over
-    // all partials and puts the counter back to zero.
-    unsigned *ws_cnt;           // [C][kConsumerWarps] arrival counters, zero between calls
+    // Math warp w < kMergeSlices of each CTA holding a partial owns a fixed
+    // slice of the unit's (head, d) elements: it writes that slice, then
+    // counts itself in ws_cnt[c_first][w]; the warp that arrives last merges
+    // the slice over all partials and puts the counter back to zero.
+    unsigned *ws_cnt;           // [C][kMergeSlices] arrival counters, zero between calls
     float *ws_o;                // [C][2][GC][D] partial outputs (normalised)
-    float *ws_lse;              // [C][2][kConsumerWarps][GC] partial log2-sum-exp2, one
+    float *ws_lse;              // [C][2][kMergeSlices][GC] partial log2-sum-exp2, one
                                 //                copy per owning warp
     int C;                      // CTAs of the split-K launch
     unsigned *err;              // device error word

@@ -8,7 +8,8 @@
 //   * every tile belongs to exactly one CTA and pkv_owner inverts pkv_split,
 //   * each CTA writes at most one partial per slot,
 //   * the producer's cursor (pkv_cursor_at / pkv_cursor_next) names the
-//     right sequence, unit and tile at every step of a CTA's walk,
+//     right sequence, unit and tile at every step of a CTA's walk, for
+//     64-token and 128-token tiles,
 //   * no two cut units share a counter, pkv_unit_parts equals the number of
 //     CTAs that touch the unit, and every counter ends back at zero,
 //   * every unit is finished exactly once: either whole by one CTA, or merged
@@ -41,11 +42,14 @@ int main() {
         const int S = 1 + rng() % 40;
         const int U = 1 + rng() % 6;
         const int C = 1 + rng() % 200;
+        const int tt = (trial & 1) ? 128 : 64;
         std::vector<int> len(S), n(S), prefix(S + 1, 0);
         for (int s = 0; s < S; ++s) {
             const int kind = rng() % 6;
             len[s] = kind == 0 ? 0 : (kind == 1 ? 1 + rng() % 64 : 1 + rng() % 3000);
-            n[s] = pkv_tiles_of_len(len[s]);
+            n[s] = pkv_tiles_of_len(len[s], tt);
+            CHECK(len[s] <= (int64_t)n[s] * tt && (n[s] == 0 || len[s] > (int64_t)(n[s] - 1) * tt),
+                  "tiles of length %d", len[s]);
             prefix[s + 1] = prefix[s] + n[s] * U;
         }
         const int64_t NT = prefix[S];
@@ -91,7 +95,7 @@ int main() {
                 // the producer's cursor walks [t0, t1) in flat order (and one step
                 // past it, which the lookahead cursor takes)
                 PkvCursor cur;
-                pkv_cursor_at(cur, t0, prefix.data(), len.data(), S);
+                pkv_cursor_at(cur, t0, prefix.data(), len.data(), S, tt);
                 for (int64_t tau = t0; tau <= t1 && tau < NT; ++tau) {
                     const int s = pkv_find_seq(prefix.data(), S, tau);
                     const int off = (int)(tau - prefix[s]);
@@ -99,7 +103,7 @@ int main() {
                               cur.n == n[s] && cur.L == len[s],
                           "CTA %d: cursor (%d,%d,%d) at tile %lld", c, cur.s, cur.u, cur.ti,
                           (long long)tau);
-                    pkv_cursor_next(cur, len.data(), S, U);
+                    pkv_cursor_next(cur, len.data(), S, U, tt);
                 }
             }
         }
