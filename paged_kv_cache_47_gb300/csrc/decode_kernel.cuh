@@ -231,6 +231,21 @@ __device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t 
     }
 }
 
+// Column of element d of head h in a math warp's combine slot [GMAX][D]:
+// the tensor-core write_comb stores one element per lane and instruction,
+// and the bits of d flipped here put those 32 stores in 32 distinct banks.
+// The combine reads 32 consecutive d of one head, which the flip permutes
+// within their 32-element window (no conflict either).
+template <bool MMA, int QK>
+__device__ __forceinline__ int comb_col(int h, int d) {
+    if constexpr (!MMA)
+        return d;
+    else if constexpr (QK != 0)   // lane (g, t) stores d = 16g + 2mt (+1), head 2t (+1) + 8nt
+        return d ^ ((((d >> 5) & 3) << 2) | ((h >> 1) & 3));
+    else                          // lane (g, t) stores d = 16mt + g (+8), head 2t (+1) + 8nt
+        return d ^ (((h >> 1) & 3) << 3);
+}
+
 // ---------------------------------------------------------------------------
 // consumer state
 // ---------------------------------------------------------------------------
@@ -452,17 +467,26 @@ struct Consumer<T, D, GMAX, true, QK> {
 #pragma unroll
             for (int nt = 0; nt < NTN; ++nt) {
                 const int h = nt * 8 + h_in;
-                const T *row = reinterpret_cast<const T *>(qslot + h * D * sizeof(T));
-                // the four lanes of head h hold all D of its elements
+                // lane (g, t) holds elements 32t .. 32t + 31 of head h (word w:
+                // elements 32t + 2w, + 1); the four lanes of head h hold all D
+                static_assert(D == 128, "8-bit caches take head_dim 128");
+                uint32_t qw[16];
+                const uint4 *row4 =
+                    reinterpret_cast<const uint4 *>(qslot + h * D * sizeof(T)) + 4 * (lane & 3);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v = h < gca ? row4[c] : make_uint4(0u, 0u, 0u, 0u);
+                    qw[4 * c] = v.x;
+                    qw[4 * c + 1] = v.y;
+                    qw[4 * c + 2] = v.z;
+                    qw[4 * c + 3] = v.w;
+                }
                 float amax = 0.f;
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int d = 32 * (lane & 3) + 4 * ks + j;   // renumbered d
-                        const float x = h < gca ? Elem<T>::to_f32(row[d]) : 0.f;
-                        amax = fmaxf(amax, fabsf(x));
-                    }
+                for (int w = 0; w < 16; ++w) {
+                    const float2 x = Elem<T>::unpack2(qw[w]);
+                    amax = fmaxf(amax, fmaxf(fabsf(x.x), fabsf(x.y)));
+                }
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
                 amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
                 // amax < 2^(F+1); scaling by 2^-e, e = max(0, F - 14), keeps |q| < 2^15
@@ -473,11 +497,10 @@ struct Consumer<T, D, GMAX, true, QK> {
                 for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        // k indices {2t, 2t+1} (half 0), {2t+8, 2t+9} (half 1)
-                        const int d = 32 * (lane & 3) + 4 * ks + 2 * half;
-                        const float x0 = h < gca ? Elem<T>::to_f32(row[d]) * mul : 0.f;
-                        const float x1 = h < gca ? Elem<T>::to_f32(row[d + 1]) * mul : 0.f;
-                        __half2 q2 = __floats2half2_rn(x0, x1);
+                        // k indices {2t, 2t+1} (half 0), {2t+8, 2t+9} (half 1) stand
+                        // for elements 32t + 4ks + 2half, + 1: word 2ks + half
+                        const float2 x = Elem<T>::unpack2(qw[2 * ks + half]);
+                        __half2 q2 = __floats2half2_rn(x.x * mul, x.y * mul);
                         qb[nt][ks][half] = *reinterpret_cast<uint32_t *>(&q2);
                     }
                 // score heads of this thread: 8nt + 2(lane%4) + hh, whose shift
@@ -491,9 +514,10 @@ struct Consumer<T, D, GMAX, true, QK> {
         }
     }
 
-    // 8-bit caches: sK / sV hold codes, ksc / vsc the tile's row scales
+    // 8-bit caches: sK / sV hold codes, ksc / vsc (shared addresses) the
+    // tile's K and V row scales
     __device__ __forceinline__ void tile(uint32_t sK, uint32_t sV, int ntok, int warp, int lane,
-                                         const float *ksc = nullptr, const float *vsc = nullptr) {
+                                         uint32_t ksc = 0, uint32_t vsc = 0) {
         const int r0 = 16 * warp;
         const int nval = ntok - r0;
         if (nval <= 0) return;
@@ -514,6 +538,27 @@ struct Consumer<T, D, GMAX, true, QK> {
                 lds_u32x4(swz<TT>(sV, r0 + 2 * t + (k & 1) + 8 * (k >> 1), g), vw[k][0], vw[k][1],
                           vw[k][2], vw[k][3]);
         }
+        const int rA = r0 + g, rB = rA + 8;   // this lane's score rows (tokens)
+        const bool vA = rA < ntok, vB = rB < ntok;
+        // 8-bit caches: row scales of K (into the scores) and V (into p); the
+        // V side does not wait for the scores
+        float ksA = 1.f, ksB = 1.f, fvA = 1.f, fvB = 1.f, ratio = 1.f;
+        if constexpr (QK != 0) {
+            ksA = vA ? lds_f32(ksc + 4 * rA) : 0.f;
+            ksB = vB ? lds_f32(ksc + 4 * rB) : 0.f;
+            const float vsA = vA ? lds_f32(vsc + 4 * rA) : 0.f;
+            const float vsB = vB ? lds_f32(vsc + 4 * rB) : 0.f;
+            float vmax = fmaxf(vsA, vsB);
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
+            if (!(vmax > 0.f)) vmax = 1.f;   // all-zero V rows: p' = 0 whatever vmax is
+            const float inv = __frcp_rn(vmax);
+            fvA = vsA * inv;
+            fvB = vsB * inv;
+            ratio = sigma * inv;             // the accumulator moves from o/sigma to o/vmax
+            sigma = vmax;
+        }
         // ---- S^T = K Q^T
         float s[NTN][4];
 #pragma unroll
@@ -521,6 +566,12 @@ struct Consumer<T, D, GMAX, true, QK> {
 #pragma unroll
             for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
         if constexpr (QK != 0) {
+            // even and odd k-steps in two accumulators: two chains of KS/2 mmas
+            float s2[NTN][4];
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s2[nt][i] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a0, a1, a2, a3;
@@ -528,8 +579,13 @@ struct Consumer<T, D, GMAX, true, QK> {
                 codes_to_f16<QK>(kw[1][ks], a1, a3);   // row g + 8
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt)
-                    MmaOp<MT>::run(s[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+                    MmaOp<MT>::run((ks & 1) ? s2[nt] : s[nt], a0, a1, a2, a3, qb[nt][ks][0],
+                                   qb[nt][ks][1]);
             }
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
         } else {
             const int row = r0 + (lane & 15);
 #pragma unroll
@@ -544,24 +600,6 @@ struct Consumer<T, D, GMAX, true, QK> {
         }
 
         // ---- online softmax (tokens rA, rB; heads 8nt + 2*(lane%4) + hh)
-        const int rA = r0 + (lane >> 2), rB = rA + 8;
-        const bool vA = rA < ntok, vB = rB < ntok;
-        // 8-bit caches: row scales of K (into the scores) and V (into p)
-        float ksA = 1.f, ksB = 1.f, fvA = 1.f, fvB = 1.f, ratio = 1.f;
-        if constexpr (QK != 0) {
-            ksA = vA ? ksc[rA] : 0.f;
-            ksB = vB ? ksc[rB] : 0.f;
-            const float vsA = vA ? vsc[rA] : 0.f, vsB = vB ? vsc[rB] : 0.f;
-            float vmax = fmaxf(vsA, vsB);
-            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 4));
-            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 8));
-            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 16));
-            if (!(vmax > 0.f)) vmax = 1.f;   // all-zero V rows: p' = 0 whatever vmax is
-            fvA = vsA / vmax;
-            fvB = vsB / vmax;
-            ratio = sigma / vmax;            // the accumulator moves from o/sigma to o/vmax
-            sigma = vmax;
-        }
         float p[NTN][4];
 #pragma unroll
         for (int nt = 0; nt < NTN; ++nt) {
@@ -682,10 +720,10 @@ struct Consumer<T, D, GMAX, true, QK> {
                 const int d = QK != 0 ? 16 * (lane >> 2) + 2 * mt : mt * 16 + (lane >> 2);
                 const int dd = QK != 0 ? 1 : 8;
                 float *o = comb_o + (warp * GMAX + h) * D;
-                o[d] = acc[mt][nt][0] * sg;
-                o[D + d] = acc[mt][nt][1] * sg;
-                o[d + dd] = acc[mt][nt][2] * sg;
-                o[D + d + dd] = acc[mt][nt][3] * sg;
+                o[comb_col<true, QK>(h, d)] = acc[mt][nt][0] * sg;
+                o[D + comb_col<true, QK>(h + 1, d)] = acc[mt][nt][1] * sg;
+                o[comb_col<true, QK>(h, d + dd)] = acc[mt][nt][2] * sg;
+                o[D + comb_col<true, QK>(h + 1, d + dd)] = acc[mt][nt][3] * sg;
             }
         }
     }
@@ -998,9 +1036,8 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         }
         if constexpr (QK != 0) {
             // the tile step reads this warp's 16 rows of codes straight into registers
-            const float *ksc = reinterpret_cast<const float *>(smem + stage * Cfg::STAGE +
-                                                               2 * Cfg::KVB);
-            cs.tile(sK, sV, mt.ntok, warp, lane, ksc, ksc + Cfg::TT);
+            const uint32_t ksc = sK + 2 * Cfg::KVB;
+            cs.tile(sK, sV, mt.ntok, warp, lane, ksc, ksc + 4 * Cfg::TT);
         } else {
             cs.tile(sK, sV, mt.ntok, warp, lane);
         }
@@ -1030,7 +1067,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 for (int w = 0; w < Cfg::CW; ++w) {
                     const float wt = exp2f(comb_m[w * GMAX + j] - M);
                     Ls = fmaf(wt, comb_l[w * GMAX + j], Ls);
-                    O = fmaf(wt, comb_o[(w * GMAX + j) * D + d], O);
+                    O = fmaf(wt, comb_o[(w * GMAX + j) * D + comb_col<MMA, QK>(j, d)], O);
                 }
                 const float o = O / Ls;
                 if (whole) {

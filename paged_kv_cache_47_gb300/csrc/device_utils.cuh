@@ -124,6 +124,12 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // ---------------------------------------------------------------- ldmatrix / mma
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
 // one 16-byte shared-memory load (addr 16-byte aligned)
 __device__ __forceinline__ void lds_u32x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                           uint32_t &r3) {
@@ -193,6 +199,9 @@ struct Elem<float> {
 template <>
 struct Elem<__half> {
     static __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+    static __device__ __forceinline__ float2 unpack2(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    }
     static __device__ __forceinline__ uint32_t pack2(float lo, float hi, float &lo_r, float &hi_r) {
         __half2 h = __floats2half2_rn(lo, hi);
         float2 f = __half22float2(h);
@@ -205,6 +214,9 @@ struct Elem<__half> {
 template <>
 struct Elem<__nv_bfloat16> {
     static __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ float2 unpack2(uint32_t w) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+    }
     static __device__ __forceinline__ uint32_t pack2(float lo, float hi, float &lo_r, float &hi_r) {
         __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
         float2 f = __bfloat1622float2(h);
