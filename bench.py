@@ -781,47 +781,106 @@ def run_ours(args):
     return 0
 
 
+def _packed(tensors, dev):
+    """One pinned host byte buffer holding `tensors` back to back (16-byte
+    aligned), a device byte buffer of the same size, and views of the device
+    buffer with each tensor's dtype and shape: one copy moves a step's inputs."""
+    offs, n = [], 0
+    for t in tensors:
+        offs.append(n)
+        n += (t.numel() * t.element_size() + 15) // 16 * 16
+    host = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    for t, o in zip(tensors, offs):
+        b = t.numel() * t.element_size()
+        host[o:o + b].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+    dbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+    views = [dbuf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for t, o in zip(tensors, offs)]
+    return host, dbuf, views
+
+
 def run_e2e(args, st, spec, vals, copies, outs, wss, tables, lens, slots, scale, stream, dev,
             total_bytes, world):
-    pin = lambda t: t.detach().cpu().pin_memory()  # noqa: E731
-    h_q, h_kn, h_vn = pin(vals["q"]), pin(vals["k_new"]), pin(vals["v_new"])
-    h_tab, h_len, h_slot = pin(st.block_tables), pin(st.context_lens), pin(st.slot_mapping)
-    d_q, d_kn, d_vn = torch.empty_like(vals["q"]), torch.empty_like(vals["k_new"]), torch.empty_like(vals["v_new"])
-    d_tab, d_len, d_slot = torch.empty_like(tables), torch.empty_like(lens), torch.empty_like(slots)
-    h_out = torch.empty(vals["q"].shape, dtype=vals["q"].dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_tab, h_len, h_slot))
-    d2h = h_out.numel() * h_out.element_size()
+    """The step through the public API with its inputs (q, the new K/V rows,
+    slot mapping, block tables, lengths) copied from pinned host memory in one
+    transfer and its output read back to pinned host memory, every step.
+    Serial: copy in, append + decode, copy out, wait, per step. Pipelined (the
+    reported value): two steps in flight, the input and output copies each on
+    a stream of their own; step i's inputs land in one of two device buffers
+    while step i - 1 computes, and the host waits for step i - 1's output
+    before it enqueues step i + 1."""
+    inputs = [vals["q"], vals["k_new"], vals["v_new"], st.block_tables, st.context_lens,
+              st.slot_mapping]
+    h_in, d_in0, v0 = _packed(inputs, dev)
+    _, d_in1, v1 = _packed(inputs, dev)
+    sets = [v0, v1]
+    bufs = [d_in0, d_in1]
+    h_out = [torch.empty(vals["q"].shape, dtype=vals["q"].dtype).pin_memory() for _ in range(2)]
+    h2d = h_in.numel()
+    d2h = h_out[0].numel() * h_out[0].element_size()
     steps = min(args.steps, args.e2e_steps)
-
-    calls = []
-    for c, out, ws in zip(copies, outs, wss):
-        calls.append((*c.prepared(d_q, d_kn, d_vn, d_slot, d_tab, d_len, scale, out, ws), out))
-
     cow = st.cow_pairs if st.cow_pairs.numel() else None
+    # prepared calls per (input set, workload copy)
+    calls = [[(*c.prepared(v[0], v[1], v[2], v[5], v[3], v[4], scale, out, ws), out)
+              for c, out, ws in zip(copies, outs, wss)] for v in sets]
 
-    def one(i):
-        app, dec, out = calls[i % len(calls)]
-        for d, h in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_tab, h_tab), (d_len, h_len),
-                     (d_slot, h_slot)):
-            d.copy_(h, non_blocking=True)
+    def compute(i, b):
+        app, dec, out = calls[b][i % len(copies)]
         if cow is not None:
             copies[i % len(copies)].cow(cow, stream)
         app(stream)
         dec(stream)
-        h_out.copy_(out, non_blocking=True)
+        return out
+
+    def serial(i):
+        bufs[0].copy_(h_in, non_blocking=True)
+        out = compute(i, 0)
+        h_out[0].copy_(out, non_blocking=True)
         stream.synchronize()            # the step's result is on the host
 
+    in_s, out_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_dec = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def pipelined(n):
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(in_s):
+                if i >= 2:
+                    in_s.wait_event(ev_dec[b])   # step i - 2 is done with buffer b
+                bufs[b].copy_(h_in, non_blocking=True)
+                ev_in[b].record(in_s)
+            stream.wait_event(ev_in[b])
+            out = compute(i, b)
+            ev_dec[b].record(stream)
+            with torch.cuda.stream(out_s):
+                out_s.wait_event(ev_dec[b])
+                h_out[b].copy_(out, non_blocking=True)
+                ev_out[b].record(out_s)
+            if i >= 1:
+                ev_out[(i - 1) % 2].synchronize()   # step i - 1's result is on the host
+        ev_out[(n - 1) % 2].synchronize()
+
+    def timed(fn):
+        barrier(world)
+        t0 = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t0
+        return reduce_max(dt, world, dev)
+
     for i in range(3):
-        one(i)
-    barrier(world)
-    t0 = time.perf_counter()
-    for i in range(steps):
-        one(i)
-    dt = time.perf_counter() - t0
-    dt = reduce_max(dt, world, dev)
-    return {"value": round(world * total_bytes * steps / dt / 1e9, 2), "unit": UNIT,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": round(1000 * dt / steps, 4)}
+        serial(i)
+    dt_serial = timed(lambda: [serial(i) for i in range(steps)])
+    pipelined(3)
+    dt = timed(lambda: pipelined(steps))
+    gbs = lambda t: round(world * total_bytes * steps / t / 1e9, 2)  # noqa: E731
+    return {"value": gbs(dt), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": round(1000 * dt / steps, 4),
+            "mode": "pipelined: one H2D of the packed inputs and one D2H of the output per "
+                    "step, each on a copy stream of its own, two steps in flight",
+            "serial": {"value": gbs(dt_serial), "ms_per_step": round(1000 * dt_serial / steps, 4),
+                       "mode": "copy in, step, copy out, wait, one step at a time"}}
 
 
 def main():
