@@ -1056,31 +1056,95 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
             // warp `warp` < kMergeSlices owns the elements idx = warp*32 +
             // lane + 128k of the unit's gca x D outputs (head j = idx / D,
             // element d = idx % D); further math warps only feed the combine
-            const int idx0 = warp < kMergeSlices ? warp * 32 + lane : mt.gca * D;
-            for (int idx = idx0; idx < mt.gca * D; idx += kMergeSlices * 32) {
-                const int j = idx / D, d = idx - (idx / D) * D;
-                float M = -CUDART_INF_F;
+            if constexpr (MMA && D == 128) {
+                // Weights first: lane L holds the (warp w, head j) pairs P = 32s + L
+                // (P = w * GMAX + j), reduces max and sum over w with shuffles and
+                // keeps w's weight 2^(m_wj - M_j) / sum_w' 2^(m_w'j - M_j) l_w'j.
+                // Element k of this lane (idx = warp*32 + lane + 128k) is head k,
+                // d = warp*32 + lane; it needs only the CW weights of head k.
+                constexpr int NPAIR = Cfg::CW * GMAX;
+                constexpr int PPL = (NPAIR + 31) / 32;
+                static_assert(NPAIR % 32 == 0 || NPAIR < 32, "pairs fill whole warps");
+                if (warp < kMergeSlices) {
+                    float mv[PPL], lv[PPL], sw[PPL];
+                    float M = -CUDART_INF_F;
 #pragma unroll
-                for (int w = 0; w < Cfg::CW; ++w) M = fmaxf(M, comb_m[w * GMAX + j]);
-                float Ls = 0.f, O = 0.f;
+                    for (int q = 0; q < PPL; ++q) {
+                        const int P = (32 * q + lane) % NPAIR;
+                        mv[q] = comb_m[P];
+                        lv[q] = comb_l[P];
+                        M = fmaxf(M, mv[q]);
+                    }
 #pragma unroll
-                for (int w = 0; w < Cfg::CW; ++w) {
-                    const float wt = exp2f(comb_m[w * GMAX + j] - M);
-                    Ls = fmaf(wt, comb_l[w * GMAX + j], Ls);
-                    O = fmaf(wt, comb_o[(w * GMAX + j) * D + comb_col<MMA, QK>(j, d)], O);
+                    for (int o = GMAX; o < 32 && o < NPAIR; o <<= 1)
+                        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                    float Lsum = 0.f;
+#pragma unroll
+                    for (int q = 0; q < PPL; ++q) {
+                        sw[q] = exp2f(mv[q] - M);
+                        Lsum = fmaf(sw[q], lv[q], Lsum);
+                    }
+#pragma unroll
+                    for (int o = GMAX; o < 32 && o < NPAIR; o <<= 1)
+                        Lsum += __shfl_xor_sync(0xffffffffu, Lsum, o);
+                    const float inv = 1.f / Lsum;
+#pragma unroll
+                    for (int q = 0; q < PPL; ++q) sw[q] *= inv;
+                    const float lse_j = M + log2f(Lsum);   // head lane % GMAX
+                    const int d = warp * 32 + lane;
+#pragma unroll
+                    for (int k = 0; k < GMAX; ++k) {
+                        if (k >= mt.gca) break;
+                        float O = 0.f;
+#pragma unroll
+                        for (int w = 0; w < Cfg::CW; ++w) {
+                            const int P = w * GMAX + k;
+                            const float wk = __shfl_sync(0xffffffffu, sw[P >> 5], P & 31);
+                            O = fmaf(wk, comb_o[(w * GMAX + k) * D + comb_col<MMA, QK>(k, d)], O);
+                        }
+                        const float lse = __shfl_sync(0xffffffffu, lse_j, k);
+                        if (whole) {
+                            store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + k) * D + d,
+                                      p.out_dtype, O);
+                            if (p.lse_out && d == 0)
+                                p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + k] = lse;
+                        } else {
+                            p.ws_o[(size_t)(base + k) * D + d] = O;
+                            // lane 0 holds one element of every head in the slice:
+                            // it writes the slice's copy of the head's lse
+                            if (lane == 0)
+                                p.ws_lse[((cta * 2 + mt.slot) * kMergeSlices + warp) * p.GC + k] =
+                                    lse;
+                        }
+                    }
                 }
-                const float o = O / Ls;
-                if (whole) {
-                    store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype, o);
-                    if (p.lse_out && d == 0)
-                        p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + j] = M + log2f(Ls);
-                } else {
-                    p.ws_o[(size_t)(base + j) * D + d] = o;
-                    // lane 0 holds one element of every head in the slice:
-                    // it writes the slice's copy of the head's lse
-                    if (lane == 0)
-                        p.ws_lse[((cta * 2 + mt.slot) * kMergeSlices + warp) * p.GC + j] =
-                            M + log2f(Ls);
+            } else {
+                const int idx0 = warp < kMergeSlices ? warp * 32 + lane : mt.gca * D;
+                for (int idx = idx0; idx < mt.gca * D; idx += kMergeSlices * 32) {
+                    const int j = idx / D, d = idx - (idx / D) * D;
+                    float M = -CUDART_INF_F;
+    #pragma unroll
+                    for (int w = 0; w < Cfg::CW; ++w) M = fmaxf(M, comb_m[w * GMAX + j]);
+                    float Ls = 0.f, O = 0.f;
+    #pragma unroll
+                    for (int w = 0; w < Cfg::CW; ++w) {
+                        const float wt = exp2f(comb_m[w * GMAX + j] - M);
+                        Ls = fmaf(wt, comb_l[w * GMAX + j], Ls);
+                        O = fmaf(wt, comb_o[(w * GMAX + j) * D + comb_col<MMA, QK>(j, d)], O);
+                    }
+                    const float o = O / Ls;
+                    if (whole) {
+                        store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype, o);
+                        if (p.lse_out && d == 0)
+                            p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + j] = M + log2f(Ls);
+                    } else {
+                        p.ws_o[(size_t)(base + j) * D + d] = o;
+                        // lane 0 holds one element of every head in the slice:
+                        // it writes the slice's copy of the head's lse
+                        if (lane == 0)
+                            p.ws_lse[((cta * 2 + mt.slot) * kMergeSlices + warp) * p.GC + j] =
+                                M + log2f(Ls);
+                    }
                 }
             }
             if (!whole && warp < kMergeSlices && warp * 32 < mt.gca * D) pend[n_pend++] = mt;
