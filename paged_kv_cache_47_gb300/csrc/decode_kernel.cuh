@@ -587,6 +587,12 @@ struct Consumer<T, D, GMAX, true, QK> {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
         } else {
+            // even and odd k-steps in two accumulators: two chains of KS/2 mmas
+            float s2[NTN][4];
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s2[nt][i] = 0.f;
             const int row = r0 + (lane & 15);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -595,8 +601,13 @@ struct Consumer<T, D, GMAX, true, QK> {
                 ldsm_x4(swz<TT>(sK, row, chunk), a0, a1, a2, a3);
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt)
-                    MmaOp<MT>::run(s[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+                    MmaOp<MT>::run((ks & 1) ? s2[nt] : s[nt], a0, a1, a2, a3, qb[nt][ks][0],
+                                   qb[nt][ks][1]);
             }
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s[nt][i] += s2[nt][i];
         }
 
         // ---- online softmax (tokens rA, rB; heads 8nt + 2*(lane%4) + hh)
