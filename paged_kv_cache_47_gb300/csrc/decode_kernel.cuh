@@ -8,13 +8,13 @@
 //
 // How (GB300 design):
 //  * Persistent, stream-K: one CTA per SM (x occupancy) takes an equal share
-//    of the flattened (sequence, kv-head unit, 64-token tile) space
-//    (decomp.h). Whole units are written directly. A unit cut by CTA
+//    of the flattened (sequence, kv-head unit, tile) space (decomp.h); tiles
+//    are 64 tokens, 128 for the 8-bit variants with one mma n-tile. Whole units are written directly. A unit cut by CTA
 //    boundaries leaves one partial per CTA; after its last tile each math
 //    warp counts its slices of those partials in per-unit arrival counters,
 //    and the warp that completes a count merges that slice by log-sum-exp
 //    (merge_slice). No CTA ever waits for another.
-//  * Warps 4-7 are producers: they walk the CTA's tiles, read block-table
+//  * The last four warps are producers: they walk the CTA's tiles, read block-table
 //    entries a few tiles ahead, and gather each (physical block, kv head)
 //    chunk with 16-byte cp.async copies into a ring of NST shared-memory
 //    stages, written in the 128-byte-swizzled order the math warps read
@@ -24,16 +24,18 @@
 //    with the 2-8 KB chunks of a paged cache it reaches 2.2-5.5 TB/s, while
 //    16-byte loads reach 6.2-6.6 TB/s on the same random-chunk pattern.
 //    The unit's q rows ride along with its first tile.
-//  * Warps 0-3 are consumers: each takes 16 of the tile's 64 tokens and keeps
-//    its own online-softmax state (running max m, sum l, accumulator) in fp32
-//    registers, in base 2 with scale*log2(e) folded in. At the end of a
-//    segment the four warps combine their states through shared memory.
+//  * The first CW warps (4, or 8 on 128-token tiles) do the math: each takes
+//    16 of the tile's tokens and keeps its own online-softmax state (running
+//    max m, sum l, accumulator) in fp32 registers, in base 2 with
+//    scale*log2(e) folded in. At the end of a segment they combine their
+//    states through shared memory.
 //  * Math: on 16-bit data the products run on tensor cores (mma.sync
 //    m16n8k16, tokens as M, q heads as N padded to 8, fp32 accumulate; P is
 //    split into hi+lo 16-bit parts so the PV product keeps fp32-level
-//    accuracy). On fp32 data (or when forced) they run on CUDA cores with
-//    each lane owning a slice of head_dim (reduce-scatter for the dot
-//    products).
+//    accuracy). 8-bit codes go from shared memory straight into the mma
+//    fragments as exact fp16 values. On fp32 data (or when forced) they run
+//    on CUDA cores with each lane owning a slice of head_dim (reduce-scatter
+//    for the dot products).
 //  * Every mbarrier wait is bounded (device_utils.cuh); there is no
 //    __syncthreads or named barrier after the producer/consumer split.
 #pragma once

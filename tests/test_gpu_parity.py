@@ -75,7 +75,7 @@ def spec_like(i, **kw):
 
 
 # ----------------------------------------------------------------- small cases
-RAGGED = [1, 2, 15, 16, 17, 63, 64, 65, 127, 129, 300, 1000]
+RAGGED = [1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 300, 1000]
 
 
 def test_tiny_workload_full():

@@ -93,7 +93,7 @@ def assert_close(got, want, what=""):
     assert err <= TOL, f"max abs err {err:.3e} > {TOL} {what}"
 
 
-RAGGED = [1, 2, 15, 16, 17, 63, 64, 65, 127, 129, 300, 1000]
+RAGGED = [1, 2, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300, 1000]
 
 
 @pytest.mark.parametrize("kind", KINDS)
