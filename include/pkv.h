@@ -252,11 +252,11 @@ pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pa
  * Passage: identical prompt prefixes are stored once and shared by every
  * request holding them ("KV-Cache Optimization & PagedAttention for
  * Long-Context Agents", section "Key KV-Cache Optimization Principles", item
- * 3). pkv_decode_attention_prefix also reads them once per group of sharers:
- * the prefix is attended for all sharers' query heads together (up to 16
- * heads per pass of the decode kernel), each sequence's private suffix on its
- * own, and the two partial attentions are merged by log-sum-exp. The result
- * is the plain decode's, up to rounding.
+ * 3). pkv_decode_attention_prefix reads them once per 8 of the group's
+ * sharers' query heads under each kv head instead of once per sequence: the
+ * prefix is attended for the sharers' heads together, each sequence's private
+ * suffix on its own, and the two partial attentions are merged by
+ * log-sum-exp. The result is the plain decode's, up to rounding.
  */
 typedef struct {
     int32_t num_groups;

@@ -13,10 +13,12 @@
 //     out = (2^{l_P} o_P + 2^{l_S} o_S) / (2^{l_P} + 2^{l_S}),
 // l_X = log2 sum_{t in X} exp(scaled score), o_X the attention over X alone.
 // The library computes o_P for all sharers at once: their q heads are
-// gathered under each kv head into one virtual sequence whose context is the
-// prefix, so a prefix block feeds every sharer's heads (up to 16 per pass of
-// the decode kernel). o_S is an ordinary decode over each sequence's table
-// shifted past its prefix. A last kernel merges.
+// gathered under each kv head and cut into virtual sequences of
+// kPrefixHeads heads per kv head, all over the prefix, so a prefix block
+// feeds that many sharers' heads per pass of the decode kernel (the 8-head
+// variant, whose code the suffix decode also runs). o_S is an ordinary
+// decode over each sequence's table shifted past its prefix. A last kernel
+// merges.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -42,21 +44,31 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4 *__restric
     }
 }
 
-// suffix tables and lengths: table row s shifted left by shift[s] entries
+// Suffix tables and lengths: table row s shifted left by shift[s] entries.
+// Then the prefix tables of the virtual sequences: row r (Mp entries) holds
+// the first vpb[r] entries of table row vsrc[r] (a member of the group).
 __global__ void __launch_bounds__(256) suffix_tables_kernel(
     const int32_t *__restrict__ tables, const int32_t *__restrict__ lens,
     const int32_t *__restrict__ shift, int S, int M, int B, int32_t *__restrict__ suf_tables,
-    int32_t *__restrict__ suf_lens, unsigned *err) {
-    const int64_t total = (int64_t)S * M;
+    int32_t *__restrict__ suf_lens, const int32_t *__restrict__ vsrc,
+    const int32_t *__restrict__ vpb, int NV, int Mp, int32_t *__restrict__ vtab, unsigned *err) {
+    const int64_t nsuf = (int64_t)S * M;
+    const int64_t total = nsuf + (int64_t)NV * Mp;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int s = (int)(i / M), j = (int)(i - (int64_t)s * M);
-        const int sh = __ldg(shift + s);
-        suf_tables[i] = j + sh < M ? __ldg(tables + (size_t)s * M + j + sh) : -1;
-        if (j == 0) {
-            const int rest = __ldg(lens + s) - sh * B;
-            if (rest < 0) atomicOr(err, PKV_DEVERR_CONTEXT);
-            suf_lens[s] = rest < 0 ? 0 : rest;
+        if (i < nsuf) {
+            const int s = (int)(i / M), j = (int)(i - (int64_t)s * M);
+            const int sh = __ldg(shift + s);
+            suf_tables[i] = j + sh < M ? __ldg(tables + (size_t)s * M + j + sh) : -1;
+            if (j == 0) {
+                const int rest = __ldg(lens + s) - sh * B;
+                if (rest < 0) atomicOr(err, PKV_DEVERR_CONTEXT);
+                suf_lens[s] = rest < 0 ? 0 : rest;
+            }
+        } else {
+            const int64_t k = i - nsuf;
+            const int r = (int)(k / Mp), j = (int)(k - (int64_t)r * Mp);
+            vtab[k] = j < __ldg(vpb + r) ? __ldg(tables + (size_t)__ldg(vsrc + r) * M + j) : 0;
         }
     }
 }
@@ -87,6 +99,9 @@ __global__ void __launch_bounds__(256) merge_prefix_kernel(
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// q heads per kv head of one virtual prefix sequence
+constexpr int kPrefixHeads = 8;
+
 // Sizes and host-side index arrays of one prefix-aware call.
 struct PrefixPlan {
     int S, Hq, Hk, Gq, M, B, D, G;
@@ -94,11 +109,12 @@ struct PrefixPlan {
     std::vector<int32_t> qidx;                   // gathered q row -> source row
     std::vector<int32_t> pref_row;               // [S*Hq] row of o_pref, or -1
     std::vector<int32_t> shift;                  // [S] leading blocks to skip
-    std::vector<int32_t> pref_lens;              // [G] prefix tokens
     std::vector<size_t> group_row0;              // first gathered row of each group
-    int total_rows = 0, max_heads = 0;
+    std::vector<int> group_v0, group_nv;         // first virtual sequence, their number
+    std::vector<int32_t> vsrc, vpb, vlen;        // per virtual sequence: table row, blocks, tokens
+    int total_rows = 0, NV = 0, Mp = 1;
     size_t split_ws = 0, off_q = 0, off_op = 0, off_lp = 0, off_os = 0, off_ls = 0, off_tab = 0,
-           off_len = 0, off_idx = 0, bytes = 0;
+           off_vtab = 0, off_len = 0, off_idx = 0, bytes = 0;
 };
 
 pkv_status plan_prefix(const pkv_cache_desc *c, int32_t S, int32_t Hq, int32_t M,
@@ -126,35 +142,50 @@ pkv_status plan_prefix(const pkv_cache_desc *c, int32_t S, int32_t Hq, int32_t M
             return pkv::set_last_error(PKV_ERR_INVALID_ARG, "group_of_seq[%d] = %d", s, gi);
         if (gi >= 0) p.members[gi].push_back(s);
     }
-    p.pref_lens.resize(p.G);
     p.group_row0.resize(p.G);
+    p.group_v0.resize(p.G);
+    p.group_nv.resize(p.G);
     p.pref_row.assign((size_t)S * Hq, -1);
+    constexpr int KH = kPrefixHeads;
     for (int32_t gi = 0; gi < p.G; ++gi) {
         const int32_t pb = g->group_prefix_blocks[gi];
         if (pb < 1 || pb > M || p.members[gi].empty())
             return pkv::set_last_error(PKV_ERR_INVALID_ARG,
                                        "group %d: prefix of %d blocks, %zu members", gi, pb,
                                        p.members[gi].size());
-        p.pref_lens[gi] = pb * p.B;
         const int J = (int)p.members[gi].size();
-        const int heads = p.Hk * J * p.Gq;       // the group's virtual q heads
+        // The J*Gq heads under each kv head, m = j*Gq + i, go to virtual
+        // sequence m / KH, head (kh, m % KH): gathered row
+        // row0 + (v*Hk + kh)*KH + m % KH. Rows past J*Gq repeat a real
+        // head; their outputs are not read.
+        const int nv = (J * p.Gq + KH - 1) / KH;
         p.group_row0[gi] = p.total_rows;
-        for (int kh = 0; kh < p.Hk; ++kh)
-            for (int j = 0; j < J; ++j)
-                for (int i = 0; i < p.Gq; ++i) {
-                    const int s = p.members[gi][j], h = kh * p.Gq + i;
-                    const int r = p.total_rows + (kh * J + j) * p.Gq + i;
+        p.group_v0[gi] = p.NV;
+        p.group_nv[gi] = nv;
+        for (int v = 0; v < nv; ++v)
+            for (int kh = 0; kh < p.Hk; ++kh)
+                for (int i8 = 0; i8 < KH; ++i8) {
+                    const int m = v * KH + i8;
+                    const int mm = m < J * p.Gq ? m : 0;
+                    const int s = p.members[gi][mm / p.Gq], h = kh * p.Gq + mm % p.Gq;
+                    const int r = p.total_rows + (v * p.Hk + kh) * KH + i8;
                     p.qidx.push_back(s * Hq + h);
-                    p.pref_row[(size_t)s * Hq + h] = r;
+                    if (m < J * p.Gq) p.pref_row[(size_t)s * Hq + h] = r;
                 }
+        for (int v = 0; v < nv; ++v) {
+            p.vsrc.push_back(p.members[gi][0]);
+            p.vpb.push_back(pb);
+            p.vlen.push_back(pb * p.B);
+        }
+        if (pb > p.Mp) p.Mp = pb;
         for (int s : p.members[gi]) p.shift[s] = pb;
-        p.total_rows += heads;
-        if (heads > p.max_heads) p.max_heads = heads;
+        p.total_rows += nv * p.Hk * KH;
+        p.NV += nv;
     }
     // the split-K workspace serves every decode of the call (they run in
     // stream order); it leads, so a zero-filled workspace keeps its counters
     const size_t w1 = pkv_decode_workspace_bytes_ex(c, Hq, num_ctas);
-    const size_t w2 = p.G ? pkv_decode_workspace_bytes_ex(c, p.max_heads, num_ctas) : 0;
+    const size_t w2 = p.G ? pkv_decode_workspace_bytes_ex(c, p.Hk * KH, num_ctas) : 0;
     if (w1 == 0 || (p.G && w2 == 0))
         return pkv::set_last_error(PKV_ERR_INVALID_ARG, "split-K workspace query failed");
     const size_t es = c->dtype == PKV_F32 ? 4 : 2;
@@ -165,9 +196,11 @@ pkv_status plan_prefix(const pkv_cache_desc *c, int32_t S, int32_t Hq, int32_t M
     p.off_os = p.off_lp + align256((size_t)p.total_rows * 4);
     p.off_ls = p.off_os + align256((size_t)S * Hq * p.D * 4);
     p.off_tab = p.off_ls + align256((size_t)S * Hq * 4);
-    p.off_len = p.off_tab + align256((size_t)S * M * 4);
-    p.off_idx = p.off_len + align256((size_t)(S + p.G) * 4);
-    p.bytes = p.off_idx + align256((p.qidx.size() + p.pref_row.size() + S) * 4);
+    p.off_vtab = p.off_tab + align256((size_t)S * M * 4);
+    p.off_len = p.off_vtab + align256((size_t)p.NV * p.Mp * 4);
+    p.off_idx = p.off_len + align256((size_t)S * 4);
+    p.bytes = p.off_idx +
+              align256((p.qidx.size() + p.pref_row.size() + S + 3 * (size_t)p.NV) * 4);
     return PKV_OK;
 }
 
@@ -217,18 +250,23 @@ pkv_status pkv_decode_attention_prefix(const pkv_cache_desc *cache, const void *
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const size_t es = cache->dtype == PKV_F32 ? 4 : 2;
     const int S = num_seqs, Hq = num_q_heads, D = pp.D, M = max_blocks_per_seq;
-    int32_t *d_len = reinterpret_cast<int32_t *>(ws + pp.off_len);      // [S] suffix, [G] prefix
+    int32_t *d_len = reinterpret_cast<int32_t *>(ws + pp.off_len);      // [S] suffix tokens
     int32_t *d_idx = reinterpret_cast<int32_t *>(ws + pp.off_idx);
     int32_t *d_qidx = d_idx;
     int32_t *d_pref_row = d_qidx + pp.qidx.size();
     int32_t *d_shift = d_pref_row + pp.pref_row.size();
-    // index arrays and prefix lengths: staged from the host
+    int32_t *d_vsrc = d_shift + S;           // per virtual prefix sequence
+    int32_t *d_vpb = d_vsrc + pp.NV;
+    int32_t *d_vlen = d_vpb + pp.NV;
+    // index arrays and the virtual sequences' tables and lengths: staged
+    // from the host in one copy
     std::vector<int32_t> stage(pp.qidx);
     stage.insert(stage.end(), pp.pref_row.begin(), pp.pref_row.end());
     stage.insert(stage.end(), pp.shift.begin(), pp.shift.end());
+    stage.insert(stage.end(), pp.vsrc.begin(), pp.vsrc.end());
+    stage.insert(stage.end(), pp.vpb.begin(), pp.vpb.end());
+    stage.insert(stage.end(), pp.vlen.begin(), pp.vlen.end());
     cudaError_t e = cudaMemcpyAsync(d_idx, stage.data(), stage.size() * 4, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess && pp.G)
-        e = cudaMemcpyAsync(d_len + S, pp.pref_lens.data(), pp.G * 4, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess)
         return pkv::set_last_error(PKV_ERR_CUDA, "staging: %s", cudaGetErrorString(e));
     unsigned *err = nullptr;
@@ -241,8 +279,10 @@ pkv_status pkv_decode_attention_prefix(const pkv_cache_desc *cache, const void *
             static_cast<const uint4 *>(q), reinterpret_cast<uint4 *>(d_q), d_qidx, pp.total_rows,
             vpr);
     int32_t *d_tab = reinterpret_cast<int32_t *>(ws + pp.off_tab);
-    suffix_tables_kernel<<<grid_for((int64_t)S * M), 256, 0, s>>>(
-        block_tables, context_lens, d_shift, S, M, pp.B, d_tab, d_len, err);
+    int32_t *d_vtab = reinterpret_cast<int32_t *>(ws + pp.off_vtab);
+    suffix_tables_kernel<<<grid_for((int64_t)S * M + (int64_t)pp.NV * pp.Mp), 256, 0, s>>>(
+        block_tables, context_lens, d_shift, S, M, pp.B, d_tab, d_len, d_vsrc, d_vpb, pp.NV, pp.Mp,
+        d_vtab, err);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return pkv::set_last_error(PKV_ERR_CUDA, "prefix set-up launch: %s", cudaGetErrorString(e));
     float *o_pref = reinterpret_cast<float *>(ws + pp.off_op);
@@ -252,15 +292,15 @@ pkv_status pkv_decode_attention_prefix(const pkv_cache_desc *cache, const void *
     pkv_decode_options o = {};
     o.num_ctas = num_ctas;
     o.consumer = options ? options->consumer : 0;
-    // each group's prefix, once, for all its sharers' heads
+    // each group's prefix, once per kPrefixHeads of its sharers' heads
     for (int gi = 0; gi < pp.G; ++gi) {
-        const int J = (int)pp.members[gi].size();
         const size_t r0 = pp.group_row0[gi];
+        const int v0 = pp.group_v0[gi];
         o.lse_out = l_pref + r0;
-        st = pkv_decode_attention_ex(cache, d_q + r0 * D * es, 1, pp.Hk * J * pp.Gq, k_pool,
-                                     v_pool, block_tables + (size_t)pp.members[gi][0] * M, M,
-                                     d_len + S + gi, scale, o_pref + r0 * D, PKV_F32, ws,
-                                     pp.split_ws, stream, &o);
+        st = pkv_decode_attention_ex(cache, d_q + r0 * D * es, pp.group_nv[gi],
+                                     pp.Hk * kPrefixHeads, k_pool, v_pool,
+                                     d_vtab + (size_t)v0 * pp.Mp, pp.Mp, d_vlen + v0, scale,
+                                     o_pref + r0 * D, PKV_F32, ws, pp.split_ws, stream, &o);
         if (st != PKV_OK) return st;
     }
     // every sequence's private suffix
