@@ -41,7 +41,7 @@ int main() {
     for (int trial = 0; trial < 3000 && fails == 0; ++trial) {
         const int S = 1 + rng() % 40;
         const int U = 1 + rng() % 6;
-        const int C = 1 + rng() % 200;
+        int C = 1 + rng() % 200;
         const int tt = (trial & 1) ? 128 : 64;
         std::vector<int> len(S), n(S), prefix(S + 1, 0);
         for (int s = 0; s < S; ++s) {
@@ -54,6 +54,10 @@ int main() {
         }
         const int64_t NT = prefix[S];
         if (NT == 0) continue;
+        if (trial % 4 == 3) {
+            // C near NT: uneven shares, empty CTAs, the switch to the weighted split
+            C = (int)std::max<int64_t>(1, std::min<int64_t>(4096, NT / 2 + (int64_t)(rng() % (NT + 1))));
+        }
         const int units = S * U;
         std::vector<int> whole(units, 0), merged(units, 0), covered(units, 0);
         std::vector<int> slot_unit(2 * C, -1), slot_tiles(2 * C, 0);
@@ -61,6 +65,11 @@ int main() {
         std::vector<std::vector<std::pair<int, int64_t>>> arrivals(C);
         std::vector<int> counter(C, 0), counter_unit(C, -1), touching(units, 0);
 
+        // with NT >= C every CTA holds a tile (pkv_unit_parts counts on it)
+        if (NT >= C)
+            for (int c = 0; c < C; ++c)
+                CHECK(!pkv_cta_empty(c, C, NT), "CTA %d of %d empty with %lld tiles", c, C,
+                      (long long)NT);
         for (int64_t t = 0; t < NT; ++t) {
             const int c = pkv_owner(t, C, NT);
             CHECK(c >= 0 && c < C && pkv_split(c, C, NT) <= t && t < pkv_split(c + 1, C, NT),
