@@ -752,9 +752,30 @@ struct Consumer<T, D, GMAX, true, QK> {
 //     lse = log2 sum_p 2^{lse_p},   out = sum_p 2^{lse_p - lse} o_p,
 // taken in CTA order with a running maximum (one pass). Loads bypass L1: the
 // other CTAs' slices were written during this launch.
+// A cut segment waiting to be counted, with the facts of its unit's split
+// (computed when the segment ends, so that the CTA's last moments do no
+// 64-bit divisions): the CTAs c_first .. c_last holding its partials, their
+// number, and the partial slot of CTA c_first.
+struct PendSeg {
+    TileMeta mt;
+    int c_first, c_last, parts, slot_first;
+};
+
+__device__ __forceinline__ PendSeg pend_seg(const TileMeta &mt, int C, int64_t NT) {
+    PendSeg ps;
+    ps.mt = mt;
+    ps.c_first = pkv_owner(mt.tu, C, NT);
+    ps.c_last = pkv_owner((int64_t)mt.tu + mt.nu - 1, C, NT);
+    ps.parts = pkv_unit_parts(mt.tu, mt.nu, C, NT);
+    ps.slot_first = pkv_partial_slot(ps.c_first, C, NT, mt.tu);
+    return ps;
+}
+
 template <int D, int GMAX>
-__device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMeta &mt,
-                                            int c_first, int warp, int lane, int64_t NT) {
+__device__ __forceinline__ void merge_slice(const DecodeParams &p, const PendSeg &ps, int warp,
+                                            int lane, int64_t NT) {
+    const TileMeta &mt = ps.mt;
+    const int c_first = ps.c_first;
     // the lane's elements are idx = warp*32 + lane + 128k, k < EPL, taken in
     // chunks of KC: all loads of one partial for a chunk are issued before
     // any of them is used, and at most KC elements are live at a time
@@ -762,8 +783,9 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
     constexpr int KC = EPL < 8 ? EPL : 8;
     const int C = p.C;
     const int n_el = mt.gca * D;
-    const int c_last = pkv_owner((int64_t)mt.tu + mt.nu - 1, C, NT);
-    const int slot_first = pkv_partial_slot(c_first, C, NT, mt.tu);
+    const int c_last = ps.c_last;
+    const int slot_first = ps.slot_first;
+    const bool some_empty = NT < C;   // with NT >= C every CTA holds a tile
 #pragma unroll 1
     for (int k0 = 0; k0 < EPL; k0 += KC) {
         if (warp * 32 + k0 * kMergeSlices * 32 >= n_el) break;
@@ -776,7 +798,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const TileMet
         }
 #pragma unroll 2
         for (int c = c_first; c <= c_last; ++c) {
-            if (pkv_cta_empty(c, C, NT)) continue;
+            if (some_empty && pkv_cta_empty(c, C, NT)) continue;
             const int slot = c * 2 + (c == c_first ? slot_first : 0);
             // lane h < gca fetches this warp's copy of head h's lse
             const float lse_h =
@@ -1033,7 +1055,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     // last segment at most). Counting them waits until the CTA's tiles are
     // done: the fence that must come before a count would otherwise wait
     // behind the copies in flight and stall the math warps mid-run.
-    TileMeta pend[2];
+    PendSeg pend[2];
     int n_pend = 0;
     for (int it = 0; it < n_my; ++it) {
         const int stage = it % Cfg::NST;
@@ -1160,7 +1182,8 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                     }
                 }
             }
-            if (!whole && warp < kMergeSlices && warp * 32 < mt.gca * D) pend[n_pend++] = mt;
+            if (!whole && warp < kMergeSlices && warp * 32 < mt.gca * D)
+                pend[n_pend++] = pend_seg(mt, C, NT);
             __syncwarp();
             if (lane == 0) mbar_arrive(comb_empty);
             ++seg;
@@ -1176,16 +1199,15 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     if (lane == 0) {
         fence_acq_rel_gpu();
         for (int i = 0; i < n_pend; ++i)
-            prev[i] = atomicAdd(p.ws_cnt + pkv_owner(pend[i].tu, C, NT) * kMergeSlices + warp, 1u);
+            prev[i] = atomicAdd(p.ws_cnt + pend[i].c_first * kMergeSlices + warp, 1u);
         fence_acq_rel_gpu();
     }
     __syncwarp();
     for (int i = 0; i < n_pend; ++i) {
-        const TileMeta &mt = pend[i];
-        const int c_first = pkv_owner(mt.tu, C, NT);
-        if ((int)__shfl_sync(0xffffffffu, prev[i], 0) + 1 == pkv_unit_parts(mt.tu, mt.nu, C, NT)) {
-            if (lane == 0) p.ws_cnt[c_first * kMergeSlices + warp] = 0u;   // for the next call
-            merge_slice<D, GMAX>(p, mt, c_first, warp, lane, NT);
+        const PendSeg &ps = pend[i];
+        if ((int)__shfl_sync(0xffffffffu, prev[i], 0) + 1 == ps.parts) {
+            if (lane == 0) p.ws_cnt[ps.c_first * kMergeSlices + warp] = 0u;   // for the next call
+            merge_slice<D, GMAX>(p, ps, warp, lane, NT);
         }
     }
 }
