@@ -359,7 +359,9 @@ def workload_config(spec, st):
                             + f" seed 0, sum {int(st.context_lens.sum())}",
             "pool_blocks": st.num_blocks,
             "step": ("pkv_block_copy (copy-on-write) + " if st.cow_pairs.numel() else "")
-                    + "pkv_append + pkv_decode_attention (split-K with in-kernel merge)"}
+                    + "pkv_append + pkv_decode_attention (split-K with in-kernel merge; "
+                    "tables_ready: the decode reads tables and lengths while the append "
+                    "finishes)"}
 
 
 # ------------------------------------------------------------------ cache copies
@@ -375,8 +377,11 @@ class Pools16:
 
     def prepared(self, q, kn, vn, slots, tables, lens, scale, out, ws, consumer=0):
         from paged_kv_cache_47_gb300 import binding
+        # the step's tables and lengths are in place before its append runs, so
+        # the decode may read them while the append finishes (tables_ready)
         return (binding.PreparedAppend(kn, vn, slots, self.kp, self.vp),
                 binding.PreparedDecode(q, self.kp, self.vp, tables, lens, scale, out, ws,
+                                       tables_ready=True,
                                        consumer=consumer))
 
     def cow(self, pairs, stream):
@@ -419,7 +424,8 @@ class PoolsQ:
     def prepared(self, q, kn, vn, slots, tables, lens, scale, out, ws, consumer=0):
         from paged_kv_cache_47_gb300 import binding
         return (binding.PreparedAppendQuant(kn, vn, slots, self.cache),
-                binding.PreparedDecodeQuant(q, self.cache, tables, lens, scale, out, ws))
+                binding.PreparedDecodeQuant(q, self.cache, tables, lens, scale, out, ws,
+                                            tables_ready=True))
 
     def cow(self, pairs, stream):
         from paged_kv_cache_47_gb300 import binding

@@ -180,6 +180,14 @@ typedef struct {
                                 log2 sum_t exp(scale <q, k_t>) (-inf for an
                                 empty context), to merge partial attentions
                                 computed apart; NULL = not written          */
+    int32_t tables_ready;    /* 1: context_lens and block_tables (slots for flat
+                                spans) are complete before the preceding kernel
+                                on `stream` finishes, so the decode may read
+                                them while that kernel still runs (it is
+                                launched with programmatic dependent launch).
+                                q, the pools, the output and the workspace are
+                                always touched after that kernel finishes.
+                                0 (default): everything waits for it.       */
 } pkv_decode_options;
 
 /* Workspace bytes for pkv_decode_attention_ex with options->num_ctas = num_ctas

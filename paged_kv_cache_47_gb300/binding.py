@@ -38,7 +38,8 @@ class QCacheDesc(ctypes.Structure):
 
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int32), ("consumer", ctypes.c_int32),
-                ("timing_events", ctypes.c_void_p * 2), ("lse_out", ctypes.c_void_p)]
+                ("timing_events", ctypes.c_void_p * 2), ("lse_out", ctypes.c_void_p),
+                ("tables_ready", ctypes.c_int32)]
 
 
 class PrefixGroups(ctypes.Structure):
@@ -170,8 +171,11 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
                      out: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None,
                      workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
                      consumer: int = 0, timing_events: Optional[Sequence] = None,
-                     stream=None, lse_out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Paged decode attention: out[s][h] = softmax(scale q K^T) V over context_lens[s] tokens."""
+                     stream=None, lse_out: Optional[torch.Tensor] = None,
+                     tables_ready: bool = False) -> torch.Tensor:
+    """Paged decode attention: out[s][h] = softmax(scale q K^T) V over context_lens[s] tokens.
+    tables_ready: the caller promises the tables and lengths are complete before the
+    preceding kernel on the stream finishes (pkv_decode_options.tables_ready)."""
     desc = _pools(k_pool, v_pool)
     S, Hq, D = q.shape
     q = q.contiguous()
@@ -185,6 +189,7 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
     opts = DecodeOptions()
     opts.num_ctas = num_ctas
     opts.consumer = consumer
+    opts.tables_ready = int(tables_ready)
     if timing_events is not None:
         for i, ev in enumerate(timing_events):
             opts.timing_events[i] = None if ev is None else ev.cuda_event
@@ -209,7 +214,7 @@ class PreparedDecode:
 
     def __init__(self, q, k_pool, v_pool, block_tables, context_lens, scale: float,
                  out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
-                 num_ctas: int = 0, consumer: int = 0):
+                 num_ctas: int = 0, consumer: int = 0, tables_ready: bool = False):
         self._desc = _pools(k_pool, v_pool)
         for t in (q, block_tables, context_lens, out):
             if not t.is_contiguous():
@@ -223,6 +228,7 @@ class PreparedDecode:
         self._opts = DecodeOptions()
         self._opts.num_ctas = num_ctas
         self._opts.consumer = consumer
+        self._opts.tables_ready = int(tables_ready)
         self._args = (ctypes.byref(self._desc), q.data_ptr(), S, Hq, k_pool.data_ptr(),
                       v_pool.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
                       context_lens.data_ptr(), float(scale), out.data_ptr(),
@@ -361,7 +367,8 @@ class PreparedDecodeQuant:
     """pkv_decode_attention_quant with its arguments marshalled once (see PreparedDecode)."""
 
     def __init__(self, q, cache: QuantCache, block_tables, context_lens, scale: float,
-                 out: torch.Tensor, workspace: Optional[torch.Tensor] = None, num_ctas: int = 0):
+                 out: torch.Tensor, workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                 tables_ready: bool = False):
         for t in (q, block_tables, context_lens, out):
             if not t.is_contiguous():
                 raise ValueError("prepared decode needs contiguous tensors")
@@ -372,6 +379,7 @@ class PreparedDecodeQuant:
         self._keep = (q, cache, block_tables, context_lens, out, workspace)
         self._opts = DecodeOptions()
         self._opts.num_ctas = num_ctas
+        self._opts.tables_ready = int(tables_ready)
         self._args = (ctypes.byref(cache.desc), q.data_ptr(), S, Hq, *cache.pointers(),
                       block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(),
                       float(scale), out.data_ptr(), DTYPE_CODE[out.dtype], workspace.data_ptr(),

@@ -871,14 +871,22 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         mbar_init(comb_empty, Cfg::CW);
         fence_mbarrier_init();
     }
-    // inputs may come from the previous kernel on the stream (launched with
-    // programmatic serialisation): wait for it before reading any of them
-    grid_dependency_wait();
+    // Inputs may come from the previous kernel on the stream (launched with
+    // programmatic serialisation): wait for it before reading any of them.
+    // With tables_ready the lengths and tables are complete already: they
+    // are read (and the first table entries fetched) while that kernel runs,
+    // and the wait comes just before q, the pools or any output is touched.
+    if (!p.tables_ready) grid_dependency_wait();
     build_seq_arrays<FLAT, Cfg::TT>(p, seq_prefix, seq_len, cta == 0);
 
     // zero-length sequences: zeros, written by CTA s % C
+    bool waited = !p.tables_ready;
     for (int s = 0; s < p.S; ++s) {
         if (seq_len[s] == 0 && s % C == cta) {
+            if (!waited) {   // the same for the whole CTA
+                grid_dependency_wait();
+                waited = true;
+            }
             for (int i = tid; i < p.Hq * D; i += Cfg::THREADS)
                 store_out(p.out, (size_t)s * p.Hq * D + i, p.out_dtype, 0.f);
             if (p.lse_out)
@@ -933,6 +941,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 pkv_cursor_next(la, seq_len, p.S, p.U, Cfg::TT);
             }
         }
+        if (!waited) grid_dependency_wait();   // before the first q or pool byte
         // This thread's chunks sit at the same places in every tile: row of
         // the tile, swizzled shared-memory offset and byte offset inside the
         // (block, kv head) chunk of the pool, computed once.

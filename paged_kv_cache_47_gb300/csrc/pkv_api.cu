@@ -441,6 +441,7 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
                       : nullptr;
         p.ws_lse = a.ws ? p.ws_o + (size_t)C * 2 * pl.GC * a.D : nullptr;
         p.C = C;
+        p.tables_ready = a.opts ? (a.opts->tables_ready != 0) : 0;
         p.err = err;
         p.kp = a.kp;
         p.vp = a.vp;

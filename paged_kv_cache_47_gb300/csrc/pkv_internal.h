@@ -55,6 +55,8 @@ struct DecodeParams {
     float *ws_lse;              // [C][2][kMergeSlices][GC] partial log2-sum-exp2, one
                                 //                copy per owning warp
     int C;                      // CTAs of the split-K launch
+    int tables_ready;           // lengths / tables / slots may be read before the
+                                // preceding kernel on the stream finishes
     unsigned *err;              // device error word
     const void *kp, *vp;        // pools [NB][Hk][B][D] (elements, or 8-bit codes)
     const float *ks, *vs;       // 8-bit caches: row scales [NB][Hk][B]; else unused

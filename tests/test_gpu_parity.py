@@ -182,6 +182,35 @@ def test_zero_length_sequences_give_zeros():
     assert_close(got, ref, "bf16")
 
 
+@pytest.mark.parametrize("num_ctas", [0, 5])
+def test_tables_ready_matches_default(num_ctas):
+    # append -> decode steps, the decode reading tables and lengths while the
+    # append may still run (programmatic dependent launch): same bits as the
+    # default, zero-length sequences included, and equal to the oracle
+    spec = W.WorkloadSpec("t", 6, 32, 8, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=9, lengths=[0, 700, 65, 0, 1, 2048])
+    dev = "cuda"
+    scale = 1.0 / math.sqrt(128)
+    q, kn, vn = vals["q"].to(dev), vals["k_new"].to(dev), vals["v_new"].to(dev)
+    tab, lens, sl = st.block_tables.to(dev), st.context_lens.to(dev), st.slot_mapping.to(dev)
+    outs = []
+    for ready in (False, True, True, False):
+        kp, vp = vals["k_pool"].to(dev).clone(), vals["v_pool"].to(dev).clone()
+        ws = binding.alloc_workspace(kp, 32, num_ctas)
+        for _ in range(3):
+            binding.append(kn, vn, sl, kp, vp)
+            out = binding.decode_attention(q, kp, vp, tab, lens, scale, out_dtype=torch.float32,
+                                           workspace=ws, num_ctas=num_ctas, tables_ready=ready)
+        torch.cuda.synchronize()
+        assert binding.get_error() == 0
+        outs.append(out.cpu())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    _, ref, _ = run_step(st, vals, out_dtype=torch.float32, num_ctas=num_ctas)
+    assert_close(outs[1].double().numpy(), ref, "bf16")
+    assert torch.all(outs[1][0] == 0) and torch.all(outs[1][3] == 0)
+
+
 def test_native_output_is_rne_of_fp32_output():
     spec = spec_like(1, num_seqs=4)
     st, vals = W.make_workload(spec, seed=8, lengths=[3, 100, 1500, 4096])
