@@ -485,7 +485,7 @@ class PoolsFlat:
 
         def dec(stream, timing_events=None):
             fc.decode_attention(q, seq, lens, scale, out=out, workspace=ws,
-                                timing_events=timing_events, stream=stream)
+                                timing_events=timing_events, stream=stream, tables_ready=True)
         return app, dec
 
     def cow(self, pairs, stream):

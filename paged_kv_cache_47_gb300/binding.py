@@ -650,7 +650,8 @@ class FlatCache:
                          out: Optional[torch.Tensor] = None,
                          out_dtype: Optional[torch.dtype] = None,
                          workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
-                         timing_events: Optional[Sequence] = None, stream=None) -> torch.Tensor:
+                         timing_events: Optional[Sequence] = None, stream=None,
+                         tables_ready: bool = False) -> torch.Tensor:
         S, Hq, D = q.shape
         q = q.contiguous()
         sl, cl = slots.contiguous(), context_lens.contiguous()
@@ -661,6 +662,7 @@ class FlatCache:
             workspace = self.workspace(Hq, num_ctas)
         opts = DecodeOptions()
         opts.num_ctas = num_ctas
+        opts.tables_ready = int(tables_ready)
         if timing_events is not None:
             for i, ev in enumerate(timing_events):
                 opts.timing_events[i] = None if ev is None else ev.cuda_event
