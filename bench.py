@@ -26,6 +26,7 @@ rank, no collective on the data path (weak scaling).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -815,6 +816,7 @@ def run_e2e(args, st, spec, vals, copies, outs, wss, tables, lens, slots, scale,
     a stream of their own; step i's inputs land in one of two device buffers
     while step i - 1 computes, and the host waits for step i - 1's output
     before it enqueues step i + 1."""
+    from paged_kv_cache_47_gb300 import binding
     inputs = [vals["q"], vals["k_new"], vals["v_new"], st.block_tables, st.context_lens,
               st.slot_mapping]
     h_in, d_in0, v0 = _packed(inputs, dev)
@@ -845,28 +847,49 @@ def run_e2e(args, st, spec, vals, copies, outs, wss, tables, lens, slots, scale,
         stream.synchronize()            # the step's result is on the host
 
     in_s, out_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_dec = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
+    # The pipelined loop drives the copies and the cross-stream order through
+    # the CUDA runtime directly (resolved through libpkv's own dependency on
+    # it), as a C++ serving loop would: torch's per-call overhead would
+    # otherwise bound the loop on the host.
+    rt = binding.lib()
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    rt.cudaMemcpyAsync.argtypes = [vp, vp, sz, ctypes.c_int, vp]
+    rt.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(vp), ctypes.c_uint]
+    rt.cudaEventRecord.argtypes = [vp, vp]
+    rt.cudaStreamWaitEvent.argtypes = [vp, vp, ctypes.c_uint]
+    rt.cudaEventSynchronize.argtypes = [vp]
+    rt.cudaEventDestroy.argtypes = [vp]
+
+    def event():
+        e = vp()
+        if rt.cudaEventCreateWithFlags(ctypes.byref(e), 2) != 0:   # cudaEventDisableTiming
+            raise RuntimeError("cudaEventCreateWithFlags failed")
+        return e
+
+    ev_in, ev_dec, ev_out = [event(), event()], [event(), event()], [event(), event()]
+    s_comp, s_in, s_out = (vp(stream.cuda_stream), vp(in_s.cuda_stream), vp(out_s.cuda_stream))
+    h_in_p = vp(h_in.data_ptr())
+    bufs_p = [vp(b.data_ptr()) for b in bufs]
+    h_out_p = [vp(h.data_ptr()) for h in h_out]
+    outs_p = [vp(o.data_ptr()) for o in outs]
+    H2D, D2H = 1, 2
 
     def pipelined(n):
         for i in range(n):
             b = i % 2
-            with torch.cuda.stream(in_s):
-                if i >= 2:
-                    in_s.wait_event(ev_dec[b])   # step i - 2 is done with buffer b
-                bufs[b].copy_(h_in, non_blocking=True)
-                ev_in[b].record(in_s)
-            stream.wait_event(ev_in[b])
-            out = compute(i, b)
-            ev_dec[b].record(stream)
-            with torch.cuda.stream(out_s):
-                out_s.wait_event(ev_dec[b])
-                h_out[b].copy_(out, non_blocking=True)
-                ev_out[b].record(out_s)
+            if i >= 2:
+                rt.cudaStreamWaitEvent(s_in, ev_dec[b], 0)   # step i - 2 is done with buffer b
+            rt.cudaMemcpyAsync(bufs_p[b], h_in_p, h2d, H2D, s_in)
+            rt.cudaEventRecord(ev_in[b], s_in)
+            rt.cudaStreamWaitEvent(s_comp, ev_in[b], 0)
+            compute(i, b)
+            rt.cudaEventRecord(ev_dec[b], s_comp)
+            rt.cudaStreamWaitEvent(s_out, ev_dec[b], 0)
+            rt.cudaMemcpyAsync(h_out_p[b], outs_p[i % len(copies)], d2h, D2H, s_out)
+            rt.cudaEventRecord(ev_out[b], s_out)
             if i >= 1:
-                ev_out[(i - 1) % 2].synchronize()   # step i - 1's result is on the host
-        ev_out[(n - 1) % 2].synchronize()
+                rt.cudaEventSynchronize(ev_out[(i - 1) % 2])   # step i - 1's result is on the host
+        rt.cudaEventSynchronize(ev_out[(n - 1) % 2])
 
     def timed(fn):
         barrier(world)
@@ -880,11 +903,14 @@ def run_e2e(args, st, spec, vals, copies, outs, wss, tables, lens, slots, scale,
     dt_serial = timed(lambda: [serial(i) for i in range(steps)])
     pipelined(3)
     dt = timed(lambda: pipelined(steps))
+    for e in ev_in + ev_dec + ev_out:
+        rt.cudaEventDestroy(e)
     gbs = lambda t: round(world * total_bytes * steps / t / 1e9, 2)  # noqa: E731
     return {"value": gbs(dt), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(1000 * dt / steps, 4),
             "mode": "pipelined: one H2D of the packed inputs and one D2H of the output per "
-                    "step, each on a copy stream of its own, two steps in flight",
+                    "step, each on a copy stream of its own, two steps in flight; copies "
+                    "and stream order through the CUDA runtime directly",
             "serial": {"value": gbs(dt_serial), "ms_per_step": round(1000 * dt_serial / steps, 4),
                        "mode": "copy in, step, copy out, wait, one step at a time"}}
 
