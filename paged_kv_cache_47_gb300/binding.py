@@ -340,8 +340,8 @@ def decode_attention_quant(q, cache: QuantCache, block_tables, context_lens, sca
                            out_dtype: Optional[torch.dtype] = None,
                            workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
                            consumer: int = 0, timing_events: Optional[Sequence] = None,
-                           stream=None) -> torch.Tensor:
-    """Paged decode attention over an 8-bit cache."""
+                           stream=None, tables_ready: bool = False) -> torch.Tensor:
+    """Paged decode attention over an 8-bit cache (tables_ready: see decode_attention)."""
     S, Hq, D = q.shape
     q = q.contiguous()
     bt, cl = block_tables.contiguous(), context_lens.contiguous()
@@ -353,6 +353,7 @@ def decode_attention_quant(q, cache: QuantCache, block_tables, context_lens, sca
     opts = DecodeOptions()
     opts.num_ctas = num_ctas
     opts.consumer = consumer
+    opts.tables_ready = int(tables_ready)
     if timing_events is not None:
         for i, ev in enumerate(timing_events):
             opts.timing_events[i] = None if ev is None else ev.cuda_event

@@ -105,6 +105,34 @@ def test_flat_and_paged_are_bitwise_equal():
     fc.close()
 
 
+def test_flat_tables_ready_matches_default():
+    dtype, Hq, Hk, D = torch.bfloat16, 32, 8, 128
+    lens = [0, 500, 64, 1300]
+    fc, hk, hv = make_flat(dtype, len(lens), 2048, Hk, D, lens, seed=88)
+    g = torch.Generator().manual_seed(89)
+    q = torch.randn(len(lens), Hq, D, generator=g).to(dtype).cuda()
+    kn = torch.randn(len(lens), Hk, D, generator=g).to(dtype).cuda()
+    slots = torch.arange(len(lens), dtype=torch.int32, device="cuda")
+    cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    # rewrite each sequence's last row (flat append), then decode, three times
+    live = [i for i, L in enumerate(lens) if L > 0]
+    sl = torch.tensor(live, dtype=torch.int32, device="cuda")
+    pos = torch.tensor([lens[i] - 1 for i in live], dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    outs = []
+    for ready in (False, True):
+        for _ in range(3):
+            fc.append(kn[live], kn[live], sl, pos)
+            out = fc.decode_attention(q, slots, cl, scale, out_dtype=torch.float32, num_ctas=9,
+                                      tables_ready=ready)
+        torch.cuda.synchronize()
+        assert binding.get_error() == 0
+        outs.append(out.cpu())
+    assert torch.equal(outs[0], outs[1])
+    assert torch.all(outs[1][0] == 0)
+    fc.close()
+
+
 def test_flat_growth_release_and_bounds():
     dtype, Hq, Hk, D = torch.float16, 8, 2, 128
     fc, hk, hv = make_flat(dtype, 3, 20480, Hk, D, [100, 0, 0], seed=86)

@@ -192,6 +192,30 @@ def test_decode_quant_llama_workload_sampled(kind):
 
 
 @pytest.mark.parametrize("kind", KINDS)
+def test_decode_quant_tables_ready_matches_default(kind):
+    # quantizing append -> decode steps with the decode reading tables and
+    # lengths while the append may still run: the same bits as the default
+    spec = W.WorkloadSpec("q", 5, 32, 8, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=57, lengths=[0, 300, 129, 1000, 1])
+    _, gpu = build_caches(kind, st, vals)
+    dev = "cuda"
+    q, kn, vn = vals["q"].to(dev), vals["k_new"].to(dev), vals["v_new"].to(dev)
+    tab, lens, sl = st.block_tables.to(dev), st.context_lens.to(dev), st.slot_mapping.to(dev)
+    scale = 1.0 / math.sqrt(128)
+    outs = []
+    for ready in (False, True):
+        for _ in range(3):
+            binding.append_quant(kn, vn, sl, gpu)
+            out = binding.decode_attention_quant(q, gpu, tab, lens, scale, out_dtype=torch.float32,
+                                                 num_ctas=7, tables_ready=ready)
+        torch.cuda.synchronize()
+        assert binding.get_error() == 0
+        outs.append(out.cpu())
+    assert torch.equal(outs[0], outs[1])
+    assert torch.all(outs[1][0] == 0)
+
+
+@pytest.mark.parametrize("kind", KINDS)
 def test_block_copy_quant_is_byte_exact(kind):
     spec = W.WorkloadSpec("q", 3, 8, 2, 128, 16, "f16", 1.0, pool_ratio=2.0)
     st, vals = W.make_workload(spec, seed=55, lengths=[40, 17, 90])
