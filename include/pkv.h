@@ -186,8 +186,26 @@ typedef struct {
                                 them while that kernel still runs (it is
                                 launched with programmatic dependent launch).
                                 q, the pools, the output and the workspace are
-                                always touched after that kernel finishes.
+                                always touched after that kernel finishes
+                                (unless pending_tail says otherwise).
                                 0 (default): everything waits for it.       */
+    int32_t pending_tail;    /* n >= 0. n > 0 (needs tables_ready): q and every
+                                K/V row at positions below L - n of each
+                                sequence of context length L are complete
+                                before the preceding kernel on `stream`
+                                finishes; only the last n rows of a sequence
+                                (typically the token a preceding append writes)
+                                may still be written by it. The decode then
+                                gathers and attends over the earlier rows while
+                                that kernel runs, and waits for it before the
+                                first tile holding one of the last n rows and
+                                before its first store to the output or the
+                                workspace. Applies to the first 1024 sequences
+                                (one launch); a longer batch's later launches
+                                wait as with tables_ready. A caller that also
+                                rewrote other rows since the preceding kernel
+                                began (a copy-on-write block copy, say) must
+                                leave it 0. 0 (default): no early rows.      */
 } pkv_decode_options;
 
 /* Workspace bytes for pkv_decode_attention_ex with options->num_ctas = num_ctas

@@ -39,7 +39,7 @@ class QCacheDesc(ctypes.Structure):
 class DecodeOptions(ctypes.Structure):
     _fields_ = [("num_ctas", ctypes.c_int32), ("consumer", ctypes.c_int32),
                 ("timing_events", ctypes.c_void_p * 2), ("lse_out", ctypes.c_void_p),
-                ("tables_ready", ctypes.c_int32)]
+                ("tables_ready", ctypes.c_int32), ("pending_tail", ctypes.c_int32)]
 
 
 class PrefixGroups(ctypes.Structure):
@@ -172,10 +172,12 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
                      workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
                      consumer: int = 0, timing_events: Optional[Sequence] = None,
                      stream=None, lse_out: Optional[torch.Tensor] = None,
-                     tables_ready: bool = False) -> torch.Tensor:
+                     tables_ready: bool = False, pending_tail: int = 0) -> torch.Tensor:
     """Paged decode attention: out[s][h] = softmax(scale q K^T) V over context_lens[s] tokens.
     tables_ready: the caller promises the tables and lengths are complete before the
-    preceding kernel on the stream finishes (pkv_decode_options.tables_ready)."""
+    preceding kernel on the stream finishes (pkv_decode_options.tables_ready).
+    pending_tail: n > 0 promises, besides, that q and every row below the last n of
+    each sequence are complete too (pkv_decode_options.pending_tail)."""
     desc = _pools(k_pool, v_pool)
     S, Hq, D = q.shape
     q = q.contiguous()
@@ -190,6 +192,7 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
     opts.num_ctas = num_ctas
     opts.consumer = consumer
     opts.tables_ready = int(tables_ready)
+    opts.pending_tail = int(pending_tail)
     if timing_events is not None:
         for i, ev in enumerate(timing_events):
             opts.timing_events[i] = None if ev is None else ev.cuda_event
@@ -214,7 +217,8 @@ class PreparedDecode:
 
     def __init__(self, q, k_pool, v_pool, block_tables, context_lens, scale: float,
                  out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
-                 num_ctas: int = 0, consumer: int = 0, tables_ready: bool = False):
+                 num_ctas: int = 0, consumer: int = 0, tables_ready: bool = False,
+                 pending_tail: int = 0):
         self._desc = _pools(k_pool, v_pool)
         for t in (q, block_tables, context_lens, out):
             if not t.is_contiguous():
@@ -229,6 +233,7 @@ class PreparedDecode:
         self._opts.num_ctas = num_ctas
         self._opts.consumer = consumer
         self._opts.tables_ready = int(tables_ready)
+        self._opts.pending_tail = int(pending_tail)
         self._args = (ctypes.byref(self._desc), q.data_ptr(), S, Hq, k_pool.data_ptr(),
                       v_pool.data_ptr(), block_tables.data_ptr(), block_tables.shape[1],
                       context_lens.data_ptr(), float(scale), out.data_ptr(),
@@ -340,8 +345,10 @@ def decode_attention_quant(q, cache: QuantCache, block_tables, context_lens, sca
                            out_dtype: Optional[torch.dtype] = None,
                            workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
                            consumer: int = 0, timing_events: Optional[Sequence] = None,
-                           stream=None, tables_ready: bool = False) -> torch.Tensor:
-    """Paged decode attention over an 8-bit cache (tables_ready: see decode_attention)."""
+                           stream=None, tables_ready: bool = False,
+                           pending_tail: int = 0) -> torch.Tensor:
+    """Paged decode attention over an 8-bit cache (tables_ready, pending_tail: see
+    decode_attention)."""
     S, Hq, D = q.shape
     q = q.contiguous()
     bt, cl = block_tables.contiguous(), context_lens.contiguous()
@@ -354,6 +361,7 @@ def decode_attention_quant(q, cache: QuantCache, block_tables, context_lens, sca
     opts.num_ctas = num_ctas
     opts.consumer = consumer
     opts.tables_ready = int(tables_ready)
+    opts.pending_tail = int(pending_tail)
     if timing_events is not None:
         for i, ev in enumerate(timing_events):
             opts.timing_events[i] = None if ev is None else ev.cuda_event
@@ -369,7 +377,7 @@ class PreparedDecodeQuant:
 
     def __init__(self, q, cache: QuantCache, block_tables, context_lens, scale: float,
                  out: torch.Tensor, workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
-                 tables_ready: bool = False):
+                 tables_ready: bool = False, pending_tail: int = 0):
         for t in (q, block_tables, context_lens, out):
             if not t.is_contiguous():
                 raise ValueError("prepared decode needs contiguous tensors")
@@ -381,6 +389,7 @@ class PreparedDecodeQuant:
         self._opts = DecodeOptions()
         self._opts.num_ctas = num_ctas
         self._opts.tables_ready = int(tables_ready)
+        self._opts.pending_tail = int(pending_tail)
         self._args = (ctypes.byref(cache.desc), q.data_ptr(), S, Hq, *cache.pointers(),
                       block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(),
                       float(scale), out.data_ptr(), DTYPE_CODE[out.dtype], workspace.data_ptr(),
@@ -652,7 +661,7 @@ class FlatCache:
                          out_dtype: Optional[torch.dtype] = None,
                          workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
                          timing_events: Optional[Sequence] = None, stream=None,
-                         tables_ready: bool = False) -> torch.Tensor:
+                         tables_ready: bool = False, pending_tail: int = 0) -> torch.Tensor:
         S, Hq, D = q.shape
         q = q.contiguous()
         sl, cl = slots.contiguous(), context_lens.contiguous()
@@ -664,6 +673,7 @@ class FlatCache:
         opts = DecodeOptions()
         opts.num_ctas = num_ctas
         opts.tables_ready = int(tables_ready)
+        opts.pending_tail = int(pending_tail)
         if timing_events is not None:
             for i, ev in enumerate(timing_events):
                 opts.timing_events[i] = None if ev is None else ev.cuda_event

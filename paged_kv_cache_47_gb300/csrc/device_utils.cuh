@@ -113,6 +113,22 @@ __device__ __forceinline__ void cp_async_16_n(uint32_t dst, const void *src, uin
                  : "memory");
 }
 
+// L2 eviction policy for the cache_hint form below: lines read once go first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// cp_async_16 with an L2 eviction policy
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void *src, bool valid,
+                                                 uint64_t pol) {
+    const uint32_t n = valid ? 16u : 0u;
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+                 "l"(src), "r"(n), "l"(pol)
+                 : "memory");
+}
+
 // One arrival on `bar` once every cp.async this thread issued so far has
 // landed (the barrier's expected count includes this arrival).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {

@@ -397,6 +397,11 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
     if (C < 0 || C > PKV_MAX_DECODE_CTAS)
         return fail(PKV_ERR_INVALID_ARG, "num_ctas %d outside [0, %d]", C, PKV_MAX_DECODE_CTAS);
     if (C == 0 && (st = default_ctas(pl, &C)) != PKV_OK) return st;
+    const int pending_tail = a.opts ? a.opts->pending_tail : 0;
+    if (pending_tail < 0)
+        return fail(PKV_ERR_INVALID_ARG, "pending_tail %d is negative", pending_tail);
+    if (pending_tail > 0 && !a.opts->tables_ready)
+        return fail(PKV_ERR_INVALID_ARG, "pending_tail needs tables_ready");
     const size_t need = workspace_for(C, pl.GC, a.D);
     if (C > 1 && (!a.ws || a.ws_bytes < need))
         return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -442,6 +447,9 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
         p.ws_lse = a.ws ? p.ws_o + (size_t)C * 2 * pl.GC * a.D : nullptr;
         p.C = C;
         p.tables_ready = a.opts ? (a.opts->tables_ready != 0) : 0;
+        // a later launch of a long batch follows the first one on the stream,
+        // not the kernel the caller's promise is about
+        p.pending_tail = s0 == 0 ? pending_tail : 0;
         p.err = err;
         p.kp = a.kp;
         p.vp = a.vp;

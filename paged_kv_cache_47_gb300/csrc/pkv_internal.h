@@ -57,6 +57,10 @@ struct DecodeParams {
     int C;                      // CTAs of the split-K launch
     int tables_ready;           // lengths / tables / slots may be read before the
                                 // preceding kernel on the stream finishes
+    int pending_tail;           // > 0: q and the rows below L - pending_tail may be
+                                // read before it finishes too (the last
+                                // pending_tail rows of a sequence and every
+                                // store wait for it)
     unsigned *err;              // device error word
     const void *kp, *vp;        // pools [NB][Hk][B][D] (elements, or 8-bit codes)
     const float *ks, *vs;       // 8-bit caches: row scales [NB][Hk][B]; else unused

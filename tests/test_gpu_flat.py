@@ -120,15 +120,16 @@ def test_flat_tables_ready_matches_default():
     pos = torch.tensor([lens[i] - 1 for i in live], dtype=torch.int32, device="cuda")
     scale = 1.0 / math.sqrt(D)
     outs = []
-    for ready in (False, True):
+    for ready, pend in ((False, 0), (True, 0), (True, 1)):
         for _ in range(3):
             fc.append(kn[live], kn[live], sl, pos)
             out = fc.decode_attention(q, slots, cl, scale, out_dtype=torch.float32, num_ctas=9,
-                                      tables_ready=ready)
+                                      tables_ready=ready, pending_tail=pend)
         torch.cuda.synchronize()
         assert binding.get_error() == 0
         outs.append(out.cpu())
-    assert torch.equal(outs[0], outs[1])
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
     assert torch.all(outs[1][0] == 0)
     fc.close()
 

@@ -194,13 +194,16 @@ def test_tables_ready_matches_default(num_ctas):
     q, kn, vn = vals["q"].to(dev), vals["k_new"].to(dev), vals["v_new"].to(dev)
     tab, lens, sl = st.block_tables.to(dev), st.context_lens.to(dev), st.slot_mapping.to(dev)
     outs = []
-    for ready in (False, True, True, False):
+    # pending_tail n: the rows below each sequence's last n are gathered while
+    # the append may still run; the appended row (the last) waits for it
+    for ready, pend in ((False, 0), (True, 0), (True, 1), (True, 3), (True, 64), (False, 0)):
         kp, vp = vals["k_pool"].to(dev).clone(), vals["v_pool"].to(dev).clone()
         ws = binding.alloc_workspace(kp, 32, num_ctas)
         for _ in range(3):
             binding.append(kn, vn, sl, kp, vp)
             out = binding.decode_attention(q, kp, vp, tab, lens, scale, out_dtype=torch.float32,
-                                           workspace=ws, num_ctas=num_ctas, tables_ready=ready)
+                                           workspace=ws, num_ctas=num_ctas, tables_ready=ready,
+                                           pending_tail=pend)
         torch.cuda.synchronize()
         assert binding.get_error() == 0
         outs.append(out.cpu())
@@ -209,6 +212,45 @@ def test_tables_ready_matches_default(num_ctas):
     _, ref, _ = run_step(st, vals, out_dtype=torch.float32, num_ctas=num_ctas)
     assert_close(outs[1].double().numpy(), ref, "bf16")
     assert torch.all(outs[1][0] == 0) and torch.all(outs[1][3] == 0)
+
+
+def test_pending_tail_sees_the_appended_row():
+    # The appended row dominates the output (large new K along q, distinct V),
+    # so a decode that gathered it before the append landed would be far off.
+    # Each step appends into a fresh cache copy right before the decode.
+    spec = W.WorkloadSpec("t", 8, 32, 8, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=4, lengths=[1, 17, 64, 65, 300, 1000, 2049, 4096])
+    dev = "cuda"
+    scale = 1.0 / math.sqrt(128)
+    q = vals["q"].to(dev)
+    kn = (vals["q"].view(8, 8, 4, 128)[:, :, 0, :] * 4.0).to(torch.bfloat16).to(dev)
+    vn = torch.full_like(vals["v_new"], 3.0).to(dev)
+    tab, lens, sl = st.block_tables.to(dev), st.context_lens.to(dev), st.slot_mapping.to(dev)
+    vals2 = dict(vals, k_new=kn.cpu(), v_new=vn.cpu())
+    _, ref, _ = run_step(st, vals2, out_dtype=torch.float32)
+    for num_ctas in (0, 3):
+        ws = binding.alloc_workspace(vals["k_pool"].to(dev), 32, num_ctas)
+        for _ in range(4):
+            kp, vp = vals["k_pool"].to(dev), vals["v_pool"].to(dev)
+            binding.append(kn, vn, sl, kp, vp)
+            out = binding.decode_attention(q, kp, vp, tab, lens, scale, out_dtype=torch.float32,
+                                           workspace=ws, num_ctas=num_ctas, tables_ready=True,
+                                           pending_tail=1)
+            torch.cuda.synchronize()
+            assert binding.get_error() == 0
+            assert_close(out.cpu().double().numpy(), ref, "bf16")
+
+
+def test_pending_tail_is_checked():
+    spec = spec_like(1, num_seqs=2)
+    st, vals = W.make_workload(spec, seed=1)
+    dev = "cuda"
+    args = (vals["q"].to(dev), vals["k_pool"].to(dev), vals["v_pool"].to(dev),
+            st.block_tables.to(dev), st.context_lens.to(dev), 0.1)
+    with pytest.raises(binding.PkvError):
+        binding.decode_attention(*args, pending_tail=1)             # without tables_ready
+    with pytest.raises(binding.PkvError):
+        binding.decode_attention(*args, tables_ready=True, pending_tail=-1)
 
 
 def test_native_output_is_rne_of_fp32_output():

@@ -203,15 +203,19 @@ def test_decode_quant_tables_ready_matches_default(kind):
     tab, lens, sl = st.block_tables.to(dev), st.context_lens.to(dev), st.slot_mapping.to(dev)
     scale = 1.0 / math.sqrt(128)
     outs = []
-    for ready in (False, True):
+    # pending_tail 1: every row but the appended one is gathered while the
+    # append may still run
+    for ready, pend in ((False, 0), (True, 0), (True, 1)):
         for _ in range(3):
             binding.append_quant(kn, vn, sl, gpu)
             out = binding.decode_attention_quant(q, gpu, tab, lens, scale, out_dtype=torch.float32,
-                                                 num_ctas=7, tables_ready=ready)
+                                                 num_ctas=7, tables_ready=ready,
+                                                 pending_tail=pend)
         torch.cuda.synchronize()
         assert binding.get_error() == 0
         outs.append(out.cpu())
-    assert torch.equal(outs[0], outs[1])
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
     assert torch.all(outs[1][0] == 0)
 
 
