@@ -609,8 +609,10 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     # prepared calls: the C-ABI arguments are marshalled once per cache copy
     # without copy-on-write only the appended row (each sequence's last) is
-    # written by the kernel before the decode: the decode may gather the rest
-    # while the append runs (pending_tail); a block copy rewrites whole blocks
+    # written by the kernel before the decode, and the other rows of a cache
+    # copy were last written three steps before (the copies are used in turn):
+    # the decode may gather them while the append runs (pending_tail); a block
+    # copy rewrites whole blocks
     pend = 0 if cow is not None else 1
     calls = [c.prepared(vals["q"], vals["k_new"], vals["v_new"], slots, tables, lens, scale, o, w,
                         consumer=args.consumer, pending_tail=pend)

@@ -191,21 +191,30 @@ typedef struct {
                                 0 (default): everything waits for it.       */
     int32_t pending_tail;    /* n >= 0. n > 0 (needs tables_ready): q and every
                                 K/V row at positions below L - n of each
-                                sequence of context length L are complete
-                                before the preceding kernel on `stream`
-                                finishes; only the last n rows of a sequence
-                                (typically the token a preceding append writes)
-                                may still be written by it. The decode then
-                                gathers and attends over the earlier rows while
-                                that kernel runs, and waits for it before the
-                                first tile holding one of the last n rows and
-                                before its first store to the output or the
-                                workspace. Applies to the first 1024 sequences
-                                (one launch); a longer batch's later launches
-                                wait as with tables_ready. A caller that also
-                                rewrote other rows since the preceding kernel
-                                began (a copy-on-write block copy, say) must
-                                leave it 0. 0 (default): no early rows.      */
+                                sequence of context length L may be read before
+                                the preceding kernel on `stream` finishes. The
+                                caller guarantees that no kernel that may still
+                                be running writes them: not the preceding
+                                kernel, and not an earlier one either, since
+                                with programmatic launch a chain of kernels can
+                                overlap. Only the last n rows of a sequence
+                                (typically the token the preceding append
+                                writes) may be in flight. The decode gathers
+                                and attends over the earlier rows at once, and
+                                waits for the preceding kernel before the first
+                                tile holding one of the last n rows and before
+                                its first store to the output or the workspace.
+                                In a loop that appends and decodes on one cache
+                                each step, the rows of earlier steps' appends
+                                count as in flight unless those kernels have
+                                certainly completed (the steps use separate
+                                cache copies in turn, or an event or host wait
+                                separates them); a caller that rewrote other
+                                rows (a copy-on-write block copy, say) leaves
+                                it 0. Applies to the first 1024 sequences (one
+                                launch); a longer batch's later launches wait
+                                as with tables_ready. 0 (default): no early
+                                rows.                                       */
 } pkv_decode_options;
 
 /* Workspace bytes for pkv_decode_attention_ex with options->num_ctas = num_ctas

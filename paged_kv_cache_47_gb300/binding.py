@@ -176,8 +176,9 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
     """Paged decode attention: out[s][h] = softmax(scale q K^T) V over context_lens[s] tokens.
     tables_ready: the caller promises the tables and lengths are complete before the
     preceding kernel on the stream finishes (pkv_decode_options.tables_ready).
-    pending_tail: n > 0 promises, besides, that q and every row below the last n of
-    each sequence are complete too (pkv_decode_options.pending_tail)."""
+    pending_tail: n > 0 promises, besides, that no kernel that may still be running
+    writes q or any row below the last n of each sequence
+    (pkv_decode_options.pending_tail)."""
     desc = _pools(k_pool, v_pool)
     S, Hq, D = q.shape
     q = q.contiguous()
