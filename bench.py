@@ -384,7 +384,9 @@ class Pools16:
         from paged_kv_cache_47_gb300 import binding
         # the step's tables and lengths are in place before its append runs, so
         # the decode may read them while the append finishes (tables_ready)
-        return (binding.PreparedAppend(kn, vn, slots, self.kp, self.vp),
+        # the new rows and slots are step inputs no kernel writes: the append
+        # reads them before it waits for the previous step's decode
+        return (binding.PreparedAppend(kn, vn, slots, self.kp, self.vp, inputs_ready=True),
                 binding.PreparedDecode(q, self.kp, self.vp, tables, lens, scale, out, ws,
                                        tables_ready=True, pending_tail=pending_tail,
                                        consumer=consumer))
@@ -526,7 +528,7 @@ class PoolsPrefix(Pools16):
         gos, gpb = [0] * S, [self.shared_blocks]
         n = binding.prefix_workspace_bytes(self.kp, S, q.shape[1], tables.shape[1], gos, gpb)
         pws = torch.zeros(n, dtype=torch.uint8, device=q.device)
-        app = binding.PreparedAppend(kn, vn, slots, self.kp, self.vp)
+        app = binding.PreparedAppend(kn, vn, slots, self.kp, self.vp, inputs_ready=True)
         kp, vp = self.kp, self.vp
 
         def dec(stream, timing_events=None):

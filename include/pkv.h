@@ -107,6 +107,22 @@ pkv_status pkv_append(const pkv_cache_desc *cache, const void *k_new, const void
                       const int64_t *slot_mapping, int32_t num_tokens,
                       void *k_pool, void *v_pool, void *stream);
 
+/* Options of pkv_append_ex. Zero-initialise for the defaults. */
+typedef struct {
+    int32_t inputs_ready;    /* 1: no kernel that may still be running writes
+                                k_new, v_new or slot_mapping (for instance they
+                                were copied from the host before the preceding
+                                kernel was launched), so the append reads them
+                                before it waits for the preceding kernel on
+                                `stream`; the pool writes still wait for it.
+                                0 (default): everything waits.              */
+} pkv_append_options;
+
+/* pkv_append with options (NULL = defaults). Same contract. */
+pkv_status pkv_append_ex(const pkv_cache_desc *cache, const void *k_new, const void *v_new,
+                         const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,
+                         void *v_pool, void *stream, const pkv_append_options *options);
+
 /*
  * pkv_decode_workspace_bytes — bytes of workspace pkv_decode_attention needs.
  *

@@ -42,6 +42,10 @@ class DecodeOptions(ctypes.Structure):
                 ("tables_ready", ctypes.c_int32), ("pending_tail", ctypes.c_int32)]
 
 
+class AppendOptions(ctypes.Structure):
+    _fields_ = [("inputs_ready", ctypes.c_int32)]
+
+
 class PrefixGroups(ctypes.Structure):
     _fields_ = [("num_groups", ctypes.c_int32), ("group_of_seq", ctypes.c_void_p),
                 ("group_prefix_blocks", ctypes.c_void_p)]
@@ -72,6 +76,9 @@ def lib():
         dp = ctypes.POINTER(CacheDesc)
         L.pkv_append.argtypes = [dp, vp, vp, vp, i32, vp, vp, vp]
         L.pkv_append.restype = i32
+        L.pkv_append_ex.argtypes = [dp, vp, vp, vp, i32, vp, vp, vp,
+                                    ctypes.POINTER(AppendOptions)]
+        L.pkv_append_ex.restype = i32
         L.pkv_decode_workspace_bytes.argtypes = [dp, i32, i32, i32]
         L.pkv_decode_workspace_bytes.restype = sz
         L.pkv_decode_workspace_bytes_ex.argtypes = [dp, i32, i32]
@@ -143,14 +150,19 @@ def _pools(k_pool, v_pool):
     return cache_desc(k_pool)
 
 
-def append(k_new, v_new, slot_mapping, k_pool, v_pool, stream=None) -> None:
-    """Write k_new/v_new [N][Hk][D] into the pools at slot_mapping [N] (int64)."""
+def append(k_new, v_new, slot_mapping, k_pool, v_pool, stream=None,
+           inputs_ready: bool = False) -> None:
+    """Write k_new/v_new [N][Hk][D] into the pools at slot_mapping [N] (int64).
+    inputs_ready: no kernel that may still be running writes the three inputs, so
+    they are read before the wait on the preceding kernel (pkv_append_options)."""
     desc = _pools(k_pool, v_pool)
     k_new, v_new = k_new.contiguous(), v_new.contiguous()
     sm = slot_mapping.contiguous()
     assert sm.dtype == torch.int64 and k_new.dtype == k_pool.dtype
-    _check(lib().pkv_append(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(sm), sm.numel(),
-                            _ptr(k_pool), _ptr(v_pool), _stream(stream)))
+    opts = AppendOptions(int(inputs_ready))
+    _check(lib().pkv_append_ex(ctypes.byref(desc), _ptr(k_new), _ptr(v_new), _ptr(sm),
+                               sm.numel(), _ptr(k_pool), _ptr(v_pool), _stream(stream),
+                               ctypes.byref(opts)))
 
 
 def workspace_bytes(k_pool, num_q_heads: int, num_ctas: int = 0) -> int:
@@ -254,20 +266,21 @@ class PreparedDecode:
 class PreparedAppend:
     """An append call whose arguments are marshalled once (see PreparedDecode)."""
 
-    def __init__(self, k_new, v_new, slot_mapping, k_pool, v_pool):
+    def __init__(self, k_new, v_new, slot_mapping, k_pool, v_pool, inputs_ready: bool = False):
         self._desc = _pools(k_pool, v_pool)
         for t in (k_new, v_new, slot_mapping):
             if not t.is_contiguous():
                 raise ValueError("prepared append needs contiguous tensors")
         assert slot_mapping.dtype == torch.int64 and k_new.dtype == k_pool.dtype
         self._keep = (k_new, v_new, slot_mapping, k_pool, v_pool)
+        self._opts = AppendOptions(int(inputs_ready))
         self._args = (ctypes.byref(self._desc), k_new.data_ptr(), v_new.data_ptr(),
                       slot_mapping.data_ptr(), slot_mapping.numel(), k_pool.data_ptr(),
                       v_pool.data_ptr())
-        self._fn = lib().pkv_append
+        self._fn = lib().pkv_append_ex
 
     def __call__(self, stream) -> None:
-        _check(self._fn(*self._args, _stream(stream)))
+        _check(self._fn(*self._args, _stream(stream), ctypes.byref(self._opts)))
 
 
 def block_copy(pairs, k_pool, v_pool, stream=None) -> None:

@@ -25,25 +25,36 @@ __device__ __forceinline__ void append_allow_next_grid() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// grid-stride over (token, vector-in-token); vectors per token = Hk*D*es/16
+// grid-stride over (token, vector-in-token); vectors per token = Hk*D*es/16.
+// With inputs_ready each thread reads its first vector (slot, K and V) before
+// the wait on the previous kernel, so only the stores remain after it.
 __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k_new,
                                                      const uint4 *__restrict__ v_new,
                                                      const int64_t *__restrict__ slot_mapping,
                                                      int num_tokens, uint4 *__restrict__ k_pool,
                                                      uint4 *__restrict__ v_pool, int NB, int B,
                                                      int vec_per_row, int vec_per_token,
-                                                     unsigned *err) {
+                                                     int inputs_ready, unsigned *err) {
     // launched with programmatic serialisation: the previous kernel on the
     // stream must be complete before any pool byte is touched; the next one
     // (the decode) may be scheduled meanwhile
     append_allow_next_grid();
-    append_wait_prior_grid();
     const int64_t total = (int64_t)num_tokens * vec_per_token;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    int64_t slot = -1;
+    uint4 kv = {}, vv = {};
+    const bool early = inputs_ready && i < total;
+    if (early) {
+        slot = __ldg(slot_mapping + i / vec_per_token);
+        kv = __ldg(k_new + i);
+        vv = __ldg(v_new + i);
+    }
+    append_wait_prior_grid();
+    for (bool have = early; i < total; i += stride, have = false) {
         const int tok = (int)(i / vec_per_token);
         const int v = (int)(i - (int64_t)tok * vec_per_token);
-        const int64_t slot = __ldg(slot_mapping + tok);
+        if (!have) slot = __ldg(slot_mapping + tok);
         if (slot < 0) continue;
         const int64_t blk = slot / B;
         const int off = (int)(slot - blk * B);
@@ -51,18 +62,23 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
             if (v == 0) atomicOr(err, PKV_DEVERR_SLOT);
             continue;
         }
+        if (!have) {
+            kv = __ldg(k_new + i);
+            vv = __ldg(v_new + i);
+        }
         const int g = v / vec_per_row;
         const int w = v - g * vec_per_row;
         const int Hk = vec_per_token / vec_per_row;
         const int64_t dst = ((blk * Hk + g) * B + off) * (int64_t)vec_per_row + w;
-        k_pool[dst] = __ldg(k_new + i);
-        v_pool[dst] = __ldg(v_new + i);
+        k_pool[dst] = kv;
+        v_pool[dst] = vv;
     }
 }
 
 cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
                           const int64_t *slot_mapping, int num_tokens, void *k_pool, void *v_pool,
-                          int NB, int Hk, int B, int D, unsigned *err, cudaStream_t st) {
+                          int NB, int Hk, int B, int D, int inputs_ready, unsigned *err,
+                          cudaStream_t st) {
     const int es = dtype == PKV_F32 ? 4 : 2;
     const int vec_per_row = D * es / 16;
     const int vec_per_token = Hk * vec_per_row;
@@ -83,7 +99,7 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
     return cudaLaunchKernelEx(&cfg, append_kernel, static_cast<const uint4 *>(k_new),
                               static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
                               static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), NB, B,
-                              vec_per_row, vec_per_token, err);
+                              vec_per_row, vec_per_token, inputs_ready, err);
 }
 
 // blockIdx.y = pair; grid-stride over the block's 16-byte vectors.

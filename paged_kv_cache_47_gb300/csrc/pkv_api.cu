@@ -273,6 +273,13 @@ const char *pkv_last_error_message(void) { return g_msg; }
 pkv_status pkv_append(const pkv_cache_desc *cache, const void *k_new, const void *v_new,
                       const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,
                       void *v_pool, void *stream) {
+    return pkv_append_ex(cache, k_new, v_new, slot_mapping, num_tokens, k_pool, v_pool, stream,
+                         nullptr);
+}
+
+pkv_status pkv_append_ex(const pkv_cache_desc *cache, const void *k_new, const void *v_new,
+                         const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,
+                         void *v_pool, void *stream, const pkv_append_options *options) {
     pkv_status st = check_cache(cache);
     if (st != PKV_OK) return st;
     if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
@@ -286,7 +293,8 @@ pkv_status pkv_append(const pkv_cache_desc *cache, const void *k_new, const void
     if ((st = device_error_ptr(&err)) != PKV_OK) return st;
     cudaError_t e = pkv::launch_append(cache->dtype, k_new, v_new, slot_mapping, num_tokens, k_pool,
                                        v_pool, cache->num_blocks, cache->num_kv_heads,
-                                       cache->block_size, cache->head_dim, err,
+                                       cache->block_size, cache->head_dim,
+                                       options ? (options->inputs_ready != 0) : 0, err,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     return PKV_OK;

@@ -122,7 +122,8 @@ pkv_status set_last_error(pkv_status st, const char *fmt, ...);
 
 cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
                           const int64_t *slot_mapping, int num_tokens, void *k_pool, void *v_pool,
-                          int NB, int Hk, int B, int D, unsigned *err, cudaStream_t st);
+                          int NB, int Hk, int B, int D, int inputs_ready, unsigned *err,
+                          cudaStream_t st);
 
 // 8-bit caches (append_quant.cu): D = 128.
 cudaError_t launch_append_quant(int code_dtype, int act_dtype, const void *k_new,

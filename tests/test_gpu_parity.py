@@ -241,6 +241,32 @@ def test_pending_tail_sees_the_appended_row():
             assert_close(out.cpu().double().numpy(), ref, "bf16")
 
 
+def test_append_inputs_ready_matches_default():
+    # the append reading its inputs before the wait on the preceding kernel
+    # (here a decode) writes the same bytes, after that kernel's reads
+    spec = W.WorkloadSpec("t", 6, 32, 8, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=12, lengths=[5, 700, 64, 1, 2049, 300])
+    dev = "cuda"
+    scale = 1.0 / math.sqrt(128)
+    q, kn, vn = vals["q"].to(dev), vals["k_new"].to(dev), vals["v_new"].to(dev)
+    tab, lens, sl = st.block_tables.to(dev), st.context_lens.to(dev), st.slot_mapping.to(dev)
+    res = []
+    for ready in (False, True):
+        kp, vp = vals["k_pool"].to(dev), vals["v_pool"].to(dev)
+        for _ in range(3):
+            binding.append(kn, vn, sl, kp, vp, inputs_ready=ready)
+            out = binding.decode_attention(q, kp, vp, tab, lens, scale, out_dtype=torch.float32,
+                                           tables_ready=True, pending_tail=int(ready))
+        torch.cuda.synchronize()
+        assert binding.get_error() == 0
+        res.append((kp.cpu(), vp.cpu(), out.cpu()))
+    for a, b in zip(res[0], res[1]):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+    _, ref, _ = run_step(st, vals, out_dtype=torch.float32)
+    assert_close(res[1][2].double().numpy(), ref, "bf16")
+
+
 def test_pending_tail_is_checked():
     spec = spec_like(1, num_seqs=2)
     st, vals = W.make_workload(spec, seed=1)
