@@ -351,7 +351,13 @@ def run_reference(args):
     return 0
 
 
-def workload_config(spec, st):
+def workload_config(spec, st, pending=None, inputs_ready=True):
+    """The workload and the launch options of its step. pending: whether the
+    decode takes pending_tail 1 (default: the 16-bit paged step, which uses it
+    unless the step copies blocks); inputs_ready: whether the append reads its
+    inputs before its wait."""
+    if pending is None:
+        pending = not st.cow_pairs.numel()
     return {"workload": spec.name + "_decode_step", "num_seqs": spec.num_seqs,
             "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
             "head_dim": spec.head_dim, "block_size": spec.block_size, "kv_dtype": spec.dtype,
@@ -360,12 +366,14 @@ def workload_config(spec, st):
                             + f" seed 0, sum {int(st.context_lens.sum())}",
             "pool_blocks": st.num_blocks,
             "step": ("pkv_block_copy (copy-on-write) + " if st.cow_pairs.numel() else "")
-                    + "pkv_append + pkv_decode_attention (split-K with in-kernel merge; "
+                    + "pkv_append"
+                    + (" (inputs_ready: it reads its inputs before waiting on the previous "
+                       "decode)" if inputs_ready else "")
+                    + " + pkv_decode_attention (split-K with in-kernel merge; "
                     "tables_ready: the decode reads tables and lengths while the append "
                     "finishes"
-                    + ("" if st.cow_pairs.numel() else
-                       "; pending_tail 1: it also gathers every row but each sequence's "
-                       "appended one meanwhile") + ")"}
+                    + ("; pending_tail 1: it also gathers every row but each sequence's "
+                       "appended one meanwhile" if pending else "") + ")"}
 
 
 # ------------------------------------------------------------------ cache copies
@@ -735,7 +743,10 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": args.kv_quant or spec.dtype,
         "data": "synthetic (seeded N(0,1) values, random block tables)",
-        "config": {**workload_config(spec, st),
+        "config": {**workload_config(spec, st,
+                                     pending=not (cow is not None or args.kv_quant or
+                                                  args.prefix_aware),
+                                     inputs_ready=not (args.kv_quant or args.flat)),
                    **({"decode": "prefix-aware: the shared prefix decoded once for all "
                                  "sharers' heads, suffixes apart, log-sum-exp merge "
                                  "(pkv_decode_attention_prefix; 5 launches)"}
