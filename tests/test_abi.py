@@ -69,6 +69,23 @@ def test_append_rejects_bad_arguments(L):
     assert b"aligned" in L.pkv_last_error_message()
 
 
+def test_append_ex_checks_like_append(L):
+    # the options change only when the inputs are read, not what is accepted
+    opts = binding.AppendOptions(1)
+    d = _desc()
+
+    def call(desc, n=4, kn=16, kp=16, o=opts):
+        return L.pkv_append_ex(ctypes.byref(desc) if desc is not None else None, kn, 16, 16, n,
+                               kp, 16, None, ctypes.byref(o) if o is not None else None)
+    assert call(None) == -1
+    assert call(_desc(dt=7)) == -2
+    assert call(d, n=-1) == -1
+    assert call(d, n=0) == 0                       # no-op
+    assert call(d, n=0, o=None) == 0               # NULL options: the defaults
+    assert call(d, kn=None) == -1
+    assert call(d, kp=24) == -1                    # misaligned
+
+
 def _decode(L, desc, S=1, Hq=4, q=16, kp=16, vp=16, bt=16, M=4, cl=16, scale=1.0, out=16,
             odt=2, ws=16, wsb=1 << 30, opts=None):
     return L.pkv_decode_attention_ex(ctypes.byref(desc), q, S, Hq, kp, vp, bt, M, cl, scale,
