@@ -113,6 +113,13 @@ def test_decode_rejects_bad_arguments(L):
     assert _decode(L, d, S=0) == 0                         # no-op
     assert _decode(L, d, q=None) == -1
     assert _decode(L, d, q=8) == -1                        # misaligned q
+    o.num_ctas = 4
+    o.pending_tail = -1
+    assert _decode(L, d, opts=o) == -1
+    assert b"pending_tail" in L.pkv_last_error_message()
+    o.pending_tail = 1                                     # needs tables_ready
+    assert _decode(L, d, opts=o) == -1
+    assert b"tables_ready" in L.pkv_last_error_message()
 
 
 def _qdesc(nb=8, b=16, hk=2, d=128, code=binding.PKV_INT8, act=binding.PKV_BF16):
