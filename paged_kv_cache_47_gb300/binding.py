@@ -42,6 +42,48 @@ class DecodeOptions(ctypes.Structure):
                 ("tables_ready", ctypes.c_int32), ("pending_tail", ctypes.c_int32)]
 
 
+class PreparedBmStep:
+    """pkv_bm_append_batch + pkv_bm_block_tables for a fixed batch of sequences,
+    marshalled once: each call reuses the same host buffers, so what remains per
+    step is the two native calls. The returned tensors are views of those
+    buffers, overwritten by the next call."""
+
+    def __init__(self, bm, seq_ids, num_tokens, max_blocks_per_seq: int):
+        self._ids = torch.as_tensor(list(seq_ids), dtype=torch.int64).contiguous()
+        self._nt = torch.as_tensor(list(num_tokens), dtype=torch.int32).contiguous()
+        S = len(self._ids)
+        self._total = int(self._nt.sum()) if S else 0
+        self.slots = torch.empty(max(1, self._total), dtype=torch.int64)
+        self.pairs = torch.empty(max(1, S), 2, dtype=torch.int64)
+        self.tables = torch.empty(S, max_blocks_per_seq, dtype=torch.int32)
+        self.lens = torch.empty(S, dtype=torch.int32)
+        self._nc, self._nd = ctypes.c_int32(0), ctypes.c_int32(0)
+        L, h = bm._L, bm._h
+        self._bm = bm       # keeps the manager alive
+        self._append = (L.pkv_bm_append_batch,
+                        (h, self._ids.data_ptr(), self._nt.data_ptr(), S, self.slots.data_ptr(),
+                         self.pairs.data_ptr(), S, ctypes.byref(self._nc),
+                         ctypes.byref(self._nd)))
+        self._tables = (L.pkv_bm_block_tables,
+                        (h, self._ids.data_ptr(), S, max_blocks_per_seq, self.tables.data_ptr(),
+                         self.lens.data_ptr()))
+        self._slots_view = self.slots[:self._total]
+        self._no_pairs = self.pairs[:0]
+
+    def append(self):
+        """(slots, copy pairs) of the step's new tokens."""
+        fn, args = self._append
+        _bm_check(fn(*args))
+        nc = self._nc.value
+        return self._slots_view, (self.pairs[:nc] if nc else self._no_pairs)
+
+    def block_tables(self):
+        """(block_tables [S][M], context_lens [S]) of the batch."""
+        fn, args = self._tables
+        _bm_check(fn(*args))
+        return self.tables, self.lens
+
+
 class AppendOptions(ctypes.Structure):
     _fields_ = [("inputs_ready", ctypes.c_int32)]
 
@@ -554,6 +596,11 @@ class BlockManager:
                                               max_blocks_per_seq, tables.data_ptr(),
                                               lens.data_ptr()))
         return tables, lens
+
+    def prepared_step(self, seq_ids, num_tokens, max_blocks_per_seq: int) -> "PreparedBmStep":
+        """A decode step's two calls (append_batch, block_tables) for a fixed batch,
+        with their argument and output buffers made once (see PreparedBmStep)."""
+        return PreparedBmStep(self, seq_ids, num_tokens, max_blocks_per_seq)
 
     def table(self, seq: int) -> list:
         width = max(1, self.stats().num_blocks)

@@ -197,3 +197,30 @@ def test_append_batch_equals_appends_in_order():
         if failed is not None:
             break
     assert failed is not None          # the pool ran out on the way
+
+
+def test_prepared_step_equals_list_calls():
+    # two managers fed the same operations: one through the list-taking calls,
+    # one through a prepared step (buffers made once); the forked sequence
+    # makes its first append copy a shared block
+    a, b = binding.BlockManager(80, 8), binding.BlockManager(80, 8)
+    for bm in (a, b):
+        for s in range(5):
+            bm.add_sequence(s)
+            bm.append(s, 2 + 5 * s)       # sequence 1: 7 tokens, a partial block
+        bm.fork(1, 5)
+    ids, counts = [0, 1, 2, 3, 4, 5], [1, 1, 2, 0, 1, 1]
+    M = 16
+    prep = b.prepared_step(ids, counts, M)
+    for step in range(6):
+        ws, wp = a.append_batch(ids, counts)
+        gs, gp = prep.append()
+        assert gs.tolist() == ws.tolist()
+        assert gp.tolist() == wp.tolist()
+        if step == 0:
+            # sequences 1 and 5 share a partial last block: the first writer copies it
+            assert len(wp) == 1
+        wt, wl = a.block_tables(ids, M)
+        gt, gl = prep.block_tables()
+        assert gt.tolist() == wt.tolist() and gl.tolist() == wl.tolist()
+    assert [a.table(s) for s in ids] == [b.table(s) for s in ids]
