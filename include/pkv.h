@@ -196,9 +196,11 @@ typedef struct {
                                 log2 sum_t exp(scale <q, k_t>) (-inf for an
                                 empty context), to merge partial attentions
                                 computed apart; NULL = not written          */
-    int32_t tables_ready;    /* 1: context_lens and block_tables (slots for flat
-                                spans) are complete before the preceding kernel
-                                on `stream` finishes, so the decode may read
+    int32_t tables_ready;    /* 1: no kernel that may still be running writes
+                                context_lens or block_tables (slots for flat
+                                spans): they come, say, from host copies that
+                                completed before the preceding kernel on
+                                `stream` was launched. The decode then reads
                                 them while that kernel still runs (it is
                                 launched with programmatic dependent launch).
                                 q, the pools, the output and the workspace are

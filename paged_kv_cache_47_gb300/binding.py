@@ -228,8 +228,8 @@ def decode_attention(q, k_pool, v_pool, block_tables, context_lens, scale: float
                      stream=None, lse_out: Optional[torch.Tensor] = None,
                      tables_ready: bool = False, pending_tail: int = 0) -> torch.Tensor:
     """Paged decode attention: out[s][h] = softmax(scale q K^T) V over context_lens[s] tokens.
-    tables_ready: the caller promises the tables and lengths are complete before the
-    preceding kernel on the stream finishes (pkv_decode_options.tables_ready).
+    tables_ready: the caller promises that no kernel that may still be running writes the
+    tables or lengths (pkv_decode_options.tables_ready).
     pending_tail: n > 0 promises, besides, that no kernel that may still be running
     writes q or any row below the last n of each sequence
     (pkv_decode_options.pending_tail)."""
