@@ -22,7 +22,7 @@ from the pages so that a reader can check it line by line:
   prefix block is identified by a caller-given hash; a hit shares the
   registered block, a miss allocates one and registers it.
 
-Readings where the pages are silent (also listed in the design doc):
+Readings where the pages are silent:
 - Free-pool order: the most recently freed block is taken first; a fresh pool
   hands out blocks 0, 1, 2, ... A sequence's blocks are freed in table order.
 - A hash is registered only for blocks allocated for a prefix, and dropped
