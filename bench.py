@@ -49,6 +49,7 @@ from paged_kv_cache_47_gb300 import workloads as W  # noqa: E402
 WORKLOAD_INDEX = 1
 METRIC = "paged decode attention KV GB/s and seq-tokens/s; fraction of GB300 HBM peak"
 UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, nominal
 KERNEL_SOURCES = ["decode_kernel.cuh", "device_utils.cuh", "decomp.h", "pkv_internal.h"]
 PROFILE = os.path.join(ROOT, "profiles", "decode_split_kernel_llama3_8b.md")
 
@@ -74,10 +75,13 @@ def unique_kv_bytes(st, spec, row_bytes):
     return sum(rows.values()) * 2 * spec.num_kv_heads * row_bytes
 
 
-def step_bytes(st, spec, row_bytes):
+def step_bytes(st, spec, row_bytes, fused=False):
     """Algorithmic bytes of one decode step (decode + append): every context
     row of K and V in the cache, q in and out, table entries, lengths; the
-    append reads the new K/V activations and writes their cache rows."""
+    append reads the new K/V activations and writes their cache rows. With the
+    append fused into the decode (fused=True) the decode reads each new row
+    from the activations once, for the attention and the write alike, so the
+    append part is only the rows written."""
     es = torch.tensor([], dtype=W.DTYPES[spec.dtype]).element_size()
     lens = st.context_lens.long()
     S = lens.numel()
@@ -85,6 +89,8 @@ def step_bytes(st, spec, row_bytes):
     qo = S * spec.num_q_heads * spec.head_dim * es * 2
     tables = int(((lens + spec.block_size - 1) // spec.block_size).sum()) * 4
     decode = kv + qo + tables + 4 * S
+    if fused:
+        return decode, S * spec.num_kv_heads * 2 * row_bytes
     append = S * spec.num_kv_heads * 2 * (spec.head_dim * es + row_bytes) + 8 * S
     return decode, append
 
@@ -365,13 +371,23 @@ def run_reference(args):
     return 0
 
 
-def workload_config(spec, st, pending=None, inputs_ready=True):
+def workload_config(spec, st, pending=None, inputs_ready=True, fused=True):
     """The workload and the launch options of its step. pending: whether the
     decode takes pending_tail 1 (default: the 16-bit paged step, which uses it
     unless the step copies blocks); inputs_ready: whether the append reads its
-    inputs before its wait."""
+    inputs before its wait; fused: the append runs inside the decode."""
     if pending is None:
         pending = not st.cow_pairs.numel()
+    if fused:
+        step = (("pkv_block_copy (copy-on-write) + " if st.cow_pairs.numel() else "")
+                + "pkv_append_decode_attention (one launch: each sequence's new row taken "
+                "from the activations for the attention and written to its slot; split-K "
+                "with in-kernel merge; tables_ready: tables and lengths read while the "
+                "previous kernel finishes"
+                + ("; pending_tail 1: every pool row gathered at once, only the stores wait "
+                   "for the previous kernel" if pending else "") + ")")
+    else:
+        step = None
     return {"workload": spec.name + "_decode_step", "num_seqs": spec.num_seqs,
             "q_heads": spec.num_q_heads, "kv_heads": spec.num_kv_heads,
             "head_dim": spec.head_dim, "block_size": spec.block_size, "kv_dtype": spec.dtype,
@@ -379,7 +395,7 @@ def workload_config(spec, st, pending=None, inputs_ready=True):
                              if spec.shared_prefix else f"U[{spec.len_lo},{spec.len_hi}]")
                             + f" seed 0, sum {int(st.context_lens.sum())}",
             "pool_blocks": st.num_blocks,
-            "step": ("pkv_block_copy (copy-on-write) + " if st.cow_pairs.numel() else "")
+            "step": step or ("pkv_block_copy (copy-on-write) + " if st.cow_pairs.numel() else "")
                     + "pkv_append"
                     + (" (inputs_ready: it reads its inputs before waiting on the previous "
                        "decode)" if inputs_ready else "")
@@ -392,10 +408,13 @@ def workload_config(spec, st, pending=None, inputs_ready=True):
 
 # ------------------------------------------------------------------ cache copies
 class Pools16:
-    """One resident copy of a 16-bit paged cache (K and V pools)."""
+    """One resident copy of a 16-bit paged cache (K and V pools). fused: the
+    step appends inside the decode (pkv_append_decode_attention, one launch)
+    instead of a separate pkv_append before it."""
 
-    def __init__(self, kp, vp):
+    def __init__(self, kp, vp, fused=True):
         self.kp, self.vp = kp, vp
+        self.fused = fused
 
     def workspace(self, Hq):
         from paged_kv_cache_47_gb300 import binding
@@ -404,6 +423,14 @@ class Pools16:
     def prepared(self, q, kn, vn, slots, tables, lens, scale, out, ws, consumer=0,
                  pending_tail=0):
         from paged_kv_cache_47_gb300 import binding
+        if self.fused:
+            # one launch: the new rows come from kn / vn (step inputs no kernel
+            # writes, read early like q); the tables and lengths are in place
+            # before the step (tables_ready)
+            return (None, binding.PreparedAppendDecode(q, kn, vn, self.kp, self.vp, tables, lens,
+                                                       scale, out, ws, tables_ready=True,
+                                                       pending_tail=pending_tail,
+                                                       consumer=consumer))
         # the step's tables and lengths are in place before its append runs, so
         # the decode may read them while the append finishes (tables_ready)
         # the new rows and slots are step inputs no kernel writes: the append
@@ -418,7 +445,7 @@ class Pools16:
         binding.block_copy(pairs, self.kp, self.vp, stream=stream)
 
     def clone(self):
-        return Pools16(self.kp.clone(), self.vp.clone())
+        return Pools16(self.kp.clone(), self.vp.clone(), self.fused)
 
 
 class PoolsQ:
@@ -564,6 +591,107 @@ class PoolsPrefix(Pools16):
         return app, dec
 
 
+# ------------------------------------------------------------------ other workloads
+SWEEP = [(0, None), (2, None), (3, None), (4, 8), (4, 16), (4, 32)]
+TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
+
+
+def workload_sweep(args, dev, peak):
+    """Every other workload once, on one resident cache copy (each is larger
+    than L2 but the tiny one, which is launch-bound): the step period over
+    `steps` back-to-back steps, the decode kernel alone (CUDA events around
+    each launch), algorithmic and unique bytes, the fraction of the measured
+    peak, and the max-abs error of the whole output against the fp64 oracle
+    (every sequence, every head)."""
+    from oracle import oracle
+    from paged_kv_cache_47_gb300 import binding
+
+    steps = max(args.steps, 10)
+    res = []
+    for idx, B in SWEEP:
+        spec = W.SPECS[idx] if B is None else W.SPECS[idx].with_block_size(B)
+        st = W.make_structure(spec, args.seed)
+        vals = W.make_values(st, args.seed, device=dev)
+        h = {k: v.cpu() for k, v in vals.items()}      # the pre-step state, for the oracle
+        cow = st.cow_pairs if st.cow_pairs.numel() else None
+        tables, lens = st.block_tables.to(dev), st.context_lens.to(dev)
+        slots = st.slot_mapping.to(dev)
+        S, Hq, D = vals["q"].shape
+        scale = 1.0 / math.sqrt(spec.head_dim)
+        pools = Pools16(vals["k_pool"], vals["v_pool"])
+        out = torch.empty(S, Hq, D, dtype=vals["q"].dtype, device=dev)
+        ws = pools.workspace(Hq)
+        # one cache copy: each step's append rewrites the same last row, so the
+        # rows below it are never in flight (pending_tail 1) unless the step
+        # copies whole blocks
+        app, dec = pools.prepared(vals["q"], vals["k_new"], vals["v_new"], slots, tables, lens,
+                                  scale, out, ws, pending_tail=0 if cow is not None else 1)
+        stream = torch.cuda.current_stream()
+
+        def step(evs=None):
+            if cow is not None:
+                pools.cow(cow, stream)
+            if app is not None:
+                app(stream)
+            dec(stream, timing_events=evs)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        step_ms = e0.elapsed_time(e1) / steps
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for pair in evs:
+            for e in pair:
+                e.record(stream)        # materialise the handles the library records
+        torch.cuda.synchronize()
+        for pair in evs:
+            step(pair)
+        torch.cuda.synchronize()
+        if binding.get_error() != 0:
+            raise RuntimeError(f"device error word set on workload {spec.name}")
+        dec_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+        row_bytes = cache_row_bytes(spec, None)
+        decode_bytes, append_bytes = step_bytes(st, spec, row_bytes)
+        total = decode_bytes + append_bytes
+        if cow is not None:
+            total += cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * row_bytes
+        uniq = decode_bytes - (int(st.context_lens.sum()) * 2 * spec.num_kv_heads * row_bytes) \
+            + unique_kv_bytes(st, spec, row_bytes)
+        # the oracle on the same inputs: copy-on-write, append, decode of all sequences
+        t0 = time.perf_counter()
+        if cow is not None:
+            oracle.block_copy(cow, h["k_pool"], h["v_pool"])
+        oracle.append(h["k_new"], h["v_new"], st.slot_mapping, h["k_pool"], h["v_pool"])
+        ref = oracle.decode(h["q"], h["k_pool"], h["v_pool"], st.block_tables, st.context_lens,
+                            scale)
+        oracle_s = time.perf_counter() - t0
+        got = out.double().cpu().numpy()
+        err = float(abs(got - ref).max()) if got.size else 0.0
+        res.append({
+            "workload": spec.name, "block_size": spec.block_size, "kv_dtype": spec.dtype,
+            "num_seqs": S, "q_heads": Hq, "kv_heads": spec.num_kv_heads,
+            "context_tokens": int(st.context_lens.sum()),
+            "step_us": round(step_ms * 1000, 2),
+            "step_gbs": round(total / (step_ms / 1000) / 1e9, 1),
+            "decode_us": round(dec_ms * 1000, 2),
+            "algorithmic_bytes": decode_bytes, "unique_bytes": uniq,
+            "decode_frac_of_measured": round(uniq / (dec_ms / 1000) / 1e9 / peak, 4),
+            "max_abs_err_vs_oracle": err, "tol": TOL[spec.dtype],
+            "parity": "pass" if err <= TOL[spec.dtype] else "FAIL",
+            "oracle_s": round(oracle_s, 2),
+            "l2": "inputs fit in L2 (launch-bound)" if idx == 0 else "inputs > L2",
+        })
+        del vals, h, pools, out, ws, app, dec, ref
+        torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------ our arm
 def run_ours(args):
     from paged_kv_cache_47_gb300 import binding, build
@@ -616,20 +744,23 @@ def run_ours(args):
         del vals["k_pool"], vals["v_pool"]      # the rows are in the flat spans now
     else:
         base = PoolsQ.fill(args.kv_quant, st, vals, dev) if args.kv_quant else \
-            Pools16(vals["k_pool"], vals["v_pool"])
+            Pools16(vals["k_pool"], vals["v_pool"], fused=not args.separate_append)
         if args.kv_quant:
             del vals["k_pool"], vals["v_pool"]      # the activations are in the 8-bit cache now
         copies = [base] + [base.clone() for _ in range(args.copies - 1)]
     outs = [torch.empty(S, Hq, D, dtype=vals["q"].dtype, device=dev) for _ in copies]
     wss = [c.workspace(Hq) for c in copies]
     row_bytes = cache_row_bytes(spec, args.kv_quant)
-    decode_bytes, append_bytes = step_bytes(st, spec, row_bytes)
+    fused = isinstance(copies[0], Pools16) and copies[0].fused and not args.prefix_aware
+    decode_bytes, append_bytes = step_bytes(st, spec, row_bytes, fused=fused)
     total_bytes = decode_bytes + append_bytes
     if cow is not None:
         total_bytes += cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * row_bytes
     # bytes the split-K kernel must bring from HBM: shared blocks once
     hbm_decode_bytes = decode_bytes - (int(st.context_lens.sum()) * 2 * spec.num_kv_heads *
                                        row_bytes) + unique_kv_bytes(st, spec, row_bytes)
+    # the split-K kernel's own bytes: with the fused append it also writes the new rows
+    kernel_bytes = hbm_decode_bytes + (append_bytes if fused else 0)
     stream = torch.cuda.current_stream()
     # prepared calls: the C-ABI arguments are marshalled once per cache copy
     # without copy-on-write only the appended row (each sequence's last) is
@@ -651,7 +782,8 @@ def run_ours(args):
             copies[i % len(copies)].cow(cow, s)
         if aevs is not None:
             aevs[1].record(s)
-        app(s)
+        if app is not None:
+            app(s)
         if aevs is not None:
             aevs[2].record(s)
         dec(s, timing_events=evs)
@@ -662,44 +794,24 @@ def run_ours(args):
     if binding.get_error() != 0:
         raise RuntimeError("device error word set during warm-up")
 
-    # per-kernel events on a strided subset of the timed steps
-    stride = max(1, args.steps // 200)
-    kev = {}
-    for i in range(0, args.steps, stride):
-        pair = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        for e in pair:
-            e.record(stream)            # materialise the CUDA event handle
-        kev[i] = pair
-    # append and copy-on-write events on the same steps (eager launches only:
-    # torch's events are not recorded as nodes of a captured graph)
-    aev = {}
-    if args.launch == "eager":
-        for i in kev:
-            trio = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-            for e in trio:
-                e.record(stream)
-            aev[i] = trio
-    torch.cuda.synchronize()
-
     if args.launch == "graph":
         # each step replays a captured graph of the same kernel launches
-        def capture(i, evs):
+        def capture(i):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, capture_error_mode="thread_local"):
-                step(i, evs)
+                step(i)
             return g
-        plain = [capture(c, None) for c in range(len(calls))]
-        timed = {i: capture(i, kev[i]) for i in kev}
+        graphs = [capture(c) for c in range(len(calls))]
         torch.cuda.synchronize()
         for i in range(3):
-            plain[i % len(plain)].replay()
+            graphs[i % len(graphs)].replay()
         torch.cuda.synchronize()
 
         def run_step(i):
-            (timed[i] if i in timed else plain[i % len(plain)]).replay()
+            graphs[i % len(graphs)].replay()
     else:
         def run_step(i):
-            step(i, kev.get(i), aevs=aev.get(i))
+            step(i)
 
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
@@ -708,6 +820,7 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.15)
 
+    # ---- the headline: exactly the step's launches, nothing between them
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
@@ -721,31 +834,73 @@ def run_ours(args):
     wall = time.perf_counter() - wall0
     barrier(world)
     clocks = sampler.stop(epoch0, epoch0 + wall)
-
     ms = t_start.elapsed_time(t_end)
     ms_max = reduce_max(ms, world, dev)
-    split_ms = [kev[i][0].elapsed_time(kev[i][1]) for i in kev]
-    split_avg = sum(split_ms) / len(split_ms)
+    if binding.get_error() != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    # ---- per-kernel durations: a second pass over as many steps, with CUDA
+    # events on the launching stream around each kernel (events between the
+    # launches stop consecutive kernels from overlapping, which is why this
+    # pass is kept apart from the headline loop)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for evs5 in kev:
+        for e in evs5:
+            e.record(stream)            # materialise the CUDA event handle (the library
+    torch.cuda.synchronize()            # records the decode's pair itself)
+    for i in range(args.steps):
+        step(i, evs=kev[i][3:5], aevs=kev[i][0:3])
+    torch.cuda.synchronize()
+    if binding.get_error() != 0:
+        raise RuntimeError("device error word set during the per-kernel pass")
+    split_avg = sum(e[3].elapsed_time(e[4]) for e in kev) / len(kev)
     side = {}
-    if aev:
-        es = vals["q"].element_size()
-        app_ms = sum(aev[i][1].elapsed_time(aev[i][2]) for i in aev) / len(aev)
+    if not fused:
+        app_ms = sum(e[1].elapsed_time(e[2]) for e in kev) / len(kev)
         side["append"] = {"avg_us": round(app_ms * 1000, 3), "bytes": append_bytes,
                           "gbs": round(append_bytes / (app_ms / 1000) / 1e9, 2),
                           "note": "K/V rows read + written, slots read; launched alone"}
-        if cow is not None:
-            cp_ms = sum(aev[i][0].elapsed_time(aev[i][1]) for i in aev) / len(aev)
-            cp_bytes = cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * spec.head_dim * es
-            side["block_copy"] = {"avg_us": round(cp_ms * 1000, 3), "bytes": cp_bytes,
-                                  "gbs": round(cp_bytes / (cp_ms / 1000) / 1e9, 2),
-                                  "note": "whole K and V blocks read + written"}
-    if binding.get_error() != 0:
-        raise RuntimeError("device error word set during the timed region")
+    if cow is not None:
+        es = vals["q"].element_size()
+        cp_ms = sum(e[0].elapsed_time(e[1]) for e in kev) / len(kev)
+        cp_bytes = cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * spec.head_dim * es
+        side["block_copy"] = {"avg_us": round(cp_ms * 1000, 3), "bytes": cp_bytes,
+                              "gbs": round(cp_bytes / (cp_ms / 1000) / 1e9, 2),
+                              "note": "whole K and V blocks read + written"}
 
     per_step_s = ms_max / 1000.0 / args.steps
     value = job_gbs(total_bytes, args.steps, ms_max / 1000.0, world)
     seq_tok = world * int(st.context_lens.sum()) / per_step_s
     peak, peak_kind = peaks()
+
+    # ------------- roofline of the split-K kernel
+    # isolated: CUDA events around each launch (the per-kernel pass); when the
+    # step is that one kernel alone (fused append, no copy-on-write), the
+    # headline loop times back-to-back launches of it, and the average launch
+    # duration there is the loop's time over its launches
+    iso_gbs = kernel_bytes / (split_avg / 1000.0) / 1e9
+    back_to_back = fused and cow is None
+    avg_ms = ms / args.steps if back_to_back else split_avg
+    ach = kernel_bytes / (avg_ms / 1000.0) / 1e9
+    roofline = {"bound": "hbm", "kernel": "decode_split_kernel",
+                "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4),
+                "frac_of_nominal": round(ach / NOMINAL_HBM_GBS, 4),
+                "traffic": profiled_traffic() if (args.workload == WORKLOAD_INDEX and
+                                                  not args.block_size and
+                                                  not args.kv_quant and fused) else None,
+                "algorithmic_bytes_per_launch": kernel_bytes,
+                "logical_bytes_per_launch": decode_bytes + (append_bytes if fused else 0),
+                "avg_launch_ms": round(avg_ms, 5),
+                "duration": ("timed region / launches: the step is this kernel alone, launched "
+                             "back to back with programmatic dependent launch"
+                             if back_to_back else
+                             "CUDA events around each launch (per-kernel pass)"),
+                "isolated": {"avg_launch_ms": round(split_avg, 5), "achieved": round(iso_gbs, 2),
+                             "frac": round(iso_gbs / peak, 4),
+                             "note": "CUDA events around each launch, which keeps consecutive "
+                                     "launches from overlapping"},
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"}
 
     # ------------- end to end: host inputs in, result out, every step
     e2e = run_e2e(args, st, spec, vals, copies, outs, wss, tables, lens, slots, scale, stream,
@@ -760,7 +915,8 @@ def run_ours(args):
         "config": {**workload_config(spec, st,
                                      pending=not (cow is not None or args.kv_quant or
                                                   args.prefix_aware),
-                                     inputs_ready=not (args.kv_quant or args.flat)),
+                                     inputs_ready=not (args.kv_quant or args.flat),
+                                     fused=fused),
                    **({"decode": "prefix-aware: the shared prefix decoded once for all "
                                  "sharers' heads, suffixes apart, log-sum-exp merge "
                                  "(pkv_decode_attention_prefix; 5 launches)"}
@@ -781,28 +937,27 @@ def run_ours(args):
                              if args.launch == "graph" else "eager C-ABI calls"},
         "seq_tokens_per_s": round(seq_tok, 1),
         "hbm_frac_of_measured": round(value / peak / world, 4),
-        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel",
-                     "achieved": round(hbm_decode_bytes / (split_avg / 1000.0) / 1e9, 2),
-                     "peak": peak, "unit": "GB/s",
-                     "frac": round(hbm_decode_bytes / (split_avg / 1000.0) / 1e9 / peak, 4),
-                     "traffic": profiled_traffic() if (args.workload == WORKLOAD_INDEX and
-                                                       not args.block_size and
-                                                       not args.kv_quant) else None,
-                     "algorithmic_bytes_per_launch": hbm_decode_bytes,
-                     "logical_bytes_per_launch": decode_bytes,
-                     "avg_launch_ms": round(split_avg, 5),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        # the same figure against the nominal 8 TB/s of GB300 HBM3e; the 75 %
+        # decode-kernel target is judged against the measured copy peak
+        "hbm_frac_of_nominal": round(value / NOMINAL_HBM_GBS / world, 4),
+        "roofline": roofline,
         "other_kernels": side or None,
         "block_manager": time_block_manager(st, spec) if rank == 0 else None,
-        # append + decode (+ copy-on-write); the prefix-aware decode is five
-        # launches: q gather, suffix tables, prefix decode, suffix decode, merge
-        "gpu_launches": (1 + (5 if args.prefix_aware else 1) + (1 if cow is not None else 0))
-                        * args.steps,
+        # the fused step is one launch; otherwise append + decode; the
+        # prefix-aware decode is five launches: q gather, suffix tables, prefix
+        # decode, suffix decode, merge; plus the copy-on-write launch
+        "gpu_launches": ((1 if fused else 1 + (5 if args.prefix_aware else 1)) +
+                         (1 if cow is not None else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
         "host_enqueue_s": round(enqueue_s, 4),
         "e2e": e2e,
     }
+    plain = (args.workload == WORKLOAD_INDEX and not (args.block_size or args.dtype or
+                                                        args.kv_quant or args.flat or
+                                                        args.prefix_aware or args.suffix_hi))
+    if rank == 0 and plain and not args.no_workloads:
+        line["workloads"] = workload_sweep(args, dev, peak)
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import oracle
         h = host_inputs_from_generator(st, args.seed, dev, args.kv_quant)
@@ -882,7 +1037,8 @@ def run_e2e(args, st, spec, vals, copies, outs, wss, tables, lens, slots, scale,
         app, dec, out = calls[b][i % len(copies)]
         if cow is not None:
             copies[i % len(copies)].cow(cow, stream)
-        app(stream)
+        if app is not None:
+            app(stream)
         dec(stream)
         return out
 
@@ -991,6 +1147,11 @@ def main():
     ap.add_argument("--consumer", type=int, default=0,
                     help="math path: 0 auto, 1 CUDA cores, 2 tensor cores (16-bit only)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="16-bit paged step as pkv_append + pkv_decode_attention (two launches) "
+                         "instead of pkv_append_decode_attention")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads' figures in the default line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -249,6 +249,46 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
                                    void *stream, const pkv_decode_options *options);
 
 /*
+ * pkv_append_decode_attention — one decode step in one launch: append each
+ * sequence's new token, then attend over the context including it.
+ *
+ * Passages: the new token's K/V go into the next slot of the sequence's last
+ * block ("KV-Cache Optimization & PagedAttention for Long-Context Agents",
+ * section "Key KV-Cache Optimization Principles", item 1; "PagedAttention —
+ * Math + Memory Model", section "PagedAttention: blocks and the block
+ * table"), and the attention gathers the context through the block table
+ * (same section; "KV-cache paging in vLLM", section "The Attention Kernel
+ * Change").
+ *
+ * For every sequence s with L = context_lens[s] >= 1 (L counts the new
+ * token), the result equals pkv_append with slot_mapping[s] = the slot of
+ * position L - 1 (block_tables[s][(L-1)/B] * B + (L-1) % B) followed by
+ * pkv_decode_attention:
+ *   k_pool[tab[s][(L-1)/B]][g][(L-1)%B][:] = k_new[s][g][:]   (same for v)
+ *   out[s][h] = softmax over t < L of scale <q[s][h], K_t>, weighting V_t
+ * The attention reads the new rows from k_new / v_new, so the pool rows of
+ * position L - 1 are never read (the slot may hold anything before the call);
+ * the kernel writes them after its other work, byte-exact. L == 0 appends
+ * nothing and writes zeros. A block id outside the pool sets
+ * PKV_DEVERR_BLOCK_ID, reads as zeros and is not written.
+ * k_new, v_new: device [num_seqs][num_kv_heads][head_dim] in cache->dtype,
+ * 16-byte aligned. Everything else, workspace and options included, as for
+ * pkv_decode_attention_ex, with one reading of pending_tail: the newest row
+ * comes from k_new / v_new, so pending_tail n names the n newest rows of the
+ * context as possibly in flight, of which only n - 1 are pool rows
+ * (pending_tail 1: none; a loop that decodes one cache every step, each call
+ * appending the row the next call reads from the pool, gives 2), and k_new
+ * and v_new count as inputs that may be read early, like q.
+ */
+pkv_status pkv_append_decode_attention(const pkv_cache_desc *cache, const void *q,
+                                       int32_t num_seqs, int32_t num_q_heads, const void *k_new,
+                                       const void *v_new, void *k_pool, void *v_pool,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *context_lens, float scale, void *out,
+                                       int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                       void *stream, const pkv_decode_options *options);
+
+/*
  * pkv_decode_attention_static — pkv_decode_attention for callers that cannot
  * allocate device memory. The pages have no counterpart to this entry point.
  *
@@ -423,10 +463,32 @@ pkv_status pkv_block_copy_quant(const pkv_qcache_desc *cache, const int64_t *src
  * word of the current device (PKV_DEVERR_* bits) into *device_error_word.
  * Returns PKV_OK when the word was zero, PKV_ERR_OUT_OF_RANGE or
  * PKV_ERR_TIMEOUT (when that bit is set) otherwise. On PKV_DEVERR_TIMEOUT it
- * also zeroes pkv_decode_attention_static's scratch on the current device
- * (synchronously); caller-owned workspaces are the caller's to zero.
+ * also zeroes pkv_decode_attention_static's scratch on the current device:
+ * the memset is enqueued on `stream` and waited for, so it has completed when
+ * the call returns, whatever stream the next call uses. Caller-owned
+ * workspaces are the caller's to zero.
  */
 pkv_status pkv_get_error(int32_t *device_error_word, void *stream);
+
+/*
+ * pkv_debug_set_wait_fault — test hook for the bounded on-chip waits; the
+ * pages have no counterpart. It lets a test make a wait run out without
+ * faulting or hanging anything.
+ *
+ * Every wait on an on-chip barrier inside a decode kernel gives up after a
+ * limit (2 s by default), sets PKV_DEVERR_TIMEOUT in the device error word
+ * and ends its warp's work, so the kernel returns and the context stays
+ * usable. After this call, decode launches (pkv_decode_attention*, on any
+ * thread and device) use wait_limit_ns as that limit (0 restores the
+ * default), and the next drop_arrivals launches each withhold one producer
+ * thread's arrival on the first stage of their first CTA: that stage never
+ * fills, so its wait runs out. Such a launch leaves the output of the units
+ * its first CTA holds unwritten and may leave split-K arrival counters set:
+ * zero the workspace before reusing it (pkv_get_error zeroes
+ * pkv_decode_attention_static's scratch). Returns PKV_ERR_INVALID_ARG for
+ * drop_arrivals < 0. Not for production use: set it back to (0, 0).
+ */
+pkv_status pkv_debug_set_wait_fault(uint64_t wait_limit_ns, int32_t drop_arrivals);
 
 /* Static text for a status code. */
 const char *pkv_status_string(pkv_status status);

@@ -130,6 +130,10 @@ def lib():
         L.pkv_decode_attention.restype = i32
         L.pkv_decode_attention_ex.argtypes = dec + [ctypes.POINTER(DecodeOptions)]
         L.pkv_decode_attention_ex.restype = i32
+        L.pkv_append_decode_attention.argtypes = [dp, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp,
+                                                  ctypes.c_float, vp, i32, vp, sz, vp,
+                                                  ctypes.POINTER(DecodeOptions)]
+        L.pkv_append_decode_attention.restype = i32
         L.pkv_block_copy.argtypes = [dp, vp, i32, vp, vp, vp]
         L.pkv_block_copy.restype = i32
         qp = ctypes.POINTER(QCacheDesc)
@@ -151,6 +155,8 @@ def lib():
                                                   vp, i32, vp, sz, vp,
                                                   ctypes.POINTER(DecodeOptions)]
         L.pkv_decode_attention_prefix.restype = i32
+        L.pkv_debug_set_wait_fault.argtypes = [ctypes.c_uint64, i32]
+        L.pkv_debug_set_wait_fault.restype = i32
         L.pkv_get_error.argtypes = [ctypes.POINTER(ctypes.c_int32), vp]
         L.pkv_get_error.restype = i32
         L.pkv_status_string.argtypes = [i32]
@@ -305,6 +311,59 @@ class PreparedDecode:
         _check(self._fn(*self._args, _stream(stream), ctypes.byref(opts)))
 
 
+def append_decode_attention(q, k_new, v_new, k_pool, v_pool, block_tables, context_lens,
+                            scale: float, out: Optional[torch.Tensor] = None,
+                            out_dtype: Optional[torch.dtype] = None,
+                            workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                            consumer: int = 0, stream=None, tables_ready: bool = False,
+                            pending_tail: int = 0) -> torch.Tensor:
+    """One decode step in one launch (pkv_append_decode_attention): each
+    sequence's new row k_new[s] / v_new[s] [S][Hk][D] goes to position
+    context_lens[s] - 1 (the slot its block table gives), and the attention
+    runs over the context including it."""
+    desc = _pools(k_pool, v_pool)
+    S, Hq, D = q.shape
+    q, k_new, v_new = q.contiguous(), k_new.contiguous(), v_new.contiguous()
+    bt, cl = block_tables.contiguous(), context_lens.contiguous()
+    assert bt.dtype == torch.int32 and cl.dtype == torch.int32
+    assert q.dtype == k_pool.dtype == k_new.dtype == v_new.dtype
+    if out is None:
+        out = torch.empty(S, Hq, D, dtype=out_dtype or q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(k_pool, Hq, num_ctas)
+    opts = DecodeOptions()
+    opts.num_ctas = num_ctas
+    opts.consumer = consumer
+    opts.tables_ready = int(tables_ready)
+    opts.pending_tail = int(pending_tail)
+    _check(lib().pkv_append_decode_attention(
+        ctypes.byref(desc), _ptr(q), S, Hq, _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+        _ptr(bt), bt.shape[1], _ptr(cl), float(scale), _ptr(out), DTYPE_CODE[out.dtype],
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream),
+        ctypes.byref(opts)))
+    return out
+
+
+class PreparedAppendDecode(PreparedDecode):
+    """A pkv_append_decode_attention call whose arguments are marshalled once
+    (see PreparedDecode); k_new and v_new are rewritten in place each step."""
+
+    def __init__(self, q, k_new, v_new, k_pool, v_pool, block_tables, context_lens,
+                 scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                 num_ctas: int = 0, consumer: int = 0, tables_ready: bool = False,
+                 pending_tail: int = 0):
+        super().__init__(q, k_pool, v_pool, block_tables, context_lens, scale, out, workspace,
+                         num_ctas, consumer, tables_ready, pending_tail)
+        for t in (k_new, v_new):
+            if not t.is_contiguous() or t.dtype != k_pool.dtype:
+                raise ValueError("k_new / v_new must be contiguous, in the cache dtype")
+        self._keep = self._keep + (k_new, v_new)
+        a = self._args
+        # q, S, Hq | k_new, v_new | pools, tables, ...
+        self._args = a[:4] + (k_new.data_ptr(), v_new.data_ptr()) + a[4:]
+        self._fn = lib().pkv_append_decode_attention
+
+
 class PreparedAppend:
     """An append call whose arguments are marshalled once (see PreparedDecode)."""
 
@@ -332,6 +391,21 @@ def block_copy(pairs, k_pool, v_pool, stream=None) -> None:
     assert p.device.type == "cpu", "block-copy pairs are host memory"
     _check(lib().pkv_block_copy(ctypes.byref(desc), _ptr(p), p.shape[0], _ptr(k_pool),
                                 _ptr(v_pool), _stream(stream)))
+
+
+def set_wait_fault(wait_limit_ns: int = 0, drop_arrivals: int = 0) -> None:
+    """Test hook (pkv_debug_set_wait_fault): the wait limit of the next decode
+    launches (0 = the default 2 s) and how many of them withhold one arrival
+    so that a bounded wait runs out. (0, 0) restores normal operation."""
+    _check(lib().pkv_debug_set_wait_fault(int(wait_limit_ns), int(drop_arrivals)))
+
+
+def get_error_status(stream=None):
+    """(status, word): pkv_get_error's return code and the device error word
+    it read and cleared."""
+    w = ctypes.c_int32(0)
+    st = lib().pkv_get_error(ctypes.byref(w), _stream(stream))
+    return int(st), int(w.value)
 
 
 def get_error(stream=None) -> int:

@@ -25,12 +25,30 @@ __device__ __forceinline__ void append_allow_next_grid() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Slot of token i: slot_mapping[i], or (slot_mapping NULL: the token is the
+// newest of sequence i) the block table's slot of position L - 1, -1 for an
+// empty context. A length past the table is clamped as the decode clamps it,
+// and a block id outside the pool is skipped (the decode flags both).
+__device__ __forceinline__ int64_t append_slot(const int64_t *slot_mapping, const int32_t *tables,
+                                               const int32_t *lens, int M, int B, int NB,
+                                               int tok) {
+    if (slot_mapping) return __ldg(slot_mapping + tok);
+    int L = __ldg(lens + tok);
+    if (L > M * B) L = M * B;
+    if (L <= 0) return -1;
+    const int blk = __ldg(tables + (size_t)tok * M + (L - 1) / B);
+    if (blk < 0 || blk >= NB) return -1;
+    return (int64_t)blk * B + (L - 1) % B;
+}
+
 // grid-stride over (token, vector-in-token); vectors per token = Hk*D*es/16.
 // With inputs_ready each thread reads its first vector (slot, K and V) before
 // the wait on the previous kernel, so only the stores remain after it.
 __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k_new,
                                                      const uint4 *__restrict__ v_new,
                                                      const int64_t *__restrict__ slot_mapping,
+                                                     const int32_t *__restrict__ tables,
+                                                     const int32_t *__restrict__ lens, int M,
                                                      int num_tokens, uint4 *__restrict__ k_pool,
                                                      uint4 *__restrict__ v_pool, int NB, int B,
                                                      int vec_per_row, int vec_per_token,
@@ -46,7 +64,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
     uint4 kv = {}, vv = {};
     const bool early = inputs_ready && i < total;
     if (early) {
-        slot = __ldg(slot_mapping + i / vec_per_token);
+        slot = append_slot(slot_mapping, tables, lens, M, B, NB, (int)(i / vec_per_token));
         kv = __ldg(k_new + i);
         vv = __ldg(v_new + i);
     }
@@ -54,7 +72,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
     for (bool have = early; i < total; i += stride, have = false) {
         const int tok = (int)(i / vec_per_token);
         const int v = (int)(i - (int64_t)tok * vec_per_token);
-        if (!have) slot = __ldg(slot_mapping + tok);
+        if (!have) slot = append_slot(slot_mapping, tables, lens, M, B, NB, tok);
         if (slot < 0) continue;
         const int64_t blk = slot / B;
         const int off = (int)(slot - blk * B);
@@ -78,7 +96,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
 cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
                           const int64_t *slot_mapping, int num_tokens, void *k_pool, void *v_pool,
                           int NB, int Hk, int B, int D, int inputs_ready, unsigned *err,
-                          cudaStream_t st) {
+                          cudaStream_t st, const int32_t *tables, const int32_t *lens, int M) {
     const int es = dtype == PKV_F32 ? 4 : 2;
     const int vec_per_row = D * es / 16;
     const int vec_per_token = Hk * vec_per_row;
@@ -97,7 +115,8 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, append_kernel, static_cast<const uint4 *>(k_new),
-                              static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
+                              static_cast<const uint4 *>(v_new), slot_mapping, tables, lens, M,
+                              num_tokens,
                               static_cast<uint4 *>(k_pool), static_cast<uint4 *>(v_pool), NB, B,
                               vec_per_row, vec_per_token, inputs_ready, err);
 }

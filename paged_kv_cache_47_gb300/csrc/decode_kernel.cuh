@@ -43,6 +43,7 @@
 #include <cuda_fp8.h>
 #include <math_constants.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "decomp.h"
@@ -70,7 +71,7 @@ constexpr int tile_tokens(int QK, int GMAX) { return big_tiles(QK, GMAX) ? 128 :
 constexpr int math_warps(int QK, int GMAX) { return big_tiles(QK, GMAX) ? 8 : kConsumerWarps; }
 constexpr int kernel_threads(int QK, int GMAX) { return 32 * (math_warps(QK, GMAX) + kProducerWarps); }
 
-template <typename T, int D, int GMAX, bool MMA, int QK = 0>
+template <typename T, int D, int GMAX, bool MMA, int QK = 0, bool FUSED = false>
 struct SplitCfg {
     static constexpr int ES = QK ? 1 : (int)sizeof(T);  // bytes of one cache element
     static constexpr int ROWB = D * ES;              // bytes of one K or V row
@@ -83,7 +84,9 @@ struct SplitCfg {
     static constexpr int KVB = NP * PLANE;           // bytes of one tile of K (or V)
     static constexpr int SCB = QK ? 1024 : 0;        // K then V scales of the tile (2 x 256 B)
     static constexpr int QB = ((GMAX * QROWB + 1023) / 1024) * 1024;
-    static constexpr int STAGE = 2 * KVB + SCB + QB; // multiple of 1024
+    // fused append: the newest row's K then V (side slot, 1 KB-aligned)
+    static constexpr int NEWB = FUSED ? ((2 * ROWB + 1023) / 1024) * 1024 : 0;
+    static constexpr int STAGE = 2 * KVB + SCB + QB + NEWB; // multiple of 1024
     static constexpr int NTN = GMAX / 8;             // mma n-tiles (MMA only)
     static constexpr int COMB_O = CW * GMAX * D * 4;
     static constexpr int COMB_ML = 2 * CW * GMAX * 4;
@@ -838,12 +841,84 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const PendSeg
 }
 
 // ---------------------------------------------------------------------------
+// fused append: the newest row into the stage's side slot
+// ---------------------------------------------------------------------------
+// Chunks i = tb, tb + tpb, ... < 2 * ROWB / 16 of row `row` ([S][Hk] rows of
+// ROWB bytes) of k_new (i < ROWB / 16), then of v_new, to side + 16 i; zeros
+// when !valid.
+template <int ROWB>
+__device__ __noinline__ void copy_new_row(uint32_t side, const void *k_new, const void *v_new,
+                                          size_t row, int tb, int tpb, bool valid) {
+    constexpr int CPR = ROWB / 16;
+    const uint8_t *kn = static_cast<const uint8_t *>(k_new) + row * ROWB;
+    const uint8_t *vn = static_cast<const uint8_t *>(v_new) + row * ROWB;
+    for (int i = tb; i < 2 * CPR; i += tpb)
+        cp_async_16(side + i * 16, i < CPR ? kn + i * 16 : vn + (i - CPR) * 16, valid);
+}
+
+// ---------------------------------------------------------------------------
+// fused append: write each context's newest K/V row into its slot
+// ---------------------------------------------------------------------------
+// Run by the producer threads of a CTA once they have issued their last
+// tile. For every unit of chunk 0 whose last tile lies in this CTA's range
+// [t_begin, t_end) (so exactly one CTA handles each (sequence, kv head)), the
+// rows k_new[s][g] and v_new[s][g] go to position L - 1 of sequence s: block
+// block_tables[s][(L - 1) / B], offset (L - 1) % B. The stores wait for the
+// preceding kernel on the stream, like every store of the decode. A block id
+// outside the pool is skipped (the tile loop has flagged it already).
+template <typename Cfg>
+__device__ __forceinline__ void fused_append_rows(const DecodeParams &p, const int *seq_prefix,
+                                                  const int *seq_len, int64_t t_begin,
+                                                  int64_t t_end, int pt, bool waited) {
+    constexpr int CPR = Cfg::ROWB / 16;        // 16-byte chunks per row
+    constexpr int CPU = 2 * CPR;               // K and V chunks per unit
+    static_assert(kProducerThreads % CPU == 0, "a unit's chunks fill whole thread groups");
+    constexpr int UPP = kProducerThreads / CPU;   // units per pass of the producer threads
+    const int j = pt / CPU, c = pt - (pt / CPU) * CPU;
+    const bool is_v = c >= CPR;
+    const int ch = is_v ? c - CPR : c;
+    PkvCursor cur;
+    pkv_cursor_at(cur, t_begin, seq_prefix, seq_len, p.S, Cfg::TT);
+    int k = 0;   // index of the unit end among this CTA's chunk-0 unit ends
+    while (cur.s < p.S) {
+        const int64_t T_u = (int64_t)seq_prefix[cur.s] + (int64_t)cur.u * cur.n;
+        if (T_u >= t_end) break;
+        const int64_t last = T_u + cur.n - 1;
+        if (last >= t_end) break;   // the unit ends in a later CTA's range
+        if (last >= t_begin && cur.u % p.NC == 0) {
+            if (k % UPP == j) {
+                if (!waited) {
+                    grid_dependency_wait();
+                    waited = true;
+                }
+                const int g = cur.u / p.NC;
+                const int pos = cur.L - 1;
+                const int e = __ldg(p.block_tables + (size_t)cur.s * p.M + pos / p.B);
+                if (e >= 0 && e < p.NB) {
+                    const size_t src = ((size_t)cur.s * p.Hk + g) * Cfg::ROWB + ch * 16;
+                    const size_t dst = (((size_t)e * p.Hk + g) * p.B + pos % p.B) * Cfg::ROWB +
+                                       ch * 16;
+                    const uint8_t *from = static_cast<const uint8_t *>(is_v ? p.v_new : p.k_new);
+                    uint8_t *to = static_cast<uint8_t *>(const_cast<void *>(is_v ? p.vp : p.kp));
+                    *reinterpret_cast<uint4 *>(to + dst) =
+                        __ldg(reinterpret_cast<const uint4 *>(from + src));
+                }
+            }
+            ++k;
+        }
+        // next unit (skipping sequences without tiles)
+        cur.ti = cur.n - 1;
+        pkv_cursor_next(cur, seq_len, p.S, p.U, Cfg::TT);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // the split-K kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA, int QK, bool FLAT>
+template <typename T, int D, int GMAX, bool MMA, int QK, bool FLAT, bool FUSED>
 __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     decode_split_kernel(const DecodeParams p) {
-    using Cfg = SplitCfg<T, D, GMAX, MMA, QK>;
+    using Cfg = SplitCfg<T, D, GMAX, MMA, QK, FUSED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -911,7 +986,10 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         // the context, blocks past the tile and out-of-pool block ids are
         // zero-filled (src-size 0): no address outside the pool is formed
         // and the math warps never see stale or garbage rows.
-        constexpr int LA = 8;
+        // LA = 4: the loop body is unrolled LA times and its code size shows
+        // in the instruction fetch (measured on the Llama-shaped step: 8 tiles
+        // ahead 118.7 us, 6: 114.3, 4: 114.1, 3: 113.9, 2: 116.4 us)
+        constexpr int LA = 4;
         constexpr int CPR = Cfg::ROWB / 16;          // 16-byte chunks per K/V row
         constexpr int CPRQ = Cfg::QROWB / 16;        // 16-byte chunks per q row
         const int pt = tid - Cfg::CW * 32;            // 0 .. kProducerThreads-1
@@ -919,6 +997,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         const int tpb = kProducerThreads / bpt;       // producer threads per block
         const int jblk = pt / tpb;
         const int tb = pt - jblk * tpb;
+        const int jrow0 = jblk * p.B;                 // first tile row of this thread's block
         const uint8_t *kpool = static_cast<const uint8_t *>(p.kp);
         const uint8_t *vpool = FLAT ? kpool + p.v_off : static_cast<const uint8_t *>(p.vp);
         PkvCursor cur, la;
@@ -974,6 +1053,10 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         // unit values, refreshed at each segment's first tile
         int h0 = 0, gca = 0;
         size_t head_off = 0, head_rows = 0;
+        // fused append (FUSED variants): the newest row of each context comes
+        // from k_new / v_new, so the pool holds rows 0 .. L - 2 of it
+        static_assert(!FUSED || (!FLAT && QK == 0), "the fused append is for paged 16/32-bit caches");
+        const bool drop_first = p.drop_arrival && cta == 0 && pt == 0;   // test hook
         bool ok = true;
         for (int it0 = 0; it0 < n_my && ok; it0 += LA) {
 #pragma unroll
@@ -987,12 +1070,19 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 }
                 const int stage = it % Cfg::NST;
                 const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
-                if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, p.err)) {
+                if (!mbar_wait(empty0 + 8 * stage, ph ^ 1u, p.err, p.wait_ns)) {
                     ok = false;
                     break;
                 }
                 const int ntok = min(Cfg::TT, cur.L - cur.ti * Cfg::TT);
-                if (!waited && cur.ti * Cfg::TT + ntok > cur.L - p.pending_tail) {
+                // fused append: tile row of the context's newest row (the last
+                // row of the unit's last tile), -1 elsewhere
+                const int rnew = (FUSED && cur.ti == cur.n - 1) ? ntok - 1 : -1;
+                // pool rows of this tile end at pool_end; with pending_tail n the
+                // last n rows of the context may still be written by the
+                // preceding kernel (a fused append's newest row is not a pool row)
+                const int pool_end = cur.ti * Cfg::TT + ntok - (FUSED && rnew >= 0 ? 1 : 0);
+                if (!waited && pool_end > cur.L - p.pending_tail) {
                     grid_dependency_wait();   // the same tiles for every producer thread
                     waited = true;
                 }
@@ -1002,6 +1092,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                     const int chunk = cur.u - g * p.NC;
                     h0 = g * p.G + chunk * p.GC;
                     gca = min(p.GC, p.G - chunk * p.GC);
+
                     head_rows = (size_t)g * p.B;               // rows before kv head g in a block
                     head_off = FLAT ? (size_t)g * Cfg::ROWB : head_rows * Cfg::ROWB;
                 }
@@ -1032,6 +1123,22 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                         cp_async_16(sV + soff[c], vpool + off, v);
                     }
                 }
+                if constexpr (FUSED) {
+                    // the unit's last tile: its newest row's K and V rows go from
+                    // k_new / v_new to the stage's side slot (zeros for a bad
+                    // block id, as the pool copy would give); the math warp
+                    // holding that row puts them in place before its tile step.
+                    // The pool copy above also fetched the row's slot: whatever
+                    // it holds is overwritten.
+                    // The threads of the row's block copy it (their blk_ok is
+                    // that block's). Out of line: the issue loop is unrolled
+                    // and its code size shows in the instruction fetch.
+                    if (rnew >= jrow0 && rnew < jrow0 + p.B)
+                        copy_new_row<Cfg::ROWB>(sQ + Cfg::QB, p.k_new, p.v_new,
+                                                (size_t)cur.s * p.Hk +
+                                                    (p.NC == 1 ? cur.u : cur.u / p.NC),
+                                                tb, tpb, blk_ok);
+                }
                 if constexpr (QK != 0) {
                     // the block's B row scales, 4 rows per 16-byte copy; the
                     // bytes of rows past the context are zeroed, not read
@@ -1051,7 +1158,10 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                     for (int i = pt; i < gca * CPRQ; i += kProducerThreads)
                         cp_async_16(sQ + i * 16, qsrc + (size_t)i * 16, true);
                 }
-                cp_async_arrive_noinc(full);
+                // test hook (off unless a test asks for it): CTA 0's first
+                // producer thread withholds its arrival on its first stage, so
+                // the math warps' wait for that stage runs out
+                if (!(drop_first && it == 0)) cp_async_arrive_noinc(full);
                 if (pt == 0) {
                     const int64_t T_u = (int64_t)seq_prefix[cur.s] + (int64_t)cur.u * cur.n;
                     const bool last = (it == n_my - 1) || (cur.ti == cur.n - 1);
@@ -1061,7 +1171,8 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                     mt.h0 = h0;
                     mt.gca = gca;
                     mt.ntok = ntok;
-                    mt.flags = (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0);
+                    mt.flags = (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0) |
+                               (FUSED && rnew >= 0 ? kNewRow : 0);
                     mt.slot = T_u > t_begin ? 1 : 0;
                     mt.tu = (int)T_u;
                     mt.nu = cur.n;
@@ -1070,6 +1181,9 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 }
                 pkv_cursor_next(cur, seq_len, p.S, p.U, Cfg::TT);
             }
+        }
+        if constexpr (FUSED) {
+            if (ok) fused_append_rows<Cfg>(p, seq_prefix, seq_len, t_begin, t_end, pt, waited);
         }
         cp_async_wait_all();   // this thread's copies land before it exits
         return;
@@ -1089,7 +1203,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     for (int it = 0; it < n_my; ++it) {
         const int stage = it % Cfg::NST;
         const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
-        if (!mbar_wait(full0 + 8 * stage, ph, p.err)) return;
+        if (!mbar_wait(full0 + 8 * stage, ph, p.err, p.wait_ns)) return;
         const TileMeta mt = meta[stage];
         const uint32_t sK = sbase + stage * Cfg::STAGE;
         const uint32_t sV = sK + Cfg::KVB;
@@ -1097,6 +1211,27 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
             cs.reset();
             cs.load_q(smem + stage * Cfg::STAGE + 2 * Cfg::KVB + Cfg::SCB, mt.gca, p.scale_log2,
                       lane);
+        }
+        if constexpr (FUSED) {
+            // the context's newest row: the math warp whose 16 rows hold it
+            // copies its K and V rows from the side slot into the tile (no
+            // other warp reads those rows)
+            if ((mt.flags & kNewRow) && (mt.ntok - 1) / 16 == warp) {
+                constexpr int CPRw = Cfg::ROWB / 16;
+                const int rn = mt.ntok - 1;
+                const uint32_t side = sK + 2 * Cfg::KVB + Cfg::SCB + Cfg::QB;
+#pragma unroll
+                for (int i = lane; i < 2 * CPRw; i += 32) {
+                    uint32_t a, b, c2, d;
+                    lds_u32x4(side + i * 16, a, b, c2, d);
+                    const uint32_t dst = i < CPRw ? swz<Cfg::TT>(sK, rn, i)
+                                                  : swz<Cfg::TT>(sV, rn, i - CPRw);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(a),
+                                 "r"(b), "r"(c2), "r"(d)
+                                 : "memory");
+                }
+                __syncwarp();
+            }
         }
         if constexpr (QK != 0) {
             // the tile step reads this warp's 16 rows of codes straight into registers
@@ -1110,11 +1245,11 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
 
         if (mt.flags & kLast) {
             // combine the math warps' softmax states for this segment
-            if (!mbar_wait(comb_empty, ((uint32_t)seg & 1u) ^ 1u, p.err)) return;
+            if (!mbar_wait(comb_empty, ((uint32_t)seg & 1u) ^ 1u, p.err, p.wait_ns)) return;
             cs.write_comb(comb_o, comb_m, comb_l, warp, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(comb_full);
-            if (!mbar_wait(comb_full, (uint32_t)seg & 1u, p.err)) return;
+            if (!mbar_wait(comb_full, (uint32_t)seg & 1u, p.err, p.wait_ns)) return;
             if (!waited && warp < kMergeSlices) {   // stores wait for the preceding kernel
                 grid_dependency_wait();
                 waited = true;
@@ -1248,20 +1383,23 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
 // ---------------------------------------------------------------------------
 // host-side launch of one variant
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA, int QK = 0, bool FLAT = false>
+template <typename T, int D, int GMAX, bool MMA, int QK = 0, bool FLAT = false, bool FUSED = false>
 struct SplitVariant {
-    using Cfg = SplitCfg<T, D, GMAX, MMA, QK>;
+    using Cfg = SplitCfg<T, D, GMAX, MMA, QK, FUSED>;
 
+    // Per-device state lives in atomics: host threads making their first
+    // calls on a device at the same time may both set the attribute (the
+    // same value, so harmless), but never read a half-written flag.
     static cudaError_t prepare(int dev) {
-        static bool done[64] = {false};
+        static std::atomic<bool> done[64];
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-        if (!done[dev]) {
+        if (!done[dev].load(std::memory_order_acquire)) {
             const size_t smem = Cfg::smem_bytes(kMaxSeqsPerLaunch);
-            cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, GMAX, MMA, QK, FLAT>,
+            cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, GMAX, MMA, QK, FLAT, FUSED>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem);
             if (e != cudaSuccess) return e;
-            done[dev] = true;
+            done[dev].store(true, std::memory_order_release);
         }
         return cudaSuccess;
     }
@@ -1281,22 +1419,23 @@ struct SplitVariant {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT>, p);
+        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT, FUSED>, p);
     }
 
     // occupancy of this variant on the current device (queried once per device)
     static int max_ctas_per_sm() {
-        static int cached[64] = {0};
+        static std::atomic<int> cached[64];
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-        if (cached[dev] > 0) return cached[dev];
+        const int c = cached[dev].load(std::memory_order_acquire);
+        if (c > 0) return c;
         if (prepare(dev) != cudaSuccess) return 0;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &n, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT>, Cfg::THREADS,
+                &n, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT, FUSED>, Cfg::THREADS,
                 Cfg::smem_bytes(kMaxSeqsPerLaunch)) != cudaSuccess)
             return 0;
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_release);
         return n;
     }
 

@@ -68,16 +68,24 @@ pkv_status scratch_for_current_device(void **ptr, int *sms) {
 
 namespace pkv {
 // Zero the scratch array of the current device if a call has used it there.
-cudaError_t clear_static_scratch() {
+// The memset is ordered on `stream` and waited for before returning, so it is
+// complete whatever stream the caller uses next (a plain cudaMemset would be
+// asynchronous for device memory and ordered only against the legacy default
+// stream, which non-blocking streams do not synchronise with).
+cudaError_t clear_static_scratch(cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return e;
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     void *p = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_scratch_mu);
         p = g_scratch_ptr[dev];
     }
-    return p ? cudaMemset(p, 0, PKV_STATIC_SCRATCH_BYTES) : cudaSuccess;
+    if (!p) return cudaSuccess;
+    e = cudaMemsetAsync(p, 0, PKV_STATIC_SCRATCH_BYTES, stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamSynchronize(stream);
 }
 }  // namespace pkv
 

@@ -1,9 +1,10 @@
 // Device helpers for the sm_103a kernels: mbarrier, cp.async, programmatic
 // dependent launch, ldmatrix, mma.sync and element conversions, as inline PTX.
 //
-// Every wait on an mbarrier is bounded in time: after PKV_WAIT_LIMIT_NS the
-// waiter sets PKV_DEVERR_TIMEOUT in the error word and returns false, so a
-// protocol mistake ends the kernel instead of hanging the GPU.
+// Every wait on an mbarrier is bounded in time: after a limit given by the
+// launch (PKV_WAIT_LIMIT_NS unless a test shortens it) the waiter sets
+// PKV_DEVERR_TIMEOUT in the error word and returns false, so a protocol
+// mistake ends the kernel instead of hanging the GPU.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -12,7 +13,6 @@
 
 #include "../../include/pkv.h"
 
-#define PKV_WAIT_LIMIT_NS 2000000000ull  // 2 s: far above any legitimate wait
 
 namespace pkv {
 
@@ -62,13 +62,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete, for at most
-// PKV_WAIT_LIMIT_NS. Returns false (and flags the error word) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err) {
+// limit_ns. Returns false (and flags the error word) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err,
+                                          uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > PKV_WAIT_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             atomicOr(err, PKV_DEVERR_TIMEOUT);
             return false;
         }

@@ -7,6 +7,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_set>
 
@@ -146,18 +147,19 @@ pkv_status make_plan_quant(const pkv_qcache_desc *c, int Hq, const pkv_decode_op
 
 // SM count of the current device (queried once per device)
 pkv_status sm_count(int *sms) {
-    static int cached[64] = {0};
+    // atomics: first calls from several host threads may race to fill it
+    static std::atomic<int> cached[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device index %d", dev);
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_acquire);
+    if (n == 0) {
         e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "querying the SM count");
-        cached[dev] = n;
+        cached[dev].store(n, std::memory_order_release);
     }
-    *sms = cached[dev];
+    *sms = n;
     return PKV_OK;
 }
 
@@ -238,9 +240,27 @@ pkv_status copy_blocks(int NB, const int64_t *pairs, int n, void *k_pool, void *
     return PKV_OK;
 }
 
+// Test hook state (pkv_debug_set_wait_fault): the wait limit of decode
+// launches and how many launches still withhold an arrival.
+std::atomic<unsigned long long> g_wait_ns{0};
+std::atomic<int> g_drop_left{0};
+
 }  // namespace
 
 namespace pkv {
+void next_wait_fault(unsigned long long *wait_ns, int *drop_arrival) {
+    const unsigned long long w = g_wait_ns.load(std::memory_order_relaxed);
+    *wait_ns = w ? w : PKV_WAIT_LIMIT_NS;
+    int left = g_drop_left.load(std::memory_order_relaxed);
+    *drop_arrival = 0;
+    while (left > 0) {
+        if (g_drop_left.compare_exchange_weak(left, left - 1, std::memory_order_relaxed)) {
+            *drop_arrival = 1;
+            break;
+        }
+    }
+}
+
 pkv_status device_error_word(unsigned **out) { return device_error_ptr(out); }
 
 pkv_status set_last_error(pkv_status st, const char *fmt, ...) {
@@ -269,6 +289,13 @@ const char *pkv_status_string(pkv_status s) {
 }
 
 const char *pkv_last_error_message(void) { return g_msg; }
+
+pkv_status pkv_debug_set_wait_fault(uint64_t wait_limit_ns, int32_t drop_arrivals) {
+    if (drop_arrivals < 0) return fail(PKV_ERR_INVALID_ARG, "drop_arrivals %d", drop_arrivals);
+    g_wait_ns.store(wait_limit_ns, std::memory_order_relaxed);
+    g_drop_left.store(drop_arrivals, std::memory_order_relaxed);
+    return PKV_OK;
+}
 
 pkv_status pkv_append(const pkv_cache_desc *cache, const void *k_new, const void *v_new,
                       const int64_t *slot_mapping, int32_t num_tokens, void *k_pool,
@@ -370,6 +397,8 @@ struct DecodeArgs {
     size_t ws_bytes;
     cudaStream_t stream;
     const pkv_decode_options *opts;
+    // fused append (paged caches): each sequence's new row, [S][Hk][D]
+    const void *k_new = nullptr, *v_new = nullptr;
     // flat spans (tables is then NULL): see DecodeParams
     const int32_t *slots = nullptr;
     const int32_t *committed = nullptr;
@@ -463,6 +492,10 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
         p.vp = a.vp;
         p.ks = a.ks;
         p.vs = a.vs;
+        pkv::next_wait_fault(&p.wait_ns, &p.drop_arrival);
+        const size_t new_off = (size_t)s0 * a.Hk * a.D * a.q_es;
+        p.k_new = a.k_new ? static_cast<const uint8_t *>(a.k_new) + new_off : nullptr;
+        p.v_new = a.v_new ? static_cast<const uint8_t *>(a.v_new) + new_off : nullptr;
         const bool first = s0 == 0;
         cudaError_t e;
         if (first && ev[0] && (e = record_timing_event(ev[0], a.stream)) != cudaSuccess)
@@ -494,6 +527,54 @@ pkv_status pkv_decode_attention_ex(const pkv_cache_desc *cache, const void *q, i
     if ((st = check_decode_args(a)) != PKV_OK) return st;
     Plan pl;
     if ((st = make_plan(cache, num_q_heads, options, &pl)) != PKV_OK) return st;
+    return run_decode(pl, a);
+}
+
+pkv_status pkv_append_decode_attention(const pkv_cache_desc *cache, const void *q,
+                                       int32_t num_seqs, int32_t num_q_heads, const void *k_new,
+                                       const void *v_new, void *k_pool, void *v_pool,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t *context_lens, float scale, void *out,
+                                       int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                       void *stream, const pkv_decode_options *options) {
+    pkv_status st = check_cache(cache);
+    if (st != PKV_OK) return st;
+    DecodeArgs a{cache->num_blocks, cache->block_size, cache->num_kv_heads, cache->head_dim,
+                 elem_bytes(cache->dtype), q, num_seqs, num_q_heads, k_pool, v_pool, nullptr,
+                 nullptr, block_tables, max_blocks_per_seq, context_lens, scale, out, out_dtype,
+                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream), options};
+    if ((st = check_decode_args(a)) != PKV_OK) return st;
+    if (num_seqs > 0 && (!k_new || !v_new))
+        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16))
+        return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    Plan pl;
+    if ((st = make_plan(cache, num_q_heads, options, &pl)) != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
+    // one launch where a fused variant exists (fp16 / bf16 with the tensor-core
+    // math); otherwise the append (slots from the tables) and then the decode,
+    // which waits for it before it reads the newest rows
+    const pkv::DecodeVariant *fv =
+        pl.mma ? pkv::find_variant_fused(cache->dtype, cache->head_dim, pl.gmax) : nullptr;
+    if (fv) {
+        pl.variant = fv;
+        a.k_new = k_new;
+        a.v_new = v_new;
+        return run_decode(pl, a);
+    }
+    if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out)
+        return fail(PKV_ERR_INVALID_ARG, "a pointer argument is NULL");
+    if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(block_tables, 4) ||
+        !aligned(context_lens, 4))
+        return fail(PKV_ERR_INVALID_ARG, "q and the pools must be 16-byte aligned");
+    unsigned *err = nullptr;
+    if ((st = device_error_ptr(&err)) != PKV_OK) return st;
+    cudaError_t e = pkv::launch_append(cache->dtype, k_new, v_new, nullptr, num_seqs, k_pool,
+                                       v_pool, cache->num_blocks, cache->num_kv_heads,
+                                       cache->block_size, cache->head_dim, 0, err,
+                                       static_cast<cudaStream_t>(stream), block_tables,
+                                       context_lens, max_blocks_per_seq);
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
     return run_decode(pl, a);
 }
 
@@ -583,7 +664,7 @@ pkv_status pkv_get_error(int32_t *device_error_word, void *stream) {
     if (w == 0) return PKV_OK;
     if (w & PKV_DEVERR_TIMEOUT) {
         // a kernel that gave up may have left split-K arrival counters set
-        if ((e = pkv::clear_static_scratch()) != cudaSuccess)
+        if ((e = pkv::clear_static_scratch(static_cast<cudaStream_t>(stream))) != cudaSuccess)
             return cuda_fail(e, "zeroing the static scratch");
         return fail(PKV_ERR_TIMEOUT, "device error word 0x%x", w);
     }

@@ -7,6 +7,9 @@
 
 #include "../../include/pkv.h"
 
+// Default limit of every on-chip wait of a decode launch.
+#define PKV_WAIT_LIMIT_NS 2000000000ull  // 2 s: far above any legitimate wait
+
 namespace pkv {
 
 constexpr int kConsumerWarps = 4;                  // math warps of the split-K kernel
@@ -32,6 +35,8 @@ struct TileMeta {
 constexpr int kFirst = 1;  // first tile of this CTA's segment of a unit
 constexpr int kLast = 2;   // last tile of this CTA's segment of a unit
 constexpr int kWhole = 4;  // the segment is the whole unit: write the output directly
+constexpr int kNewRow = 8; // fused append: the tile's last row is the context's newest,
+                           // whose K/V rows wait in the stage's side slot
 
 struct DecodeParams {
     const void *q;              // [S][Hq][D]
@@ -72,7 +77,22 @@ struct DecodeParams {
     const int32_t *slots;       // [S] batch entry -> slot (flat spans only)
     const int32_t *committed;   // [NB] tokens of each slot backed by memory
     size_t slot_stride, v_off;
+    // Append fused into the decode (paged 16/32-bit caches; NULL = none):
+    // k_new / v_new [S][Hk][D] hold the row each sequence adds at position
+    // L - 1. The attention takes that row from here instead of the pool, and
+    // the producer warps write it into its slot (the block table's entry for
+    // position L - 1) once they have issued their last tile.
+    const void *k_new, *v_new;
+    // Bounded waits: every mbarrier wait of the launch gives up after wait_ns
+    // (PKV_WAIT_LIMIT_NS by default). drop_arrival != 0 is a test hook: the
+    // first producer thread of CTA 0 withholds its arrival on its first stage.
+    unsigned long long wait_ns;
+    int drop_arrival;
 };
+
+// Wait limit and withheld arrivals for the next decode launches (test hook,
+// pkv_debug_set_wait_fault); returns the limit and whether this launch drops.
+void next_wait_fault(unsigned long long *wait_ns, int *drop_arrival);
 
 using SplitLaunchFn = cudaError_t (*)(const DecodeParams &, cudaStream_t);
 using MaxCtasFn = int (*)();
@@ -88,6 +108,9 @@ struct DecodeVariant {
 const DecodeVariant *find_variant_f32(int D, int gmax, bool mma);
 const DecodeVariant *find_variant_f16(int D, int gmax, bool mma);
 const DecodeVariant *find_variant_bf16(int D, int gmax, bool mma);
+// Variants with the append fused in (decode_fused.cu): fp16 / bf16, tensor-
+// core math, D 64 or 128, gmax 8 or 16; nullptr for any other shape.
+const DecodeVariant *find_variant_fused(int dtype, int D, int gmax);
 // 8-bit caches (decode_quant.cu): code_dtype PKV_INT8 / PKV_FP8_E4M3, q in
 // act_dtype PKV_F16 / PKV_BF16, tensor-core math, D = 128, gmax 8 or 16.
 const DecodeVariant *find_variant_quant(int code_dtype, int act_dtype, int D, int gmax);
@@ -114,16 +137,20 @@ size_t flat_workspace_bytes(const FlatGeom &g, int32_t Hq, int32_t num_ctas);
 pkv_status device_error_word(unsigned **out);
 
 // Zero pkv_decode_attention_static's scratch on the current device (after a
-// timed-out wait may have left arrival counters set).
-cudaError_t clear_static_scratch();
+// timed-out wait may have left arrival counters set): ordered on `stream` and
+// complete when it returns.
+cudaError_t clear_static_scratch(cudaStream_t stream);
 
 // Record the text pkv_last_error_message returns on this thread; returns st.
 pkv_status set_last_error(pkv_status st, const char *fmt, ...);
 
+// slot_mapping NULL: token i is the newest of sequence i and goes to the
+// block table's slot of position context_lens[i] - 1 (tables [num_tokens][M]).
 cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
                           const int64_t *slot_mapping, int num_tokens, void *k_pool, void *v_pool,
                           int NB, int Hk, int B, int D, int inputs_ready, unsigned *err,
-                          cudaStream_t st);
+                          cudaStream_t st, const int32_t *tables = nullptr,
+                          const int32_t *lens = nullptr, int M = 0);
 
 // 8-bit caches (append_quant.cu): D = 128.
 cudaError_t launch_append_quant(int code_dtype, int act_dtype, const void *k_new,
