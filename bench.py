@@ -559,10 +559,11 @@ class PoolsFlat:
 
 class PoolsPrefix(Pools16):
     """A 16-bit paged cache decoded prefix-aware: all sequences form one group
-    sharing the prefix blocks they still hold in common."""
+    sharing the prefix blocks they still hold in common (one launch of
+    pkv_decode_attention_prefix after the separate append)."""
 
     def __init__(self, kp, vp, shared_blocks):
-        super().__init__(kp, vp)
+        super().__init__(kp, vp, fused=False)
         self.shared_blocks = shared_blocks
 
     def clone(self):
@@ -575,25 +576,18 @@ class PoolsPrefix(Pools16):
                  pending_tail=0):
         from paged_kv_cache_47_gb300 import binding
         S = q.shape[0]
-        gos, gpb = [0] * S, [self.shared_blocks]
-        n = binding.prefix_workspace_bytes(self.kp, S, q.shape[1], tables.shape[1], gos, gpb)
-        pws = torch.zeros(n, dtype=torch.uint8, device=q.device)
         app = binding.PreparedAppend(kn, vn, slots, self.kp, self.vp, inputs_ready=True)
-        kp, vp = self.kp, self.vp
-
-        def dec(stream, timing_events=None):
-            s = stream if stream is not None else torch.cuda.current_stream()
-            if timing_events is not None:
-                timing_events[0].record(s)
-            binding.decode_attention_prefix(q, kp, vp, tables, lens, scale, gos, gpb, out=out,
-                                            workspace=pws, stream=s)
-            if timing_events is not None:
-                timing_events[1].record(s)
+        dec = binding.PreparedDecodePrefix(q, self.kp, self.vp, tables, lens, scale, [0] * S,
+                                           [self.shared_blocks], out=out, tables_ready=True,
+                                           consumer=consumer)
         return app, dec
 
 
 # ------------------------------------------------------------------ other workloads
-SWEEP = [(0, None), (2, None), (3, None), (4, 8), (4, 16), (4, 32)]
+# (workload, block size override, largest suffix override, prefix-aware decode)
+SWEEP = [(0, None, None, False), (2, None, None, False), (3, None, None, False),
+         (3, None, None, True), (3, None, 500, False), (3, None, 500, True),
+         (4, 8, None, False), (4, 16, None, False), (4, 32, None, False)]
 TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
 
 
@@ -607,10 +601,13 @@ def workload_sweep(args, dev, peak):
     from oracle import oracle
     from paged_kv_cache_47_gb300 import binding
 
+    from dataclasses import replace
     steps = max(args.steps, 10)
     res = []
-    for idx, B in SWEEP:
+    for idx, B, suffix_hi, prefix_aware in SWEEP:
         spec = W.SPECS[idx] if B is None else W.SPECS[idx].with_block_size(B)
+        if suffix_hi is not None:
+            spec = replace(spec, suffix_hi=suffix_hi)
         st = W.make_structure(spec, args.seed)
         vals = W.make_values(st, args.seed, device=dev)
         h = {k: v.cpu() for k, v in vals.items()}      # the pre-step state, for the oracle
@@ -619,7 +616,13 @@ def workload_sweep(args, dev, peak):
         slots = st.slot_mapping.to(dev)
         S, Hq, D = vals["q"].shape
         scale = 1.0 / math.sqrt(spec.head_dim)
-        pools = Pools16(vals["k_pool"], vals["v_pool"])
+        if prefix_aware:
+            # after the copy-on-write the last prefix block is private to all
+            # but one holder: the group shares the blocks before it
+            pools = PoolsPrefix(vals["k_pool"], vals["v_pool"],
+                                spec.shared_prefix // spec.block_size - (1 if cow is not None else 0))
+        else:
+            pools = Pools16(vals["k_pool"], vals["v_pool"])
         out = torch.empty(S, Hq, D, dtype=vals["q"].dtype, device=dev)
         ws = pools.workspace(Hq)
         # one cache copy: each step's append rewrites the same last row, so the
@@ -676,7 +679,11 @@ def workload_sweep(args, dev, peak):
         got = out.double().cpu().numpy()
         err = float(abs(got - ref).max()) if got.size else 0.0
         res.append({
-            "workload": spec.name, "block_size": spec.block_size, "kv_dtype": spec.dtype,
+            "workload": spec.name + (f" (suffix U[{spec.suffix_lo},{spec.suffix_hi}])"
+                                     if suffix_hi is not None else ""),
+            "decode": "prefix-aware (pkv_decode_attention_prefix)" if prefix_aware else
+                      ("pkv_append_decode_attention" if pools.fused else "plain"),
+            "block_size": spec.block_size, "kv_dtype": spec.dtype,
             "num_seqs": S, "q_heads": Hq, "kv_heads": spec.num_kv_heads,
             "context_tokens": int(st.context_lens.sum()),
             "step_us": round(step_ms * 1000, 2),
@@ -924,9 +931,9 @@ def run_ours(args):
                                                   args.prefix_aware),
                                      inputs_ready=not (args.kv_quant or args.flat),
                                      fused=fused),
-                   **({"decode": "prefix-aware: the shared prefix decoded once for all "
-                                 "sharers' heads, suffixes apart, log-sum-exp merge "
-                                 "(pkv_decode_attention_prefix; 5 launches)"}
+                   **({"decode": "prefix-aware: the shared prefix decoded once per unit of "
+                                 "several sharers' heads, each suffix apart, merged by "
+                                 "log-sum-exp in the same launch (pkv_decode_attention_prefix)"}
                       if args.prefix_aware else {}),
                    **({"kv_cache": "flat spans: one virtual range per sequence, physical "
                                    "chunks mapped on demand (pkv_flat_*)",
@@ -950,11 +957,9 @@ def run_ours(args):
         "roofline": roofline,
         "other_kernels": side or None,
         "block_manager": time_block_manager(st, spec) if rank == 0 else None,
-        # the fused step is one launch; otherwise append + decode; the
-        # prefix-aware decode is five launches: q gather, suffix tables, prefix
-        # decode, suffix decode, merge; plus the copy-on-write launch
-        "gpu_launches": ((1 if fused else 1 + (5 if args.prefix_aware else 1)) +
-                         (1 if cow is not None else 0)) * args.steps,
+        # the fused step is one launch; otherwise append + decode (the
+        # prefix-aware decode is one launch too); plus the copy-on-write launch
+        "gpu_launches": ((1 if fused else 2) + (1 if cow is not None else 0)) * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
         "host_enqueue_s": round(enqueue_s, 4),

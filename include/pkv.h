@@ -345,11 +345,12 @@ pkv_status pkv_block_copy(const pkv_cache_desc *cache, const int64_t *src_dst_pa
  * Passage: identical prompt prefixes are stored once and shared by every
  * request holding them ("KV-Cache Optimization & PagedAttention for
  * Long-Context Agents", section "Key KV-Cache Optimization Principles", item
- * 3). pkv_decode_attention_prefix reads them once per 8 of the group's
- * sharers' query heads under each kv head instead of once per sequence: the
- * prefix is attended for the sharers' heads together, each sequence's private
- * suffix on its own, and the two partial attentions are merged by
- * log-sum-exp. The result is the plain decode's, up to rounding.
+ * 3). pkv_decode_attention_prefix decodes a group's shared prefix once per
+ * unit of several sharers' query heads (8 or 16 heads a unit: 8 / G members
+ * for G q heads per kv head) instead of once per sequence, each sequence's
+ * private suffix on its own, and merges the two partial attentions by
+ * log-sum-exp, all in one launch of the split-K kernel. The result is the
+ * plain decode's, up to rounding.
  */
 typedef struct {
     int32_t num_groups;
@@ -369,11 +370,16 @@ size_t pkv_decode_prefix_workspace_bytes(const pkv_cache_desc *cache, int32_t nu
 
 /*
  * pkv_decode_attention_ex for sequences that share prefixes: same inputs and
- * output, plus the group description. workspace: at least
- * pkv_decode_prefix_workspace_bytes, zero-filled before its first use. The
- * call enqueues a few kernels and copies its small index arrays from the host
- * (so it is not capturable in a CUDA graph). options: num_ctas and consumer
- * apply to each decode; timing_events and lse_out are ignored.
+ * output, plus the group description (host arrays, read during the call).
+ * workspace: at least pkv_decode_prefix_workspace_bytes, zero-filled before
+ * its first use; every call leaves its counters zero again. One launch, no
+ * host-to-device copy. options: num_ctas (at most PKV_MAX_DECODE_CTAS / 2),
+ * consumer, tables_ready, lse_out and timing_events apply; pending_tail is
+ * ignored (every read waits for the preceding kernel). The one launch covers
+ * fp16 / bf16 caches on the tensor-core math whose q heads per kv head times
+ * head_dim is a multiple of 128, and batches whose sequences plus prefix
+ * units number at most 1024; any other call is served by the plain decode,
+ * with the same result.
  */
 pkv_status pkv_decode_attention_prefix(const pkv_cache_desc *cache, const void *q,
                                        int32_t num_seqs, int32_t num_q_heads, const void *k_pool,

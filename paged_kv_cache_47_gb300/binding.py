@@ -844,26 +844,59 @@ def decode_attention_prefix(q, k_pool, v_pool, block_tables, context_lens, scale
                             out: Optional[torch.Tensor] = None,
                             out_dtype: Optional[torch.dtype] = None,
                             workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
-                            stream=None) -> torch.Tensor:
+                            stream=None, lse_out: Optional[torch.Tensor] = None,
+                            tables_ready: bool = False, consumer: int = 0) -> torch.Tensor:
     """Decode where the sequences of each group share their first
     group_prefix_blocks[g] table entries (group_of_seq[s] = g, or -1)."""
-    desc = _pools(k_pool, v_pool)
-    S, Hq, D = q.shape
-    q = q.contiguous()
-    bt, cl = block_tables.contiguous(), context_lens.contiguous()
-    g = _Groups(group_of_seq, group_prefix_blocks)
-    if out is None:
-        out = torch.empty(S, Hq, D, dtype=out_dtype or q.dtype, device=q.device)
-    if workspace is None:
-        n = prefix_workspace_bytes(k_pool, S, Hq, bt.shape[1], group_of_seq, group_prefix_blocks,
-                                   num_ctas)
-        if n == 0:
-            raise PkvError(-1, lib().pkv_last_error_message().decode())
-        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
-    opts = DecodeOptions()
-    opts.num_ctas = num_ctas
-    _check(lib().pkv_decode_attention_prefix(
-        ctypes.byref(desc), _ptr(q), S, Hq, _ptr(k_pool), _ptr(v_pool), _ptr(bt), bt.shape[1],
-        _ptr(cl), float(scale), ctypes.byref(g.st), _ptr(out), DTYPE_CODE[out.dtype],
-        _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts)))
-    return out
+    return PreparedDecodePrefix(q, k_pool, v_pool, block_tables, context_lens, scale,
+                                group_of_seq, group_prefix_blocks, out=out, out_dtype=out_dtype,
+                                workspace=workspace, num_ctas=num_ctas, lse_out=lse_out,
+                                tables_ready=tables_ready, consumer=consumer)(stream)
+
+
+class PreparedDecodePrefix:
+    """A pkv_decode_attention_prefix call whose arguments (and group arrays)
+    are marshalled once; each call passes the stream (see PreparedDecode)."""
+
+    def __init__(self, q, k_pool, v_pool, block_tables, context_lens, scale: float,
+                 group_of_seq, group_prefix_blocks, out: Optional[torch.Tensor] = None,
+                 out_dtype: Optional[torch.dtype] = None,
+                 workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                 lse_out: Optional[torch.Tensor] = None, tables_ready: bool = False,
+                 consumer: int = 0):
+        self._desc = _pools(k_pool, v_pool)
+        S, Hq, D = q.shape
+        q = q.contiguous()
+        bt, cl = block_tables.contiguous(), context_lens.contiguous()
+        assert bt.dtype == torch.int32 and cl.dtype == torch.int32 and q.dtype == k_pool.dtype
+        self._g = _Groups(group_of_seq, group_prefix_blocks)
+        if out is None:
+            out = torch.empty(S, Hq, D, dtype=out_dtype or q.dtype, device=q.device)
+        if workspace is None:
+            n = prefix_workspace_bytes(k_pool, S, Hq, bt.shape[1], group_of_seq,
+                                       group_prefix_blocks, num_ctas)
+            if n == 0:
+                raise PkvError(-1, lib().pkv_last_error_message().decode())
+            workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+        self._opts = DecodeOptions()
+        self._opts.num_ctas = num_ctas
+        self._opts.consumer = consumer
+        self._opts.tables_ready = int(tables_ready)
+        if lse_out is not None:
+            assert lse_out.dtype == torch.float32 and lse_out.shape == (S, Hq) and lse_out.is_contiguous()
+            self._opts.lse_out = lse_out.data_ptr()
+        self._keep = (q, k_pool, v_pool, bt, cl, out, workspace, lse_out)
+        self._args = (ctypes.byref(self._desc), _ptr(q), S, Hq, _ptr(k_pool), _ptr(v_pool),
+                      _ptr(bt), bt.shape[1], _ptr(cl), float(scale), ctypes.byref(self._g.st),
+                      _ptr(out), DTYPE_CODE[out.dtype], _ptr(workspace), workspace.numel())
+        self._fn = lib().pkv_decode_attention_prefix
+        self.out = out
+        self.workspace = workspace
+
+    def __call__(self, stream=None, timing_events: Optional[Sequence] = None) -> torch.Tensor:
+        opts = self._opts
+        for i in range(2):
+            ev = timing_events[i] if timing_events is not None else None
+            opts.timing_events[i] = None if ev is None else ev.cuda_event
+        _check(self._fn(*self._args, _stream(stream), ctypes.byref(opts)))
+        return self.out

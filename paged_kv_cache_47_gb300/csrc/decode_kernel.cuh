@@ -71,7 +71,10 @@ constexpr int tile_tokens(int QK, int GMAX) { return big_tiles(QK, GMAX) ? 128 :
 constexpr int math_warps(int QK, int GMAX) { return big_tiles(QK, GMAX) ? 8 : kConsumerWarps; }
 constexpr int kernel_threads(int QK, int GMAX) { return 32 * (math_warps(QK, GMAX) + kProducerWarps); }
 
-template <typename T, int D, int GMAX, bool MMA, int QK = 0, bool FUSED = false>
+// Pending final arrivals a merge-slice warp can hold (prefix-aware variants).
+constexpr int kFinCap = 32;
+
+template <typename T, int D, int GMAX, bool MMA, int QK = 0, bool FUSED = false, bool PFX = false>
 struct SplitCfg {
     static constexpr int ES = QK ? 1 : (int)sizeof(T);  // bytes of one cache element
     static constexpr int ROWB = D * ES;              // bytes of one K or V row
@@ -91,10 +94,12 @@ struct SplitCfg {
     static constexpr int COMB_O = CW * GMAX * D * 4;
     static constexpr int COMB_ML = 2 * CW * GMAX * 4;
     static constexpr int PBUF = MMA ? CW * NTN * 2 * 256 : 0;
-    static constexpr int SEQ_MAX = (2 * kMaxSeqsPerLaunch + 1) * 4;
+    // work sequences: tile prefix and length (and, prefix-aware, the table offset)
+    static constexpr int SEQ_MAX = (2 * kMaxSeqsPerLaunch + 1) * 4 + (PFX ? kMaxPrefixWork * 6 : 0);
+    static constexpr int FINB = PFX ? kMergeSlices * kFinCap * 4 : 0;
     static constexpr int SMEM_LIMIT = 227 * 1024;
     static constexpr int PER_STAGE_EXTRA = (int)sizeof(TileMeta) + 16;  // meta + 2 barriers
-    static constexpr int FIXED = 1024 /*alignment slack*/ + COMB_O + COMB_ML + PBUF +
+    static constexpr int FIXED = 1024 /*alignment slack*/ + COMB_O + COMB_ML + PBUF + FINB +
                                  16 /*comb bars*/ + SEQ_MAX + 64;
     static constexpr int NST_FIT = (SMEM_LIMIT - FIXED) / (STAGE + PER_STAGE_EXTRA);
     static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
@@ -111,9 +116,14 @@ struct SplitCfg {
     static constexpr int OFF_COMB_M = OFF_COMB_O + COMB_O;
     static constexpr int OFF_COMB_L = OFF_COMB_M + CW * GMAX * 4;
     static constexpr int OFF_PBUF = OFF_COMB_L + CW * GMAX * 4;
-    static constexpr int OFF_SEQ = OFF_PBUF + PBUF;
+    static constexpr int OFF_FIN = OFF_PBUF + PBUF;
+    static constexpr int OFF_SEQ = OFF_FIN + FINB;
 
-    static size_t smem_bytes(int S) { return 1024 + OFF_SEQ + (size_t)(2 * S + 1) * 4; }
+    // W work sequences (the batch, plus the virtual prefix ones when prefix-aware,
+    // with their table offsets and the member list)
+    static size_t smem_bytes(int W) {
+        return 1024 + OFF_SEQ + (size_t)(2 * W + 1) * 4 + (PFX ? (size_t)W * 6 + 4 : 0);
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -121,13 +131,22 @@ struct SplitCfg {
 // ---------------------------------------------------------------------------
 // seq_len[s]   = context length clamped to [0, M*B] (a clamp flags the error word)
 // seq_prefix[s]= U * sum_{s'<s} ceil(seq_len[s'] / 64), seq_prefix[S] = NT
+// Prefix-aware launches (PFX): W = nv + S work sequences; virtual w < nv spans
+// its group's prefix, real w = nv + s the context of s past its group's
+// prefix (a context shorter than the prefix flags the error word and counts
+// 0); seq_tab[w] is the offset of the work sequence's first table entry.
+// members[] (the sequence ids of the prefix units) is copied to shared memory.
 // Ends with __syncthreads(); all threads of the block must call it.
-template <bool FLAT, int TT>
-__device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq_prefix,
-                                                 int *seq_len, bool report) {
+template <bool FLAT, int TT, bool PFX = false, typename PM = NoPrefixMap>
+__device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int W, int *seq_prefix,
+                                                 int *seq_len, bool report, const PM &pm = PM{},
+                                                 int *seq_tab = nullptr,
+                                                 int16_t *members = nullptr) {
     const int tid = threadIdx.x;
     const int max_len = p.M * p.B;
-    for (int s = tid; s < p.S; s += blockDim.x) {
+    if constexpr (PFX)
+        for (int i = tid; i < p.S; i += blockDim.x) members[i] = pm.members[i];
+    for (int s = tid; s < W; s += blockDim.x) {
         int bad = 0;
         int L;
         if constexpr (FLAT) {
@@ -139,6 +158,17 @@ __device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq
             } else {
                 L = pkv_clamp_len(p.context_lens[s], min(max_len, p.committed[slot]), &bad);
             }
+        } else if constexpr (PFX) {
+            const PrefixWork wk = pm.w[s];
+            if (s < pm.nv) {
+                L = wk.blocks * p.B;
+            } else {
+                const int Lc = pkv_clamp_len(p.context_lens[s - pm.nv], max_len, &bad);
+                const int sh = wk.blocks * p.B;
+                if (Lc < sh) bad = 1;
+                L = Lc < sh ? 0 : Lc - sh;
+            }
+            seq_tab[s] = wk.row * p.M + (s < pm.nv ? 0 : wk.blocks);
         } else {
             L = pkv_clamp_len(p.context_lens[s], max_len, &bad);
         }
@@ -149,19 +179,19 @@ __device__ __forceinline__ void build_seq_arrays(const DecodeParams &p, int *seq
     if (tid < 32) {
         const int lane = tid;
         int running = 0;
-        for (int base = 0; base < p.S; base += 32) {
+        for (int base = 0; base < W; base += 32) {
             const int s = base + lane;
-            const int n = (s < p.S) ? pkv_tiles_of_len(seq_len[s], TT) * p.U : 0;
+            const int n = (s < W) ? pkv_tiles_of_len(seq_len[s], TT) * p.U : 0;
             int incl = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 int v = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += v;
             }
-            if (s < p.S) seq_prefix[s] = running + incl - n;
+            if (s < W) seq_prefix[s] = running + incl - n;
             running += __shfl_sync(0xffffffffu, incl, 31);
         }
-        if (lane == 0) seq_prefix[p.S] = running;
+        if (lane == 0) seq_prefix[W] = running;
     }
     __syncthreads();
 }
@@ -755,14 +785,154 @@ struct Consumer<T, D, GMAX, true, QK> {
 //     lse = log2 sum_p 2^{lse_p},   out = sum_p 2^{lse_p - lse} o_p,
 // taken in CTA order with a running maximum (one pass). Loads bypass L1: the
 // other CTAs' slices were written during this launch.
+// Where a unit's results go. Plain launches: the out rows of sequence s.
+// Prefix-aware launches: head j of a prefix unit belongs to member
+// members[m0 + j / G] (head h0 + j % G) and goes to that member's prefix
+// result row, or straight to out when the member's context ends with the
+// prefix; a grouped sequence's own unit goes to its suffix result rows.
+struct UnitDest {
+    int kind;   // 0 out rows of sequence s, 1 prefix unit (members), 2 suffix rows of s
+    int s;      // kinds 0, 2
+    int m0;     // kind 1
+};
+
+// Store element (head j, d) of a unit's result and its head's log2-sum-exp2:
+// for out, with the element d == 0; for a result row, one copy per merge
+// slice (elements idx = j D + d with idx % 128 in [32 w, 32 w + 32) form slice
+// w), written with the slice's first element of the head, so that the slice's
+// merge needs nothing another warp wrote.
+template <int D>
+__device__ __forceinline__ void put_result(const DecodeParams &p, const UnitDest &u, int h0, int j,
+                                           int d, float o, float lse, const int16_t *members,
+                                           const int *seq_len, int nv) {
+    int s = u.s, h = h0 + j, dest = u.kind;
+    if (u.kind == 1) {
+        s = members[u.m0 + j / p.G];
+        h = h0 + j % p.G;
+        dest = seq_len[nv + s] == 0 ? 0 : 1;
+    }
+    const size_t row = (size_t)s * p.Hq + h;
+    if (dest == 0) {
+        store_out(p.out, row * D + d, p.out_dtype, o);
+        if (p.lse_out && d == 0) p.lse_out[row] = lse;
+    } else {
+        const size_t r = (size_t)(dest - 1) * p.S * p.Hq + row;
+        p.pb.res_o[r * D + d] = o;
+        if ((d & 31) == 0) p.pb.res_l[r * kMergeSlices + (((j * D + d) & 127) >> 5)] = lse;
+    }
+}
+
+// Count this warp's pending result slices: slice `warp` of each (sequence,
+// kv head) entry of its list (elements idx = 32 warp + lane + 128 k of the
+// kv group's G x D outputs). A slice whose count reaches 2 (the prefix
+// result's and the suffix result's slice are in) is merged by this warp into
+// out: out = (2^{l_P} o_P + 2^{l_S} o_S) / (2^{l_P} + 2^{l_S}), up to 16
+// elements per lane with their loads in flight together.
+template <int D>
+__device__ __forceinline__ void flush_final(const DecodeParams &p, int *list, int &n, int warp,
+                                            int lane) {
+    __syncwarp();
+    const int e = lane < n ? list[lane] : 0;
+    fence_acq_rel_gpu();
+    unsigned prev = 0u;
+    unsigned *cnt = p.pb.fin + (size_t)e * kMergeSlices + warp;
+    if (lane < n) prev = atomicAdd(cnt, 1u);
+    fence_acq_rel_gpu();
+    const bool mine = lane < n && prev == 1u;
+    const unsigned done = __ballot_sync(0xffffffffu, mine);
+    __syncwarp();
+    if (mine) {
+        *cnt = 0u;   // both arrivals are in: reset for the next call
+        // the finished entries' first output rows, compacted into the list
+        const int sq = e / p.Hk, g = e - (e / p.Hk) * p.Hk;
+        list[__popc(done & ((1u << lane) - 1u))] = sq * p.Hq + g * p.G;
+    }
+    __syncwarp();
+    const int GD = p.G * D;
+    const int ksv = (GD - 32 * warp + 127) / 128;   // this slice's elements per lane (at most)
+    const int total = __popc(done) * ksv;
+    const size_t plane = (size_t)p.S * p.Hq;
+    for (int i0 = 0; i0 < total; i0 += 16) {
+        float lp[16], ls[16], op[16], os[16];
+        size_t row[16];
+        int dd[16];
+        bool ok[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const int it = i0 + t;
+            const int b = it < total ? it / ksv : 0, k = it - b * ksv;
+            const int idx = 32 * warp + lane + 128 * k;
+            ok[t] = it < total && idx < GD;
+            const int j = idx / D;
+            dd[t] = idx - j * D;
+            row[t] = (size_t)list[b] + j;
+            if (ok[t]) {
+                lp[t] = __ldcg(p.pb.res_l + row[t] * kMergeSlices + warp);
+                ls[t] = __ldcg(p.pb.res_l + (plane + row[t]) * kMergeSlices + warp);
+                op[t] = __ldcg(p.pb.res_o + row[t] * D + dd[t]);
+                os[t] = __ldcg(p.pb.res_o + (plane + row[t]) * D + dd[t]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            if (!ok[t]) continue;
+            const float m = fmaxf(lp[t], ls[t]);
+            const float wp = exp2f(lp[t] - m), ws = exp2f(ls[t] - m);
+            store_out(p.out, row[t] * D + dd[t], p.out_dtype, (wp * op[t] + ws * os[t]) / (wp + ws));
+            if (p.lse_out && dd[t] == 0) p.lse_out[row[t]] = m + log2f(wp + ws);
+        }
+    }
+    __syncwarp();
+    n = 0;
+}
+
+// Note the (sequence, kv head) entries whose prefix or suffix result this
+// warp has just written a slice of.
+template <int D>
+__device__ __forceinline__ void note_final(const DecodeParams &p, const UnitDest &u, int h0,
+                                           int gca, const int16_t *members, const int *seq_len,
+                                           int nv, int *list, int &n, int warp, int lane) {
+    const int g = h0 / p.G;
+    const int cnt = u.kind == 1 ? gca / p.G : 1;
+    for (int m = 0; m < cnt; ++m) {
+        const int s = u.kind == 1 ? members[u.m0 + m] : u.s;
+        if (u.kind == 1 && seq_len[nv + s] == 0) continue;   // written to out directly
+        if (lane == 0) list[n] = s * p.Hk + g;
+        if (++n == kFinCap) flush_final<D>(p, list, n, warp, lane);
+    }
+}
+
 // A cut segment waiting to be counted, with the facts of its unit's split
 // (computed when the segment ends, so that the CTA's last moments do no
 // 64-bit divisions): the CTAs c_first .. c_last holding its partials, their
 // number, and the partial slot of CTA c_first.
+// The work list may have two sections (prefix-aware launches: the prefix
+// units, then every sequence's own units), each split over the C CTAs on its
+// own, so that every CTA gets an equal share of both kinds of tile. Section k
+// covers tiles [base, base + nt); a CTA's partial slots 2k and 2k + 1 serve
+// it, and its arrival counters follow those of section 0 (c + k C).
 struct PendSeg {
     TileMeta mt;
     int c_first, c_last, parts, slot_first;
 };
+// prefix-aware launches also keep the unit's section and where its results go
+struct PendSegPfx : PendSeg {
+    int sec;        // section of the unit
+    int64_t nt;     // tiles of that section
+    UnitDest ud;
+};
+template <bool PFX>
+using PendSegT = typename std::conditional<PFX, PendSegPfx, PendSeg>::type;
+
+// section of global tile tau: NT0 tiles in section 0 when there are two
+// sections (NT0 > 0), else one section of NT tiles
+__device__ __forceinline__ int section_of(int64_t tau, int64_t NT0, int64_t NT, int64_t &base,
+                                          int64_t &nt) {
+    const int k = (NT0 > 0 && tau >= NT0) ? 1 : 0;
+    base = k ? NT0 : 0;
+    nt = NT0 > 0 ? (k ? NT - NT0 : NT0) : NT;
+    return k;
+}
 
 __device__ __forceinline__ PendSeg pend_seg(const TileMeta &mt, int C, int64_t NT) {
     PendSeg ps;
@@ -774,9 +944,32 @@ __device__ __forceinline__ PendSeg pend_seg(const TileMeta &mt, int C, int64_t N
     return ps;
 }
 
-template <int D, int GMAX>
-__device__ __forceinline__ void merge_slice(const DecodeParams &p, const PendSeg &ps, int warp,
-                                            int lane, int64_t NT) {
+__device__ __forceinline__ PendSegPfx pend_seg_pfx(const TileMeta &mt, int C, int64_t NT0,
+                                                   int64_t NT, const UnitDest &ud) {
+    PendSegPfx ps;
+    ps.mt = mt;
+    ps.ud = ud;
+    int64_t base, nt;
+    ps.sec = section_of(mt.tu, NT0, NT, base, nt);
+    ps.nt = nt;
+    const int64_t tu = mt.tu - base;
+    ps.c_first = pkv_owner(tu, C, nt);
+    ps.c_last = pkv_owner(tu + mt.nu - 1, C, nt);
+    ps.parts = pkv_unit_parts(tu, mt.nu, C, nt);
+    ps.slot_first = pkv_partial_slot(ps.c_first, C, nt, tu) + 2 * ps.sec;
+    return ps;
+}
+
+template <int D, int GMAX, int SLOTS, bool PFX>
+__device__ __forceinline__ void merge_slice(const DecodeParams &p, const PendSegT<PFX> &ps,
+                                            int warp, int lane, int64_t NT_all,
+                                            const int16_t *members, const int *seq_len, int nv) {
+    int64_t NT = NT_all;
+    int sec = 0;
+    if constexpr (PFX) {
+        NT = ps.nt;
+        sec = ps.sec;
+    }
     const TileMeta &mt = ps.mt;
     const int c_first = ps.c_first;
     // the lane's elements are idx = warp*32 + lane + 128k, k < EPL, taken in
@@ -802,7 +995,7 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const PendSeg
 #pragma unroll 2
         for (int c = c_first; c <= c_last; ++c) {
             if (some_empty && pkv_cta_empty(c, C, NT)) continue;
-            const int slot = c * 2 + (c == c_first ? slot_first : 0);
+            const int slot = c * SLOTS + (c == c_first ? slot_first : 2 * sec);
             // lane h < gca fetches this warp's copy of head h's lse
             const float lse_h =
                 lane < mt.gca ? __ldcg(p.ws_lse + (slot * kMergeSlices + warp) * p.GC + lane)
@@ -831,10 +1024,15 @@ __device__ __forceinline__ void merge_slice(const DecodeParams &p, const PendSeg
             const int idx = warp * 32 + lane + (k0 + k) * kMergeSlices * 32;
             if (idx < n_el) {
                 const int j = idx / D, d = idx - (idx / D) * D;
-                store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype,
-                          O[k] / W[k]);
-                if (p.lse_out && d == 0)
-                    p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + j] = Mx[k] + log2f(W[k]);
+                if constexpr (PFX) {
+                    put_result<D>(p, ps.ud, mt.h0, j, d, O[k] / W[k], Mx[k] + log2f(W[k]),
+                                  members, seq_len, nv);
+                } else {
+                    store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype,
+                              O[k] / W[k]);
+                    if (p.lse_out && d == 0)
+                        p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + j] = Mx[k] + log2f(W[k]);
+                }
             }
         }
     }
@@ -854,6 +1052,34 @@ __device__ __noinline__ void copy_new_row(uint32_t side, const void *k_new, cons
     const uint8_t *vn = static_cast<const uint8_t *>(v_new) + row * ROWB;
     for (int i = tb; i < 2 * CPR; i += tpb)
         cp_async_16(side + i * 16, i < CPR ? kn + i * 16 : vn + (i - CPR) * 16, valid);
+}
+
+// ---------------------------------------------------------------------------
+// prefix-aware: the producers' jump to their range of the second section
+// ---------------------------------------------------------------------------
+// Out of line: the issue loop is unrolled and its code size shows in the
+// instruction fetch.
+static __device__ __noinline__ void cursor_jump(PkvCursor &c, int64_t tau, const int *seq_prefix,
+                                                const int *seq_len, int W, int tt) {
+    pkv_cursor_at(c, tau, seq_prefix, seq_len, W, tt);
+}
+
+// ---------------------------------------------------------------------------
+// prefix-aware: the q rows of a prefix unit
+// ---------------------------------------------------------------------------
+// Row j of the unit is head h0 + j % G of member j / G (a sequence id from
+// `members`); rows are QROWB bytes, copied in 16-byte chunks by the producer
+// threads.
+template <int QROWB>
+__device__ __noinline__ void copy_q_members(uint32_t sQ, const void *q, const int16_t *members,
+                                            int G, int Hq, int h0, int rows, int pt) {
+    constexpr int CPRQ = QROWB / 16;
+    const uint8_t *qb = static_cast<const uint8_t *>(q);
+    for (int i = pt; i < rows * CPRQ; i += kProducerThreads) {
+        const int j = i / CPRQ, c = i - (i / CPRQ) * CPRQ;
+        const size_t row = (size_t)members[j / G] * Hq + h0 + j % G;
+        cp_async_16(sQ + i * 16, qb + row * QROWB + c * 16, true);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -915,10 +1141,12 @@ __device__ __forceinline__ void fused_append_rows(const DecodeParams &p, const i
 // ---------------------------------------------------------------------------
 // the split-K kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA, int QK, bool FLAT, bool FUSED>
+template <typename T, int D, int GMAX, bool MMA, int QK, bool FLAT, bool FUSED, bool PFX>
 __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
-    decode_split_kernel(const DecodeParams p) {
-    using Cfg = SplitCfg<T, D, GMAX, MMA, QK, FUSED>;
+    decode_split_kernel(const DecodeParams p,
+                        const typename std::conditional<PFX, PrefixMap, NoPrefixMap>::type pm) {
+    using Cfg = SplitCfg<T, D, GMAX, MMA, QK, FUSED, PFX>;
+    static_assert(!PFX || (MMA && QK == 0 && !FLAT && !FUSED), "prefix-aware: 16-bit paged mma");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -931,8 +1159,14 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     float *comb_o = reinterpret_cast<float *>(smem + Cfg::OFF_COMB_O);
     float *comb_m = reinterpret_cast<float *>(smem + Cfg::OFF_COMB_M);
     float *comb_l = reinterpret_cast<float *>(smem + Cfg::OFF_COMB_L);
+    // work sequences: the batch, preceded (prefix-aware) by the virtual prefix ones
+    int nv = 0;
+    if constexpr (PFX) nv = pm.nv;
+    const int W = nv + p.S;
     int *seq_prefix = reinterpret_cast<int *>(smem + Cfg::OFF_SEQ);
-    int *seq_len = seq_prefix + p.S + 1;
+    int *seq_len = seq_prefix + W + 1;
+    int *seq_tab = seq_len + W;                       // prefix-aware only
+    int16_t *members = reinterpret_cast<int16_t *>(seq_tab + W);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int cta = blockIdx.x, C = p.C;
@@ -952,12 +1186,19 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     // are read (and the first table entries fetched) while that kernel runs,
     // and the wait comes just before q, the pools or any output is touched.
     if (!p.tables_ready) grid_dependency_wait();
-    build_seq_arrays<FLAT, Cfg::TT>(p, seq_prefix, seq_len, cta == 0);
+    if constexpr (PFX)
+        build_seq_arrays<FLAT, Cfg::TT, true>(p, W, seq_prefix, seq_len, cta == 0, pm, seq_tab,
+                                              members);
+    else
+        build_seq_arrays<FLAT, Cfg::TT>(p, W, seq_prefix, seq_len, cta == 0);
 
-    // zero-length sequences: zeros, written by CTA s % C
+    // zero-length sequences: zeros, written by CTA s % C (prefix-aware: not
+    // the members of a group, whose output comes at least from the prefix)
     bool waited = !p.tables_ready;
     for (int s = 0; s < p.S; ++s) {
-        if (seq_len[s] == 0 && s % C == cta) {
+        bool empty = seq_len[nv + s] == 0;
+        if constexpr (PFX) empty = empty && pm.w[nv + s].blocks == 0;
+        if (empty && s % C == cta) {
             if (!waited) {   // the same for the whole CTA
                 grid_dependency_wait();
                 waited = true;
@@ -970,9 +1211,17 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         }
     }
 
-    const int64_t NT = seq_prefix[p.S];
-    const int64_t t_begin = NT ? pkv_split(cta, C, NT) : 0, t_end = NT ? pkv_split(cta + 1, C, NT) : 0;
-    const int n_my = (int)(t_end - t_begin);
+    // this CTA's tiles: [b0, e0) of section 0 (prefix-aware: the prefix
+    // units, NT0 tiles) and [b1, e1) of the rest; one section otherwise
+    const int64_t NT = seq_prefix[W];
+    const int64_t NT0 = PFX ? seq_prefix[nv] : 0, NT1 = NT - NT0;
+    const int64_t b0 = NT0 ? pkv_split(cta, C, NT0) : 0, e0 = NT0 ? pkv_split(cta + 1, C, NT0) : 0;
+    const int64_t b1 = NT0 + (NT1 ? pkv_split(cta, C, NT1) : 0);
+    const int64_t e1 = NT0 + (NT1 ? pkv_split(cta + 1, C, NT1) : 0);
+    const int n0 = (int)(e0 - b0);
+    const int n_my = n0 + (int)(e1 - b1);
+    const int64_t t_begin = n0 ? b0 : b1;
+    constexpr int SLOTS = PFX ? 4 : 2;   // partial slots per CTA: two per section
     grid_dependents_launch();   // the next kernel on the stream may start its launch now
     if (n_my <= 0) return;
 
@@ -1001,8 +1250,14 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         const uint8_t *kpool = static_cast<const uint8_t *>(p.kp);
         const uint8_t *vpool = FLAT ? kpool + p.v_off : static_cast<const uint8_t *>(p.vp);
         PkvCursor cur, la;
-        pkv_cursor_at(cur, t_begin, seq_prefix, seq_len, p.S, Cfg::TT);
+        pkv_cursor_at(cur, t_begin, seq_prefix, seq_len, W, Cfg::TT);
         la = cur;
+        // prefix-aware: the cursors jump from section 0's range to section 1's
+        int la_it = 0;
+        auto advance = [&](PkvCursor &c, int next_it) {
+            if (PFX && next_it == n0) cursor_jump(c, b1, seq_prefix, seq_len, W, Cfg::TT);
+            else pkv_cursor_next(c, seq_len, W, p.U, Cfg::TT);
+        };
         // per tile: the physical block of this thread's rows, or (flat
         // spans) the sequence's slot
         // 8-bit caches: the pools stream through L2 once per call, so their
@@ -1010,10 +1265,15 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         // the 16-bit step, which overlaps the next call's start with this
         // one's end, 0.7 % slower, so 16-bit copies keep the default policy)
         const uint64_t pol_stream = QK != 0 ? l2_policy_evict_first() : 0ull;
+        // prefix-aware: a shared prefix is read by every chunk of its sharers'
+        // heads, so its lines are kept (evict_last) and the rest stream by
+        const uint64_t pol_keep = PFX ? l2_policy_evict_last() : 0ull;
+        const uint64_t pol_pass = PFX ? l2_policy_evict_normal() : 0ull;
         auto load_entry = [&](const PkvCursor &c) -> int {
             const int ntok = min(Cfg::TT, c.L - c.ti * Cfg::TT);
             if (jblk * p.B >= ntok) return -1;
             if constexpr (FLAT) return __ldg(p.slots + c.s);
+            if constexpr (PFX) return __ldg(p.block_tables + seq_tab[c.s] + c.ti * bpt + jblk);
             return __ldg(p.block_tables + (size_t)c.s * p.M + c.ti * bpt + jblk);
         };
         int ent[LA];
@@ -1022,7 +1282,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
             ent[k] = -1;
             if (k < n_my) {
                 ent[k] = load_entry(la);
-                pkv_cursor_next(la, seq_len, p.S, p.U, Cfg::TT);
+                advance(la, ++la_it);
             }
         }
         // before the first q or pool byte; with pending_tail, q and the rows
@@ -1066,7 +1326,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 const int e = ent[k];
                 if (it + LA < n_my) {
                     ent[k] = load_entry(la);
-                    pkv_cursor_next(la, seq_len, p.S, p.U, Cfg::TT);
+                    advance(la, ++la_it);
                 }
                 const int stage = it % Cfg::NST;
                 const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
@@ -1086,12 +1346,14 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                     grid_dependency_wait();   // the same tiles for every producer thread
                     waited = true;
                 }
-                const bool first = (it == 0) || (cur.ti == 0);
+                const bool first = (it == 0) || (cur.ti == 0) || (PFX && it == n0);
                 if (first) {
                     const int g = p.NC == 1 ? cur.u : cur.u / p.NC;
                     const int chunk = cur.u - g * p.NC;
                     h0 = g * p.G + chunk * p.GC;
                     gca = min(p.GC, p.G - chunk * p.GC);
+                    if constexpr (PFX)   // a prefix unit: G heads of each of its members
+                        if (cur.s < nv) gca = pm.w[cur.s].nm * p.G;
 
                     head_rows = (size_t)g * p.B;               // rows before kv head g in a block
                     head_off = FLAT ? (size_t)g * Cfg::ROWB : head_rows * Cfg::ROWB;
@@ -1111,13 +1373,15 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                                           head_off
                                     : (size_t)e * blk_stride + head_off;
                 }
+                uint64_t pol_tile = pol_stream;
+                if constexpr (PFX) pol_tile = cur.s < nv ? pol_keep : pol_pass;
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     const bool v = blk_ok && crow[c] < ntok;
                     const size_t off = v ? blk_base + goff[c] : 0;
-                    if constexpr (QK != 0) {
-                        cp_async_16_hint(sK + soff[c], kpool + off, v, pol_stream);
-                        cp_async_16_hint(sV + soff[c], vpool + off, v, pol_stream);
+                    if constexpr (QK != 0 || PFX) {
+                        cp_async_16_hint(sK + soff[c], kpool + off, v, pol_tile);
+                        cp_async_16_hint(sV + soff[c], vpool + off, v, pol_tile);
                     } else {
                         cp_async_16(sK + soff[c], kpool + off, v);
                         cp_async_16(sV + soff[c], vpool + off, v);
@@ -1153,10 +1417,16 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 }
                 // ---- q rows of the unit ride along with its first tile
                 if (first) {
-                    const uint8_t *qsrc = static_cast<const uint8_t *>(p.q) +
-                                          ((size_t)cur.s * p.Hq + h0) * Cfg::QROWB;
-                    for (int i = pt; i < gca * CPRQ; i += kProducerThreads)
-                        cp_async_16(sQ + i * 16, qsrc + (size_t)i * 16, true);
+                    if (PFX && cur.s < nv) {   // a prefix unit: rows of several members
+                        if constexpr (PFX)
+                            copy_q_members<Cfg::QROWB>(sQ, p.q, members + pm.w[cur.s].m0, p.G,
+                                                       p.Hq, h0, gca, pt);
+                    } else {
+                        const uint8_t *qsrc = static_cast<const uint8_t *>(p.q) +
+                                              ((size_t)(cur.s - nv) * p.Hq + h0) * Cfg::QROWB;
+                        for (int i = pt; i < gca * CPRQ; i += kProducerThreads)
+                            cp_async_16(sQ + i * 16, qsrc + (size_t)i * 16, true);
+                    }
                 }
                 // test hook (off unless a test asks for it): CTA 0's first
                 // producer thread withholds its arrival on its first stage, so
@@ -1164,8 +1434,11 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 if (!(drop_first && it == 0)) cp_async_arrive_noinc(full);
                 if (pt == 0) {
                     const int64_t T_u = (int64_t)seq_prefix[cur.s] + (int64_t)cur.u * cur.n;
-                    const bool last = (it == n_my - 1) || (cur.ti == cur.n - 1);
-                    const bool whole = (T_u >= t_begin) && (T_u + cur.n <= t_end);
+                    const bool last = (it == n_my - 1) || (cur.ti == cur.n - 1) ||
+                                      (PFX && it == n0 - 1);
+                    const bool sec0 = PFX && it < n0;   // the tile's section and its range here
+                    const int64_t rb = sec0 ? b0 : b1, re = sec0 ? e0 : e1;
+                    const bool whole = (T_u >= rb) && (T_u + cur.n <= re);
                     TileMeta mt;
                     mt.s = cur.s;
                     mt.h0 = h0;
@@ -1173,17 +1446,17 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                     mt.ntok = ntok;
                     mt.flags = (first ? kFirst : 0) | (last ? kLast : 0) | (whole ? kWhole : 0) |
                                (FUSED && rnew >= 0 ? kNewRow : 0);
-                    mt.slot = T_u > t_begin ? 1 : 0;
+                    mt.slot = (T_u > rb ? 1 : 0) + (PFX && !sec0 ? 2 : 0);
                     mt.tu = (int)T_u;
                     mt.nu = cur.n;
                     meta[stage] = mt;
                     mbar_arrive(full);   // release: the record is visible with the data
                 }
-                pkv_cursor_next(cur, seq_len, p.S, p.U, Cfg::TT);
+                advance(cur, it + 1);
             }
         }
         if constexpr (FUSED) {
-            if (ok) fused_append_rows<Cfg>(p, seq_prefix, seq_len, t_begin, t_end, pt, waited);
+            if (ok) fused_append_rows<Cfg>(p, seq_prefix, seq_len, t_begin, e1, pt, waited);
         }
         cp_async_wait_all();   // this thread's copies land before it exits
         return;
@@ -1194,12 +1467,16 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     if constexpr (MMA) cs.pbuf = sbase + Cfg::OFF_PBUF + warp * Cfg::NTN * 512;
     cs.reset();
     int seg = 0;
-    // Cut segments whose partial this warp has written (the range's first and
-    // last segment at most). Counting them waits until the CTA's tiles are
+    // Cut segments whose partial this warp has written (a range's first and
+    // last segment at most, per section). Counting them waits until the CTA's tiles are
     // done: the fence that must come before a count would otherwise wait
     // behind the copies in flight and stall the math warps mid-run.
-    PendSeg pend[2];
+    PendSegT<PFX> pend[SLOTS];   // two per section of the work list
     int n_pend = 0;
+    // prefix-aware: (sequence, kv head) entries whose result slices this warp
+    // has written, counted at the CTA's end like the cut segments
+    int *fin_list = reinterpret_cast<int *>(smem + Cfg::OFF_FIN) + warp * kFinCap;
+    int n_fin = 0;
     for (int it = 0; it < n_my; ++it) {
         const int stage = it % Cfg::NST;
         const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
@@ -1254,8 +1531,13 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 grid_dependency_wait();
                 waited = true;
             }
-            const int base = (cta * 2 + mt.slot) * p.GC;
+            const int base = (cta * SLOTS + mt.slot) * p.GC;
             const bool whole = (mt.flags & kWhole) != 0;
+            UnitDest ud{0, mt.s, 0};
+            if constexpr (PFX) {
+                if (mt.s < nv) ud = UnitDest{1, 0, pm.w[mt.s].m0};
+                else ud = UnitDest{pm.w[mt.s].blocks > 0 ? 2 : 0, mt.s - nv, 0};
+            }
             // warp `warp` < kMergeSlices owns the elements idx = warp*32 +
             // lane + 128k of the unit's gca x D outputs (head j = idx / D,
             // element d = idx % D); further math warps only feed the combine
@@ -1307,16 +1589,20 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                         }
                         const float lse = __shfl_sync(0xffffffffu, lse_j, k);
                         if (whole) {
-                            store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + k) * D + d,
-                                      p.out_dtype, O);
-                            if (p.lse_out && d == 0)
-                                p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + k] = lse;
+                            if constexpr (PFX) {
+                                put_result<D>(p, ud, mt.h0, k, d, O, lse, members, seq_len, nv);
+                            } else {
+                                store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + k) * D + d,
+                                          p.out_dtype, O);
+                                if (p.lse_out && d == 0)
+                                    p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + k] = lse;
+                            }
                         } else {
                             p.ws_o[(size_t)(base + k) * D + d] = O;
                             // lane 0 holds one element of every head in the slice:
                             // it writes the slice's copy of the head's lse
                             if (lane == 0)
-                                p.ws_lse[((cta * 2 + mt.slot) * kMergeSlices + warp) * p.GC + k] =
+                                p.ws_lse[((cta * SLOTS + mt.slot) * kMergeSlices + warp) * p.GC + k] =
                                     lse;
                         }
                     }
@@ -1337,55 +1623,87 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                     }
                     const float o = O / Ls;
                     if (whole) {
-                        store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d, p.out_dtype, o);
-                        if (p.lse_out && d == 0)
-                            p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + j] = M + log2f(Ls);
+                        if constexpr (PFX) {
+                            put_result<D>(p, ud, mt.h0, j, d, o, M + log2f(Ls), members, seq_len,
+                                          nv);
+                        } else {
+                            store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + j) * D + d,
+                                      p.out_dtype, o);
+                            if (p.lse_out && d == 0)
+                                p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + j] = M + log2f(Ls);
+                        }
                     } else {
                         p.ws_o[(size_t)(base + j) * D + d] = o;
                         // lane 0 holds one element of every head in the slice:
                         // it writes the slice's copy of the head's lse
                         if (lane == 0)
-                            p.ws_lse[((cta * 2 + mt.slot) * kMergeSlices + warp) * p.GC + j] =
+                            p.ws_lse[((cta * SLOTS + mt.slot) * kMergeSlices + warp) * p.GC + j] =
                                 M + log2f(Ls);
                     }
                 }
             }
-            if (!whole && warp < kMergeSlices && warp * 32 < mt.gca * D)
-                pend[n_pend++] = pend_seg(mt, C, NT);
+            if (!whole && warp < kMergeSlices && warp * 32 < mt.gca * D) {
+                if constexpr (PFX) pend[n_pend++] = pend_seg_pfx(mt, C, NT0, NT, ud);
+                else pend[n_pend++] = pend_seg(mt, C, NT);
+            }
+            if constexpr (PFX)
+                if (whole && warp < kMergeSlices && ud.kind != 0)
+                    note_final<D>(p, ud, mt.h0, mt.gca, members, seq_len, nv, fin_list, n_fin,
+                                  warp, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(comb_empty);
             ++seg;
         }
     }
-    if (n_pend == 0) return;
+    if (n_pend == 0) {
+        if constexpr (PFX)
+            if (n_fin) flush_final<D>(p, fin_list, n_fin, warp, lane);
+        return;
+    }
     // Count this warp's slices of its cut segments; for each unit, the last of
     // its partials to arrive merges the slice. Lane 0 releases the whole
     // warp's stores (ordered before it by __syncwarp) with its counts and
     // acquires the other partials with them.
     __syncwarp();
-    unsigned prev[2] = {0u, 0u};
+    unsigned prev[SLOTS] = {};
     if (lane == 0) {
         fence_acq_rel_gpu();
-        for (int i = 0; i < n_pend; ++i)
-            prev[i] = atomicAdd(p.ws_cnt + pend[i].c_first * kMergeSlices + warp, 1u);
+        for (int i = 0; i < n_pend; ++i) {
+            int sec = 0;
+            if constexpr (PFX) sec = pend[i].sec;
+            prev[i] = atomicAdd(p.ws_cnt + (pend[i].c_first + sec * C) * kMergeSlices + warp, 1u);
+        }
         fence_acq_rel_gpu();
     }
     __syncwarp();
     for (int i = 0; i < n_pend; ++i) {
-        const PendSeg &ps = pend[i];
+        const PendSegT<PFX> &ps = pend[i];
         if ((int)__shfl_sync(0xffffffffu, prev[i], 0) + 1 == ps.parts) {
-            if (lane == 0) p.ws_cnt[ps.c_first * kMergeSlices + warp] = 0u;   // for the next call
-            merge_slice<D, GMAX>(p, ps, warp, lane, NT);
+            int sec = 0;
+            if constexpr (PFX) sec = ps.sec;
+            if (lane == 0)   // for the next call
+                p.ws_cnt[(ps.c_first + sec * C) * kMergeSlices + warp] = 0u;
+            merge_slice<D, GMAX, SLOTS, PFX>(p, ps, warp, lane, NT, members, seq_len, nv);
+            if constexpr (PFX)
+                if (ps.ud.kind != 0)
+                    note_final<D>(p, ps.ud, ps.mt.h0, ps.mt.gca, members, seq_len, nv, fin_list,
+                                  n_fin, warp, lane);
         }
     }
+    if constexpr (PFX)
+        if (n_fin) flush_final<D>(p, fin_list, n_fin, warp, lane);
 }
 
 // ---------------------------------------------------------------------------
 // host-side launch of one variant
 // ---------------------------------------------------------------------------
-template <typename T, int D, int GMAX, bool MMA, int QK = 0, bool FLAT = false, bool FUSED = false>
+template <typename T, int D, int GMAX, bool MMA, int QK = 0, bool FLAT = false, bool FUSED = false,
+          bool PFX = false>
 struct SplitVariant {
-    using Cfg = SplitCfg<T, D, GMAX, MMA, QK, FUSED>;
+    using Cfg = SplitCfg<T, D, GMAX, MMA, QK, FUSED, PFX>;
+    using PM = typename std::conditional<PFX, PrefixMap, NoPrefixMap>::type;
+
+    static constexpr auto kernel() { return decode_split_kernel<T, D, GMAX, MMA, QK, FLAT, FUSED, PFX>; }
 
     // Per-device state lives in atomics: host threads making their first
     // calls on a device at the same time may both set the attribute (the
@@ -1395,7 +1713,7 @@ struct SplitVariant {
         if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
         if (!done[dev].load(std::memory_order_acquire)) {
             const size_t smem = Cfg::smem_bytes(kMaxSeqsPerLaunch);
-            cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<T, D, GMAX, MMA, QK, FLAT, FUSED>,
+            cudaError_t e = cudaFuncSetAttribute(kernel(),
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)smem);
             if (e != cudaSuccess) return e;
@@ -1404,7 +1722,8 @@ struct SplitVariant {
         return cudaSuccess;
     }
 
-    static cudaError_t launch(const DecodeParams &p, cudaStream_t st) {
+    // W work sequences: the batch, plus the virtual prefix ones (prefix-aware)
+    static cudaError_t launch_with(const DecodeParams &p, const PM &pm, int W, cudaStream_t st) {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = prepare(dev);
@@ -1412,14 +1731,24 @@ struct SplitVariant {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)p.C);
         cfg.blockDim = dim3(Cfg::THREADS);
-        cfg.dynamicSmemBytes = Cfg::smem_bytes(p.S);
+        cfg.dynamicSmemBytes = Cfg::smem_bytes(W);
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT, FUSED>, p);
+        return cudaLaunchKernelEx(&cfg, kernel(), p, pm);
+    }
+
+    static cudaError_t launch(const DecodeParams &p, cudaStream_t st) {
+        if constexpr (PFX) return cudaErrorInvalidValue;   // needs the prefix map
+        else return launch_with(p, PM{}, p.S, st);
+    }
+
+    static cudaError_t launch_prefix(const DecodeParams &p, const PrefixMap &pm, cudaStream_t st) {
+        if constexpr (PFX) return launch_with(p, pm, pm.nv + p.S, st);
+        else return cudaErrorInvalidValue;
     }
 
     // occupancy of this variant on the current device (queried once per device)
@@ -1431,16 +1760,17 @@ struct SplitVariant {
         if (c > 0) return c;
         if (prepare(dev) != cudaSuccess) return 0;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &n, decode_split_kernel<T, D, GMAX, MMA, QK, FLAT, FUSED>, Cfg::THREADS,
-                Cfg::smem_bytes(kMaxSeqsPerLaunch)) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel(), Cfg::THREADS,
+                                                          Cfg::smem_bytes(kMaxSeqsPerLaunch)) !=
+            cudaSuccess)
             return 0;
         cached[dev].store(n, std::memory_order_release);
         return n;
     }
 
     static const DecodeVariant *get() {
-        static const DecodeVariant v{&launch, &max_ctas_per_sm};
+        static const DecodeVariant v{PFX ? nullptr : &launch, &max_ctas_per_sm,
+                                     PFX ? &launch_prefix : nullptr};
         return &v;
     }
 };

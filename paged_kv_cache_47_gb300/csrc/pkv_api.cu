@@ -8,8 +8,10 @@
 #include <string.h>
 
 #include <atomic>
+#include <memory>
 #include <mutex>
 #include <unordered_set>
+#include <vector>
 
 #include "../../include/pkv.h"
 #include "decomp.h"
@@ -94,6 +96,7 @@ struct Plan {
     bool mma;
     int gmax;
     const pkv::DecodeVariant *variant;
+    int slots = 2;   // partial slots per CTA: 2 per section of the work list
 };
 
 // Head grouping and math path shared by every decode entry point.
@@ -399,6 +402,9 @@ struct DecodeArgs {
     const pkv_decode_options *opts;
     // fused append (paged caches): each sequence's new row, [S][Hk][D]
     const void *k_new = nullptr, *v_new = nullptr;
+    // prefix-aware launch: the work map and the result buffers (one launch)
+    const pkv::PrefixMap *pfx_map = nullptr;
+    pkv::PrefixBuffers pfx_buf = {nullptr, nullptr, nullptr};
     // flat spans (tables is then NULL): see DecodeParams
     const int32_t *slots = nullptr;
     const int32_t *committed = nullptr;
@@ -425,7 +431,8 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
     // flattened tile count must fit in int32
     const int64_t max_tiles_per_unit =
         ((int64_t)a.M * a.B + PKV_TILE_TOKENS - 1) / PKV_TILE_TOKENS;
-    const int64_t chunk_seqs = a.S < pkv::kMaxSeqsPerLaunch ? a.S : pkv::kMaxSeqsPerLaunch;
+    const int64_t chunk_seqs = (a.S < pkv::kMaxSeqsPerLaunch ? a.S : pkv::kMaxSeqsPerLaunch) +
+                               (a.pfx_map ? a.pfx_map->nv : 0);
     if (chunk_seqs * pl.U * max_tiles_per_unit >= (int64_t)INT32_MAX)
         return fail(PKV_ERR_UNSUPPORTED, "batch x context too large for one launch");
 
@@ -439,7 +446,11 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
         return fail(PKV_ERR_INVALID_ARG, "pending_tail %d is negative", pending_tail);
     if (pending_tail > 0 && !a.opts->tables_ready)
         return fail(PKV_ERR_INVALID_ARG, "pending_tail needs tables_ready");
-    const size_t need = workspace_for(C, pl.GC, a.D);
+    // partial slots: workspace_for counts two per CTA
+    const size_t need = workspace_for(C * pl.slots / 2, pl.GC, a.D);
+    if (pl.slots > 2 && 2 * C > PKV_MAX_DECODE_CTAS)
+        return fail(PKV_ERR_INVALID_ARG, "num_ctas %d above %d for a prefix-aware launch", C,
+                    PKV_MAX_DECODE_CTAS / 2);
     if (C > 1 && (!a.ws || a.ws_bytes < need))
         return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                     a.ws ? a.ws_bytes : (size_t)0);
@@ -481,7 +492,7 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
         p.ws_cnt = static_cast<unsigned *>(a.ws);
         p.ws_o = a.ws ? reinterpret_cast<float *>(static_cast<uint8_t *>(a.ws) + kCounterBytes)
                       : nullptr;
-        p.ws_lse = a.ws ? p.ws_o + (size_t)C * 2 * pl.GC * a.D : nullptr;
+        p.ws_lse = a.ws ? p.ws_o + (size_t)C * pl.slots * pl.GC * a.D : nullptr;
         p.C = C;
         p.tables_ready = a.opts ? (a.opts->tables_ready != 0) : 0;
         // a later launch of a long batch follows the first one on the stream,
@@ -493,6 +504,7 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
         p.ks = a.ks;
         p.vs = a.vs;
         pkv::next_wait_fault(&p.wait_ns, &p.drop_arrival);
+        p.pb = a.pfx_buf;
         const size_t new_off = (size_t)s0 * a.Hk * a.D * a.q_es;
         p.k_new = a.k_new ? static_cast<const uint8_t *>(a.k_new) + new_off : nullptr;
         p.v_new = a.v_new ? static_cast<const uint8_t *>(a.v_new) + new_off : nullptr;
@@ -500,8 +512,15 @@ pkv_status run_decode(const Plan &pl, const DecodeArgs &a) {
         cudaError_t e;
         if (first && ev[0] && (e = record_timing_event(ev[0], a.stream)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
-        if ((e = pl.variant->launch(p, a.stream)) != cudaSuccess)
-            return cuda_fail(e, "split-K decode launch");
+        if (a.pfx_map) {
+            // one launch for the whole batch (the plan keeps it within one);
+            // every read waits for the preceding kernel
+            p.pending_tail = 0;
+            e = pl.variant->launch_prefix(p, *a.pfx_map, a.stream);
+        } else {
+            e = pl.variant->launch(p, a.stream);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "split-K decode launch");
         if (first && ev[1] && (e = record_timing_event(ev[1], a.stream)) != cudaSuccess)
             return cuda_fail(e, "cudaEventRecord");
     }
@@ -669,6 +688,157 @@ pkv_status pkv_get_error(int32_t *device_error_word, void *stream) {
         return fail(PKV_ERR_TIMEOUT, "device error word 0x%x", w);
     }
     return fail(PKV_ERR_OUT_OF_RANGE, "device error word 0x%x", w);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- prefix-aware decode
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Host plan of one prefix-aware call (include/pkv.h, pkv_decode_attention_prefix).
+struct PrefixPlan {
+    bool one_launch = false;   // false: the plain decode serves the call
+    int G = 0, gmax = 0, per_unit = 0;   // q heads per kv head; variant width; members per prefix unit
+    size_t off_res_o = 0, off_res_l = 0, off_fin = 0, bytes = 0;
+    pkv::PrefixMap pm;
+};
+
+pkv_status plan_prefix(const pkv_cache_desc *c, int32_t S, int32_t Hq, int32_t M,
+                       const pkv_prefix_groups *g, const pkv_decode_options *o, PrefixPlan *pp) {
+    pkv_status st = check_cache(c);
+    if (st != PKV_OK) return st;
+    if (!g) return fail(PKV_ERR_INVALID_ARG, "prefix groups are NULL");
+    if (S < 0 || M < 1 || Hq < 1 || Hq % c->num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "bad sizes");
+    if (g->num_groups < 0 || (S > 0 && !g->group_of_seq) ||
+        (g->num_groups > 0 && !g->group_prefix_blocks))
+        return fail(PKV_ERR_INVALID_ARG, "bad prefix groups");
+    const int32_t num_ctas = o ? o->num_ctas : 0;
+    if (num_ctas < 0 || num_ctas > PKV_MAX_DECODE_CTAS)
+        return fail(PKV_ERR_INVALID_ARG, "num_ctas %d outside [0, %d]", num_ctas,
+                    PKV_MAX_DECODE_CTAS);
+    std::vector<std::vector<int32_t>> members(g->num_groups);
+    for (int32_t s = 0; s < S; ++s) {
+        const int32_t gi = g->group_of_seq[s];
+        if (gi < -1 || gi >= g->num_groups)
+            return fail(PKV_ERR_INVALID_ARG, "group_of_seq[%d] = %d", s, gi);
+        if (gi >= 0) members[gi].push_back(s);
+    }
+    for (int32_t gi = 0; gi < g->num_groups; ++gi) {
+        const int32_t pb = g->group_prefix_blocks[gi];
+        if (pb < 1 || pb > M || members[gi].empty())
+            return fail(PKV_ERR_INVALID_ARG, "group %d: prefix of %d blocks, %zu members", gi, pb,
+                        members[gi].size());
+    }
+    PrefixPlan &p = *pp;
+    const int Hk = c->num_kv_heads, D = c->head_dim;
+    p.G = Hq / Hk;
+    p.gmax = p.G <= 8 ? 8 : 16;
+    p.per_unit = p.gmax / (p.G < 1 ? 1 : p.G);
+    int nv = 0;
+    for (auto &mem : members) nv += ((int)mem.size() + p.per_unit - 1) / (p.per_unit ? p.per_unit : 1);
+    // one launch for 16-bit caches on the tensor cores, kv groups of a whole
+    // number of 128-element slice periods (a member's outputs then fall in the
+    // same merge slices in a prefix unit as in its own units, and every slice
+    // holds part of each) and work lists that fit the map
+    p.one_launch = (c->dtype == PKV_F16 || c->dtype == PKV_BF16) && !(o && o->consumer == 1) &&
+                   p.G <= 16 && (p.G * D) % 128 == 0 && S + nv <= pkv::kMaxPrefixWork &&
+                   g->num_groups > 0;
+    int C = num_ctas;
+    if (C == 0 && (st = max_default_ctas(&C)) != PKV_OK) return st;
+    if (!p.one_launch) {
+        p.bytes = workspace_for(C, p.G < pkv::kMaxHeadsPerUnit ? p.G : pkv::kMaxHeadsPerUnit, D);
+        return PKV_OK;
+    }
+    // the work map: the groups' prefix units (per_unit members each), then every sequence
+    pkv::PrefixMap &m = p.pm;
+    m.nv = nv;
+    int w = 0, k = 0;
+    for (int32_t gi = 0; gi < g->num_groups; ++gi) {
+        const int m_first = k;
+        for (int32_t s : members[gi]) m.members[k++] = (int16_t)s;
+        for (int j = 0; j < (int)members[gi].size(); j += p.per_unit) {
+            const int n = (int)members[gi].size() - j < p.per_unit ? (int)members[gi].size() - j
+                                                                  : p.per_unit;
+            m.w[w++] = pkv::PrefixWork{g->group_prefix_blocks[gi], members[gi][0], m_first + j, n};
+        }
+    }
+    for (int32_t s = 0; s < S; ++s) {
+        const int32_t gi = g->group_of_seq[s];
+        m.w[nv + s] = pkv::PrefixWork{gi >= 0 ? g->group_prefix_blocks[gi] : 0, s, 0, 0};
+    }
+    // workspace: the split-K part (units carry up to gmax heads), then the
+    // prefix and suffix result rows, then the (sequence, kv head) counters
+    // four partial slots per CTA (two sections), arrival counters for 2 C
+    if (2 * C > PKV_MAX_DECODE_CTAS)
+        return fail(PKV_ERR_INVALID_ARG, "num_ctas %d above %d for a prefix-aware launch", C,
+                    PKV_MAX_DECODE_CTAS / 2);
+    p.off_res_o = align256(workspace_for(2 * C, p.per_unit * p.G, D));
+    p.off_res_l = p.off_res_o + align256((size_t)2 * S * Hq * D * sizeof(float));
+    p.off_fin = p.off_res_l + align256((size_t)2 * S * Hq * pkv::kMergeSlices * sizeof(float));
+    p.bytes = p.off_fin + align256((size_t)S * Hk * pkv::kMergeSlices * sizeof(unsigned));
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pkv_decode_prefix_workspace_bytes(const pkv_cache_desc *cache, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t max_blocks_per_seq,
+                                         const pkv_prefix_groups *groups, int32_t num_ctas) {
+    pkv_decode_options o = {};
+    o.num_ctas = num_ctas;
+    std::unique_ptr<PrefixPlan> pp(new PrefixPlan());
+    if (plan_prefix(cache, num_seqs, num_q_heads, max_blocks_per_seq, groups, &o, pp.get()) !=
+        PKV_OK)
+        return 0;
+    return pp->bytes;
+}
+
+pkv_status pkv_decode_attention_prefix(const pkv_cache_desc *cache, const void *q,
+                                       int32_t num_seqs, int32_t num_q_heads, const void *k_pool,
+                                       const void *v_pool, const int32_t *block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t *context_lens,
+                                       float scale, const pkv_prefix_groups *groups, void *out,
+                                       int32_t out_dtype, void *workspace,
+                                       size_t workspace_bytes, void *stream,
+                                       const pkv_decode_options *options) {
+    std::unique_ptr<PrefixPlan> pp(new PrefixPlan());
+    pkv_status st = plan_prefix(cache, num_seqs, num_q_heads, max_blocks_per_seq, groups,
+                                options, pp.get());
+    if (st != PKV_OK) return st;
+    if (!pp->one_launch)
+        return pkv_decode_attention_ex(cache, q, num_seqs, num_q_heads, k_pool, v_pool,
+                                       block_tables, max_blocks_per_seq, context_lens, scale, out,
+                                       out_dtype, workspace, workspace_bytes, stream, options);
+    DecodeArgs a{cache->num_blocks, cache->block_size, cache->num_kv_heads, cache->head_dim,
+                 elem_bytes(cache->dtype), q, num_seqs, num_q_heads, k_pool, v_pool, nullptr,
+                 nullptr, block_tables, max_blocks_per_seq, context_lens, scale, out, out_dtype,
+                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream), options};
+    if ((st = check_decode_args(a)) != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
+    if (!workspace || workspace_bytes < pp->bytes)
+        return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", pp->bytes,
+                    workspace ? workspace_bytes : (size_t)0);
+    Plan pl;
+    pl.G = pp->G;
+    pl.GC = pp->per_unit * pp->G;   // heads a unit may carry: the workspace's partial rows
+    pl.NC = 1;
+    pl.U = cache->num_kv_heads;
+    pl.mma = true;
+    pl.gmax = pp->gmax;
+    pl.slots = 4;
+    pl.variant = pkv::find_variant_prefix(cache->dtype, cache->head_dim, pp->gmax);
+    if (!pl.variant) return fail(PKV_ERR_UNSUPPORTED, "no kernel variant for this shape");
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.pfx_map = &pp->pm;
+    a.pfx_buf = pkv::PrefixBuffers{reinterpret_cast<float *>(ws + pp->off_res_o),
+                                   reinterpret_cast<float *>(ws + pp->off_res_l),
+                                   reinterpret_cast<unsigned *>(ws + pp->off_fin)};
+    return run_decode(pl, a);
 }
 
 }  // extern "C"

@@ -38,6 +38,36 @@ constexpr int kWhole = 4;  // the segment is the whole unit: write the output di
 constexpr int kNewRow = 8; // fused append: the tile's last row is the context's newest,
                            // whose K/V rows wait in the stage's side slot
 
+// ---------------------------------------------------------------- prefix-aware decode
+// One launch decodes sequences that share leading blocks: each group's shared
+// prefix is a run of "virtual" work sequences placed first in the work list,
+// each carrying up to GMAX / G members' q heads under every kv head; each
+// grouped sequence's own units cover its context past the prefix. A unit's
+// result for a member goes to a workspace row (prefix or suffix); per
+// (sequence, kv head, merge slice) an arrival counter takes one count when
+// the slice of the prefix result is written and one for the suffix result's,
+// and the warp that brings it to two merges that slice of the two by
+// log-sum-exp into `out`. A member
+// whose context ends with the prefix gets its prefix result directly.
+constexpr int kMaxPrefixWork = 1024;   // virtual + real work sequences of one launch
+struct PrefixWork {
+    int32_t blocks;   // shared prefix blocks (virtual: the prefix; real: its group's, 0 = none)
+    int32_t row;      // table row the work sequence reads (virtual: a member; real: itself)
+    int32_t m0, nm;   // virtual: first member in members[], member count; real: 0, 0
+};
+struct PrefixMap {
+    int32_t nv;                               // virtual work sequences (first in the list)
+    PrefixWork w[kMaxPrefixWork];             // [nv + S]
+    int16_t members[kMaxPrefixWork];          // sequence ids, each group's together
+};
+struct NoPrefixMap {};
+// Workspace pointers of the prefix-aware launch (NULL otherwise).
+struct PrefixBuffers {
+    float *res_o;      // [2][S][Hq][D]: prefix, then suffix result rows
+    float *res_l;      // [2][S][Hq][kMergeSlices]: their log2-sum-exp2, a copy per slice
+    unsigned *fin;     // [S][Hk][kMergeSlices] arrival counters, zero between calls
+};
+
 struct DecodeParams {
     const void *q;              // [S][Hq][D]
     void *out;                  // [S][Hq][D] in out_dtype
@@ -88,6 +118,7 @@ struct DecodeParams {
     // first producer thread of CTA 0 withholds its arrival on its first stage.
     unsigned long long wait_ns;
     int drop_arrival;
+    PrefixBuffers pb;           // prefix-aware launch only
 };
 
 // Wait limit and withheld arrivals for the next decode launches (test hook,
@@ -95,11 +126,13 @@ struct DecodeParams {
 void next_wait_fault(unsigned long long *wait_ns, int *drop_arrival);
 
 using SplitLaunchFn = cudaError_t (*)(const DecodeParams &, cudaStream_t);
+using PrefixLaunchFn = cudaError_t (*)(const DecodeParams &, const PrefixMap &, cudaStream_t);
 using MaxCtasFn = int (*)();
 
 struct DecodeVariant {
-    SplitLaunchFn launch;
+    SplitLaunchFn launch;       // NULL for prefix-aware variants
     MaxCtasFn max_ctas_per_sm;  // occupancy of the split-K kernel (0 = cannot run)
+    PrefixLaunchFn launch_prefix = nullptr;   // prefix-aware variants only
 };
 
 // Variant lookup per K/V dtype (defined in decode_<dtype>.cu). gmax is the
@@ -111,6 +144,9 @@ const DecodeVariant *find_variant_bf16(int D, int gmax, bool mma);
 // Variants with the append fused in (decode_fused.cu): fp16 / bf16, tensor-
 // core math, D 64 or 128, gmax 8 or 16; nullptr for any other shape.
 const DecodeVariant *find_variant_fused(int dtype, int D, int gmax);
+// Prefix-aware variants (decode_prefix.cu): fp16 / bf16, tensor-core math, D 64
+// or 128, gmax 8 or 16.
+const DecodeVariant *find_variant_prefix(int dtype, int D, int gmax);
 // 8-bit caches (decode_quant.cu): code_dtype PKV_INT8 / PKV_FP8_E4M3, q in
 // act_dtype PKV_F16 / PKV_BF16, tensor-core math, D = 128, gmax 8 or 16.
 const DecodeVariant *find_variant_quant(int code_dtype, int act_dtype, int D, int gmax);
