@@ -66,9 +66,18 @@ constexpr int kQuantE4m3 = 2;
 // tokens keep the producer's per-tile cost and the math warps' per-tile
 // latency below the time HBM takes to deliver it. Every other variant takes
 // 64-token tiles and four math warps.
-constexpr bool big_tiles(int QK, int GMAX) { return QK != 0 && GMAX == 8; }
+constexpr bool big_tiles(int QK, int GMAX) { return QK != 0 && GMAX <= 8; }
 constexpr int tile_tokens(int QK, int GMAX) { return big_tiles(QK, GMAX) ? 128 : PKV_TILE_TOKENS; }
-constexpr int math_warps(int QK, int GMAX) { return big_tiles(QK, GMAX) ? 8 : kConsumerWarps; }
+// E4M3 caches with one mma n-tile run both products on the 5th-generation
+// tensor cores (tcgen05.mma kind::f8f6f4, accumulators in tensor memory):
+// the codes are mma operands as they are, so no math warp converts them.
+// Their math warps form kTcGroups groups of four that take turns on tiles.
+// Units of up to 4 q heads take a 4-head variant (less code per tile).
+constexpr bool tc_path(int QK, int GMAX) { return QK == kQuantE4m3 && (GMAX == 4 || GMAX == 8); }
+constexpr int kTcGroups = 3;
+constexpr int math_warps(int QK, int GMAX) {
+    return tc_path(QK, GMAX) ? 4 * kTcGroups : big_tiles(QK, GMAX) ? 8 : kConsumerWarps;
+}
 constexpr int kernel_threads(int QK, int GMAX) { return 32 * (math_warps(QK, GMAX) + kProducerWarps); }
 
 // Pending final arrivals a merge-slice warp can hold (prefix-aware variants).
@@ -91,16 +100,26 @@ struct SplitCfg {
     static constexpr int NEWB = FUSED ? ((2 * ROWB + 1023) / 1024) * 1024 : 0;
     static constexpr int STAGE = 2 * KVB + SCB + QB + NEWB; // multiple of 1024
     static constexpr int NTN = GMAX / 8;             // mma n-tiles (MMA only)
-    static constexpr int COMB_O = CW * GMAX * D * 4;
+    static constexpr bool TC = tc_path(QK, GMAX);
+    static constexpr int NG = TC ? CW / 4 : 0;        // warp groups (TC)
+    // combine entries of the output: one per math warp, one per warp group (TC)
+    static constexpr int CWC = TC ? NG : CW;
+    static constexpr int COMB_O = CWC * GMAX * D * 4;
     static constexpr int COMB_ML = 2 * CW * GMAX * 4;
-    static constexpr int PBUF = MMA ? CW * NTN * 2 * 256 : 0;
+    static constexpr int PBUF = (MMA && !TC) ? CW * NTN * 2 * 256 : 0;
+    // TC: per warp group, the q parts and the p parts (mma B operands, 4 KB
+    // each, 1024-byte aligned); then the max-exchange slots, q scales, the
+    // tensor-memory address and the group barriers
+    static constexpr int TCB = TC ? NG * 8192 : 0;
+    static constexpr int TCX = TC ? 2048 : 0;
+    static constexpr int TMEM_COLS = NG <= 2 ? 128 : 256;   // S and O: 64 columns per group
     // work sequences: tile prefix and length (and, prefix-aware, the table offset)
     static constexpr int SEQ_MAX = (2 * kMaxSeqsPerLaunch + 1) * 4 + (PFX ? kMaxPrefixWork * 6 : 0);
     static constexpr int FINB = PFX ? kMergeSlices * kFinCap * 4 : 0;
     static constexpr int SMEM_LIMIT = 227 * 1024;
     static constexpr int PER_STAGE_EXTRA = (int)sizeof(TileMeta) + 16;  // meta + 2 barriers
     static constexpr int FIXED = 1024 /*alignment slack*/ + COMB_O + COMB_ML + PBUF + FINB +
-                                 16 /*comb bars*/ + SEQ_MAX + 64;
+                                 TCB + TCX + 16 /*comb bars*/ + SEQ_MAX + 64;
     static constexpr int NST_FIT = (SMEM_LIMIT - FIXED) / (STAGE + PER_STAGE_EXTRA);
     static constexpr int NST = NST_FIT > 8 ? 8 : NST_FIT;
     static_assert(NST >= 2, "shared-memory plan leaves fewer than two stages");
@@ -108,7 +127,8 @@ struct SplitCfg {
     static_assert(!QK || MMA, "8-bit caches use the tensor-core math");
 
     // offsets from the 1024-aligned base
-    static constexpr int OFF_META = NST * STAGE;
+    static constexpr int OFF_TC = NST * STAGE;
+    static constexpr int OFF_META = OFF_TC + TCB;
     static constexpr int OFF_FULL = OFF_META + NST * (int)sizeof(TileMeta);
     static constexpr int OFF_EMPTY = OFF_FULL + NST * 8;
     static constexpr int OFF_CBAR = OFF_EMPTY + NST * 8;   // comb_full, comb_empty
@@ -117,7 +137,8 @@ struct SplitCfg {
     static constexpr int OFF_COMB_L = OFF_COMB_M + CW * GMAX * 4;
     static constexpr int OFF_PBUF = OFF_COMB_L + CW * GMAX * 4;
     static constexpr int OFF_FIN = OFF_PBUF + PBUF;
-    static constexpr int OFF_SEQ = OFF_FIN + FINB;
+    static constexpr int OFF_TCX = OFF_FIN + FINB;
+    static constexpr int OFF_SEQ = OFF_TCX + TCX;
 
     // W work sequences (the batch, plus the virtual prefix ones when prefix-aware,
     // with their table offsets and the member list)
@@ -776,6 +797,328 @@ struct Consumer<T, D, GMAX, true, QK> {
 };
 
 // ---------------------------------------------------------------------------
+// E4M3 codes on the 5th-generation tensor cores (tcgen05)
+// ---------------------------------------------------------------------------
+// x rounded to 4 significant bits (half away from zero): half of the 20
+// dropped mantissa bits added, then those bits cleared. Every value of 4
+// significant bits in E4M3's normal range is an E4M3 value.
+__device__ __forceinline__ float round_sig4(float x) {
+    return __uint_as_float((__float_as_uint(x) + 0x80000u) & 0xFFF00000u);
+}
+
+// x = x1 + x2 / 16 + x3 / 256 + e, |e| <= 2^-12 |x| (E4M3 normal range), with
+// x1, x2 of 4 significant bits; x3 is left for the E4M3 conversion to round.
+__device__ __forceinline__ void e4m3_parts(float x, float &x1, float &x2, float &x3) {
+    x1 = round_sig4(x);
+    const float r1 = __fmul_rn(__fsub_rn(x, x1), 16.f);
+    x2 = round_sig4(r1);
+    x3 = __fmul_rn(__fsub_rn(r1, x2), 16.f);
+}
+
+// two fp32 to E4M3 codes (round to nearest, saturating): a in the low byte
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+    return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// Heads h0 .. h0 + 3 of x as their three E4M3 parts each, byte 3i + j for
+// part j of head h0 + i; bytes 12..15 are 0.
+template <int GMAX>
+__device__ __forceinline__ uint4 pack_parts4(const float (&x)[GMAX], int h0) {
+    float v[12];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e4m3_parts(x[h0 + i], v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+    uint32_t w[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q)
+        w[q] = e4m3x2(v[4 * q], v[4 * q + 1]) | (e4m3x2(v[4 * q + 2], v[4 * q + 3]) << 16);
+    return make_uint4(w[0], w[1], w[2], 0u);
+}
+
+// Largest of v_i over the warp for i = lane / 8, the four values reduced
+// together: the first exchange halves the values each lane holds, the second
+// halves them again, and three more finish the reduction (6 shuffles, not 20).
+__device__ __forceinline__ float warp_max4(float v0, float v1, float v2, float v3, int lane) {
+    const bool hi16 = lane & 16, hi8 = lane & 8;
+    float a = hi16 ? v2 : v0, b = hi16 ? v3 : v1;   // kept
+    const float c = hi16 ? v0 : v2, d = hi16 ? v1 : v3;
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, c, 16));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, d, 16));
+    float e = hi8 ? b : a;
+    e = fmaxf(e, __shfl_xor_sync(0xffffffffu, hi8 ? a : b, 8));
+    e = fmaxf(e, __shfl_xor_sync(0xffffffffu, e, 4));
+    e = fmaxf(e, __shfl_xor_sync(0xffffffffu, e, 2));
+    return fmaxf(e, __shfl_xor_sync(0xffffffffu, e, 1));
+}
+
+// The math warps form groups of four that take turns on the tiles of the
+// CTA's range (tile i goes to group i % groups). In a group, thread r = 32 (warp % 4) + lane owns tensor-memory
+// lane r: token r of the tile for the scores, element d = r of head_dim for
+// the output. Per tile, one thread of the group issues
+//   S = K Q^T   M = 128 tokens (the stage's K codes, K-major), N = 3 gca
+//               columns (each q head as three E4M3 parts), K = 128 in 4 mmas,
+//   O = V^T P   M = 128 elements (the stage's V codes, read M-major), N = 16
+//               columns (four heads' p as three E4M3 parts each; a second
+//               product for heads 4..7), K = 128 tokens in 4 mmas,
+// both with fp32 accumulators in tensor memory. P is stored token-major
+// without swizzle (16 bytes per token), so each thread writes its token's
+// parts with one 16-byte store. q_h c_h = x1 + x2/16 + x3/256
+// with E4M3 parts and c_h a power of two; p' = p s_v 256 / max s_v alike. The
+// group keeps one running max per head (exchanged through shared memory each
+// tile); each thread keeps its token's share of the sums l and its element's
+// accumulators. The swizzled stage is the operands' layout as it is: rows of
+// 128 bytes, 16-byte chunk c of row r at c ^ (r % 8), 1024-byte atoms.
+template <typename T, int D, int GMAX>
+struct TcConsumer {
+    static_assert(D == 128 && (GMAX == 4 || GMAX == 8),
+                  "tensor-core E4M3 path: head_dim 128, up to 4 or 8 heads");
+    float m[GMAX], lp[GMAX], acc[GMAX], sl2[GMAX];
+    int gca = 0, g = 0, qw = 0, r = 0;
+    bool issuer = false;                 // the group's first warp
+    bool wide = false, pv2 = false;      // scores on 32 columns (gca > 5); a second PV product (gca > 4)
+    uint32_t idesc_qk = 0, idesc_pv = 0;
+    uint64_t dq = 0;                     // descriptor of the q parts
+    uint32_t nproc = 0, xph = 0;         // tiles processed; group barrier uses
+    uint32_t tS = 0, tO = 0;             // this lane quarter's S and O columns
+    uint32_t qp = 0, pb = 0, xbuf = 0, qsc = 0;
+    uint32_t barS = 0, barO = 0, barX = 0, barP = 0;
+    unsigned *err = nullptr;
+    uint64_t wait_ns = 0;
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            m[h] = -CUDART_INF_F;
+            lp[h] = 0.f;
+            acc[h] = 0.f;
+        }
+    }
+
+    // A bounded wait whose outcome is the whole warp's: the tcgen05 loads that
+    // follow are .sync.aligned, so every lane goes on or every lane leaves.
+    __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+        const bool ok = mbar_wait(bar, parity, err, wait_ns);
+        return __all_sync(0xffffffffu, ok);
+    }
+
+    // barrier of the group's four warps (mbarrier, bounded)
+    __device__ __forceinline__ bool gsync(int lane) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(barX);
+        const bool ok = warp_wait(barX, xph & 1u);
+        ++xph;
+        return ok;
+    }
+
+    // The unit's q heads as E4M3 parts: rows 3h + j of this group's B operand
+    // (K-major, 128-byte swizzle), and each head's score factor.
+    __device__ __forceinline__ bool first(const uint8_t *qslot, int gca_, float scale_log2,
+                                          int lane) {
+        reset();
+        gca = gca_;
+        wide = GMAX > 4 && 3 * gca > 16;
+        pv2 = GMAX > 4 && gca > 4;
+        idesc_qk = idesc_e4m3(128, wide ? 32 : 16, false, false);
+        idesc_pv = idesc_e4m3(128, 16, true, true);
+        dq = sdesc_sw128(qp, 16, 1024);
+        const int h = r >> 4, c8 = r & 15;   // head and 8-element chunk of this thread
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = 0.f;
+        if (h < gca) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(qslot + (size_t)h * D * sizeof(T) +
+                                                             c8 * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 f = Elem<T>::unpack2(w[k]);
+                x[2 * k] = f.x;
+                x[2 * k + 1] = f.y;
+            }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        // amax in [2^F, 2^(F+1)): c = 2^E, E = 7 - F, puts the head's largest
+        // element in [128, 256); E is clamped so that c and 1/c stay normal
+        const int F = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+        const int E = max(-120, min(120, 7 - F));
+        const float c = __uint_as_float((uint32_t)(127 + E) << 23);
+        if (h < gca) {
+            uint32_t b[3][2];
+#pragma unroll
+            for (int hw = 0; hw < 2; ++hw) {
+                float p1[4], p2[4], p3[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) e4m3_parts(x[4 * hw + k] * c, p1[k], p2[k], p3[k]);
+                b[0][hw] = e4m3x2(p1[0], p1[1]) | (e4m3x2(p1[2], p1[3]) << 16);
+                b[1][hw] = e4m3x2(p2[0], p2[1]) | (e4m3x2(p2[2], p2[3]) << 16);
+                b[2][hw] = e4m3x2(p3[0], p3[1]) | (e4m3x2(p3[2], p3[3]) << 16);
+            }
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int n = 3 * h + j;
+                sts_u32x2(qp + n * 128 + ((((c8 >> 1) ^ (n & 7))) << 4) + (c8 & 1) * 8, b[j][0],
+                          b[j][1]);
+            }
+            if (c8 == 0)
+                asm volatile("st.shared.f32 [%0], %1;" ::"r"(qsc + 4 * h),
+                             "f"(__uint_as_float((uint32_t)(127 - E) << 23))
+                             : "memory");
+        }
+        fence_proxy_async_smem();
+        if (!gsync(lane)) return false;
+#pragma unroll
+        for (int hh = 0; hh < GMAX; ++hh) sl2[hh] = hh < gca ? scale_log2 * lds_f32(qsc + 4 * hh) : 0.f;
+        return true;
+    }
+
+    // column c of the loaded S or O values
+    __device__ __forceinline__ static float col(const uint32_t (&a)[16], const uint32_t (&b)[16],
+                                                int c) {
+        return __uint_as_float(c < 16 ? a[c] : b[c - 16]);
+    }
+
+    __device__ __forceinline__ bool tile(uint32_t sK, uint32_t sV, uint32_t ksc, uint32_t vsc,
+                                         int ntok, int lane) {
+        const uint32_t ph = nproc & 1u;
+        // ---- S = K Q^T: the issuing warp builds the (warp-uniform)
+        // descriptors, one elected lane issues
+        if (issuer) {
+            // K step k: 32 bytes further along each 128-byte row (start field + 2k)
+            const uint64_t dk = sdesc_sw128(sK, 16, 1024);
+            if (elect_one()) {
+                fence_proxy_async_smem();   // the stage's data, seen complete through its barrier
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tc_mma_e4m3(tS, dk + 2 * k, dq + 2 * k, idesc_qk, k);
+                tc_commit(barS);
+            }
+        }
+        __syncwarp();
+        if (!warp_wait(barS, ph)) return false;
+        tc_fence_after();
+        uint32_t a[16], b[16];
+        tmem_ld16(tS, a);
+        if (wide) tmem_ld16(tS + 16, b);
+        tmem_ld_wait(a);
+        if (wide) tmem_ld_wait(b);
+        const bool valid = r < ntok;
+        const float ks = lds_f32(ksc + 4 * r);
+        const float vs = lds_f32(vsc + 4 * r);
+        float s[GMAX];
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            const float v = col(a, b, 3 * h) + col(a, b, 3 * h + 1) * 0.0625f +
+                            col(a, b, 3 * h + 2) * 0.00390625f;
+            s[h] = (valid && h < gca) ? v * ks * sl2[h] : -CUDART_INF_F;
+        }
+        // ---- the group's max of each head's scores and of the V row scales:
+        // this warp's maxima to the exchange slot (heads 4j .. 4j + 3 reduced
+        // together; lane 8i then holds head 4j + i)
+        const uint32_t slot = xbuf + (xph & 1u) * 4 * 64 + qw * 64;
+        const float m03 = warp_max4(s[0], s[1], s[2], s[3], lane);
+        const float vmx = warp_max_f32(valid ? vs : 0.f);
+        if ((lane & 7) == 0) sts_f32(slot + 4 * (lane >> 3), m03);
+        if constexpr (GMAX > 4) {
+            if (pv2) {
+                const float m47 = warp_max4(s[4], s[5], s[6], s[7], lane);
+                if ((lane & 7) == 0) sts_f32(slot + 16 + 4 * (lane >> 3), m47);
+            }
+        }
+        if (lane == 0) sts_f32(slot + 4 * GMAX, vmx);
+        if (!gsync(lane)) return false;
+        const uint32_t slot0 = slot - qw * 64;
+        float M[GMAX + 1];
+#pragma unroll
+        for (int h = 0; h <= GMAX; ++h) {
+            M[h] = -CUDART_INF_F;
+            if (h < GMAX && h >= gca) continue;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) M[h] = fmaxf(M[h], lds_f32(slot0 + w * 64 + 4 * h));
+        }
+        float VM = M[GMAX];
+        if (!(VM > 0.f)) VM = 1.f;   // all-zero V rows: p' = 0 whatever VM is
+        const float vf = vs * __frcp_rn(VM) * 256.f;
+        // ---- online softmax; token r's p' parts: 16 bytes (heads 0..3) at
+        // pb + 16 r, and heads 4..7 at pb + 2048 + 16 r
+        float alpha[GMAX], x[GMAX];
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            alpha[h] = 1.f;
+            x[h] = 0.f;
+            if (h >= gca) continue;
+            const float mn = fmaxf(m[h], M[h]);
+            alpha[h] = ex2_approx(m[h] - mn);
+            m[h] = mn;
+            const float p = valid ? ex2_approx(s[h] - mn) : 0.f;
+            lp[h] = lp[h] * alpha[h] + p;
+            x[h] = p * vf;
+        }
+        sts_u32x4(pb + 16 * r, pack_parts4(x, 0));
+        if constexpr (GMAX > 4)
+            if (pv2) sts_u32x4(pb + 2048 + 16 * r, pack_parts4(x, 4));
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(barP);
+        // ---- O = V^T P'
+        if (issuer) {
+            if (!warp_wait(barP, ph)) return false;
+            // K step k: tokens 32k..: V 4 atoms (4096 bytes) further, P 512 bytes
+            const uint64_t dv = sdesc_sw128(sV, 1024, 1024), dp = sdesc_none(pb, 128);
+            if (elect_one()) {
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tc_mma_e4m3(tO, dv + 256 * k, dp + 32 * k, idesc_pv, k);
+                if (pv2)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        tc_mma_e4m3(tO + 16, dv + 256 * k, dp + 128 + 32 * k, idesc_pv, k);
+                tc_commit(barO);
+            }
+            __syncwarp();
+        }
+        if (!warp_wait(barO, ph)) return false;
+        tc_fence_after();
+        tmem_ld16(tO, a);
+        if (pv2) tmem_ld16(tO + 16, b);
+        tmem_ld_wait(a);
+        if (pv2) tmem_ld_wait(b);
+        const float of = VM * (1.f / 256.f);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            if (h >= gca) continue;
+            const int c0 = h < 4 ? 3 * h : 16 + 3 * (h - 4);   // O columns of head h
+            const float o = col(a, b, c0) + col(a, b, c0 + 1) * 0.0625f +
+                            col(a, b, c0 + 2) * 0.00390625f;
+            acc[h] = fmaf(acc[h], alpha[h], o * of);
+        }
+        tc_fence_before();
+        ++nproc;
+        return true;
+    }
+
+    // the group's state for the segment: m (the same in all four warps), this
+    // warp's share of l, and the group's output (entry g)
+    __device__ __forceinline__ void write_comb(float *comb_o, float *comb_m, float *comb_l,
+                                               int warp, int lane) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            float l = lp[h];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+            if (lane == 0) {
+                comb_m[warp * GMAX + h] = m[h];
+                comb_l[warp * GMAX + h] = l;
+            }
+            comb_o[(g * GMAX + h) * D + r] = acc[h];
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
 // log-sum-exp merge of one warp's slice of a unit cut by CTA boundaries
 // ---------------------------------------------------------------------------
 // The partials of the unit come from CTAs c_first .. c_last (those with an
@@ -1151,6 +1494,12 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
+    // TC: exchange slots (NG groups x 2 slots x 4 warps x 64 B), q scales
+    // (NG x 8 floats), the TMEM address, then 4 NG + 2 barriers (8-byte aligned)
+    const uint32_t tcx = (sbase + Cfg::OFF_TCX + 15u) & ~15u;
+    const uint32_t tcbar = tcx + 1680;
+    static_assert(!Cfg::TC || (Cfg::NG <= 3 && 1680 + (4 * Cfg::NG + 2) * 8 + 15 <= Cfg::TCX),
+                  "TC scratch layout");
     TileMeta *meta = reinterpret_cast<TileMeta *>(smem + Cfg::OFF_META);
     const uint32_t full0 = sbase + Cfg::OFF_FULL;
     const uint32_t empty0 = sbase + Cfg::OFF_EMPTY;
@@ -1177,7 +1526,20 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
             mbar_init(empty0 + 8 * i, Cfg::CW);
         }
         mbar_init(comb_full, Cfg::CW);
-        mbar_init(comb_empty, Cfg::CW);
+        mbar_init(comb_empty, Cfg::TC ? 4 : Cfg::CW);   // TC: the merging group's warps
+        if constexpr (Cfg::TC) {
+            // per group: S done, O done (tcgen05.commit), the group's barrier,
+            // p parts written; then TMEM allocated, TMEM no longer used
+            const uint32_t tb = tcbar;
+            for (int gi = 0; gi < Cfg::NG; ++gi) {
+                mbar_init(tb + 8 * (0 * Cfg::NG + gi), 1);
+                mbar_init(tb + 8 * (1 * Cfg::NG + gi), 1);
+                mbar_init(tb + 8 * (2 * Cfg::NG + gi), 4);
+                mbar_init(tb + 8 * (3 * Cfg::NG + gi), 4);
+            }
+            mbar_init(tb + 8 * (4 * Cfg::NG), 1);
+            mbar_init(tb + 8 * (4 * Cfg::NG + 1), Cfg::CW);
+        }
         fence_mbarrier_init();
     }
     // Inputs may come from the previous kernel on the stream (launched with
@@ -1463,8 +1825,63 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     }
 
     // ======================= consumer warps =======================
-    Consumer<T, D, GMAX, MMA, QK> cs;
-    if constexpr (MMA) cs.pbuf = sbase + Cfg::OFF_PBUF + warp * Cfg::NTN * 512;
+    using Cs = typename std::conditional<Cfg::TC, TcConsumer<T, D, GMAX>,
+                                         Consumer<T, D, GMAX, MMA, QK>>::type;
+    Cs cs;
+    // TC: warp 0 allocates TMEM (per group g: S at column 64g, O at 64g + 32)
+    // and frees them once every math warp has arrived on the done barrier,
+    // on every way out of the loop below
+    uint32_t tmem_base = 0;
+    const uint32_t tslot = tcx + 1664;
+    const uint32_t bar_tready = tcbar + 8 * (4 * Cfg::NG), bar_done = bar_tready + 8;
+    auto tc_leave = [&]() {
+        if constexpr (Cfg::TC) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_done);
+            if (warp == 0) {
+                mbar_wait(bar_done, 0, p.err, 4 * p.wait_ns);
+                tc_fence_after();
+                __syncwarp();
+                tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+            }
+        }
+    };
+    if constexpr (Cfg::TC) {
+        __syncwarp();
+        if (warp == 0) {
+            tmem_alloc(tslot, Cfg::TMEM_COLS);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tready);
+        }
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_tready, 0, p.err, p.wait_ns));
+        tc_fence_after();
+        tmem_base = ok || warp == 0 ? lds_u32(tslot) : 0u;
+        if (!ok) {
+            tc_leave();
+            return;
+        }
+        const uint32_t tb = tcbar;
+        cs.g = warp >> 2;
+        cs.qw = warp & 3;
+        cs.r = cs.qw * 32 + lane;
+        cs.issuer = cs.qw == 0;
+        cs.tS = tmem_base + ((uint32_t)(cs.qw * 32) << 16) + 64 * cs.g;
+        cs.tO = cs.tS + 32;
+        cs.qp = sbase + Cfg::OFF_TC + 8192 * cs.g;
+        cs.pb = cs.qp + 4096;
+        cs.xbuf = tcx + 512 * cs.g;
+        cs.qsc = tcx + 1536 + 32 * cs.g;
+        cs.barS = tb + 8 * (0 * Cfg::NG + cs.g);
+        cs.barO = tb + 8 * (1 * Cfg::NG + cs.g);
+        cs.barX = tb + 8 * (2 * Cfg::NG + cs.g);
+        cs.barP = tb + 8 * (3 * Cfg::NG + cs.g);
+        cs.err = p.err;
+        cs.wait_ns = p.wait_ns;
+    } else if constexpr (MMA) {
+        cs.pbuf = sbase + Cfg::OFF_PBUF + warp * Cfg::NTN * 512;
+    }
     cs.reset();
     int seg = 0;
     // Cut segments whose partial this warp has written (a range's first and
@@ -1480,14 +1897,27 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     for (int it = 0; it < n_my; ++it) {
         const int stage = it % Cfg::NST;
         const uint32_t ph = (uint32_t)(it / Cfg::NST) & 1u;
-        if (!mbar_wait(full0 + 8 * stage, ph, p.err, p.wait_ns)) return;
+        bool full_ok = mbar_wait(full0 + 8 * stage, ph, p.err, p.wait_ns);
+        if constexpr (Cfg::TC) full_ok = __all_sync(0xffffffffu, full_ok);
+        if (!full_ok) {
+            tc_leave();
+            return;
+        }
         const TileMeta mt = meta[stage];
         const uint32_t sK = sbase + stage * Cfg::STAGE;
         const uint32_t sV = sK + Cfg::KVB;
         if (mt.flags & kFirst) {
-            cs.reset();
-            cs.load_q(smem + stage * Cfg::STAGE + 2 * Cfg::KVB + Cfg::SCB, mt.gca, p.scale_log2,
-                      lane);
+            if constexpr (Cfg::TC) {
+                if (!cs.first(smem + stage * Cfg::STAGE + 2 * Cfg::KVB + Cfg::SCB, mt.gca,
+                              p.scale_log2, lane)) {
+                    tc_leave();
+                    return;
+                }
+            } else {
+                cs.reset();
+                cs.load_q(smem + stage * Cfg::STAGE + 2 * Cfg::KVB + Cfg::SCB, mt.gca,
+                          p.scale_log2, lane);
+            }
         }
         if constexpr (FUSED) {
             // the context's newest row: the math warp whose 16 rows hold it
@@ -1510,7 +1940,14 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 __syncwarp();
             }
         }
-        if constexpr (QK != 0) {
+        if constexpr (Cfg::TC) {
+            // the group whose turn it is runs the tile's products on the tensor cores
+            const uint32_t ksc = sK + 2 * Cfg::KVB;
+            if (it % Cfg::NG == cs.g && !cs.tile(sK, sV, ksc, ksc + 4 * Cfg::TT, mt.ntok, lane)) {
+                tc_leave();
+                return;
+            }
+        } else if constexpr (QK != 0) {
             // the tile step reads this warp's 16 rows of codes straight into registers
             const uint32_t ksc = sK + 2 * Cfg::KVB;
             cs.tile(sK, sV, mt.ntok, warp, lane, ksc, ksc + 4 * Cfg::TT);
@@ -1521,13 +1958,29 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         if (lane == 0) mbar_arrive(empty0 + 8 * stage);
 
         if (mt.flags & kLast) {
-            // combine the math warps' softmax states for this segment
-            if (!mbar_wait(comb_empty, ((uint32_t)seg & 1u) ^ 1u, p.err, p.wait_ns)) return;
+            // combine the math warps' softmax states for this segment. Merge
+            // slice `slice` < kMergeSlices owns the outputs idx = slice*32 +
+            // lane + 128k: warp `slice` (TC: warp slice of the group that ran
+            // the segment's last tile, while the other groups go on; they
+            // only feed the combine)
+            int slice = warp;
+            if constexpr (Cfg::TC) slice = it % Cfg::NG == cs.g ? cs.qw : kMergeSlices;
+            if (!mbar_wait(comb_empty, ((uint32_t)seg & 1u) ^ 1u, p.err, p.wait_ns)) {
+                tc_leave();
+                return;
+            }
             cs.write_comb(comb_o, comb_m, comb_l, warp, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(comb_full);
-            if (!mbar_wait(comb_full, (uint32_t)seg & 1u, p.err, p.wait_ns)) return;
-            if (!waited && warp < kMergeSlices) {   // stores wait for the preceding kernel
+            if (Cfg::TC && slice >= kMergeSlices) {
+                ++seg;
+                continue;
+            }
+            if (!mbar_wait(comb_full, (uint32_t)seg & 1u, p.err, p.wait_ns)) {
+                tc_leave();
+                return;
+            }
+            if (!waited && slice < kMergeSlices) {   // stores wait for the preceding kernel
                 grid_dependency_wait();
                 waited = true;
             }
@@ -1538,10 +1991,43 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 if (mt.s < nv) ud = UnitDest{1, 0, pm.w[mt.s].m0};
                 else ud = UnitDest{pm.w[mt.s].blocks > 0 ? 2 : 0, mt.s - nv, 0};
             }
-            // warp `warp` < kMergeSlices owns the elements idx = warp*32 +
+            // slice `slice` < kMergeSlices owns the elements idx = slice*32 +
             // lane + 128k of the unit's gca x D outputs (head j = idx / D,
-            // element d = idx % D); further math warps only feed the combine
-            if constexpr (MMA && D == 128) {
+            // element d = idx % D)
+            if constexpr (Cfg::TC) {
+                // warp groups: m and O per group, l in shares per warp
+                if (slice < kMergeSlices) {
+                    const int d = slice * 32 + lane;
+#pragma unroll
+                    for (int k = 0; k < GMAX; ++k) {
+                        if (k >= mt.gca) break;
+                        float M = -CUDART_INF_F;
+#pragma unroll
+                        for (int gi = 0; gi < Cfg::NG; ++gi) M = fmaxf(M, comb_m[4 * gi * GMAX + k]);
+                        float Ls = 0.f, O = 0.f;
+#pragma unroll
+                        for (int gi = 0; gi < Cfg::NG; ++gi) {
+                            const float w = exp2f(comb_m[4 * gi * GMAX + k] - M);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) Ls = fmaf(w, comb_l[(4 * gi + q) * GMAX + k], Ls);
+                            O = fmaf(w, comb_o[(gi * GMAX + k) * D + d], O);
+                        }
+                        O /= Ls;
+                        const float lse = M + log2f(Ls);
+                        if (whole) {
+                            store_out(p.out, ((size_t)mt.s * p.Hq + mt.h0 + k) * D + d,
+                                      p.out_dtype, O);
+                            if (p.lse_out && d == 0)
+                                p.lse_out[(size_t)mt.s * p.Hq + mt.h0 + k] = lse;
+                        } else {
+                            p.ws_o[(size_t)(base + k) * D + d] = O;
+                            if (lane == 0)
+                                p.ws_lse[((cta * SLOTS + mt.slot) * kMergeSlices + slice) * p.GC + k] =
+                                    lse;
+                        }
+                    }
+                }
+            } else if constexpr (MMA && D == 128) {
                 // Weights first: lane L holds the (warp w, head j) pairs P = 32s + L
                 // (P = w * GMAX + j), reduces max and sum over w with shuffles and
                 // keeps w's weight 2^(m_wj - M_j) / sum_w' 2^(m_w'j - M_j) l_w'j.
@@ -1550,7 +2036,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                 constexpr int NPAIR = Cfg::CW * GMAX;
                 constexpr int PPL = (NPAIR + 31) / 32;
                 static_assert(NPAIR % 32 == 0 || NPAIR < 32, "pairs fill whole warps");
-                if (warp < kMergeSlices) {
+                if (slice < kMergeSlices) {
                     float mv[PPL], lv[PPL], sw[PPL];
                     float M = -CUDART_INF_F;
 #pragma unroll
@@ -1576,7 +2062,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
 #pragma unroll
                     for (int q = 0; q < PPL; ++q) sw[q] *= inv;
                     const float lse_j = M + log2f(Lsum);   // head lane % GMAX
-                    const int d = warp * 32 + lane;
+                    const int d = slice * 32 + lane;
 #pragma unroll
                     for (int k = 0; k < GMAX; ++k) {
                         if (k >= mt.gca) break;
@@ -1602,13 +2088,13 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                             // lane 0 holds one element of every head in the slice:
                             // it writes the slice's copy of the head's lse
                             if (lane == 0)
-                                p.ws_lse[((cta * SLOTS + mt.slot) * kMergeSlices + warp) * p.GC + k] =
+                                p.ws_lse[((cta * SLOTS + mt.slot) * kMergeSlices + slice) * p.GC + k] =
                                     lse;
                         }
                     }
                 }
             } else {
-                const int idx0 = warp < kMergeSlices ? warp * 32 + lane : mt.gca * D;
+                const int idx0 = slice < kMergeSlices ? slice * 32 + lane : mt.gca * D;
                 for (int idx = idx0; idx < mt.gca * D; idx += kMergeSlices * 32) {
                     const int j = idx / D, d = idx - (idx / D) * D;
                     float M = -CUDART_INF_F;
@@ -1637,17 +2123,17 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
                         // lane 0 holds one element of every head in the slice:
                         // it writes the slice's copy of the head's lse
                         if (lane == 0)
-                            p.ws_lse[((cta * SLOTS + mt.slot) * kMergeSlices + warp) * p.GC + j] =
+                            p.ws_lse[((cta * SLOTS + mt.slot) * kMergeSlices + slice) * p.GC + j] =
                                 M + log2f(Ls);
                     }
                 }
             }
-            if (!whole && warp < kMergeSlices && warp * 32 < mt.gca * D) {
+            if (!whole && slice < kMergeSlices && slice * 32 < mt.gca * D) {
                 if constexpr (PFX) pend[n_pend++] = pend_seg_pfx(mt, C, NT0, NT, ud);
                 else pend[n_pend++] = pend_seg(mt, C, NT);
             }
             if constexpr (PFX)
-                if (whole && warp < kMergeSlices && ud.kind != 0)
+                if (whole && slice < kMergeSlices && ud.kind != 0)
                     note_final<D>(p, ud, mt.h0, mt.gca, members, seq_len, nv, fin_list, n_fin,
                                   warp, lane);
             __syncwarp();
@@ -1655,6 +2141,10 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
             ++seg;
         }
     }
+    tc_leave();
+    // this warp's merge slice (TC: its place in its group)
+    int mslice = warp;
+    if constexpr (Cfg::TC) mslice = cs.qw;
     if (n_pend == 0) {
         if constexpr (PFX)
             if (n_fin) flush_final<D>(p, fin_list, n_fin, warp, lane);
@@ -1671,7 +2161,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         for (int i = 0; i < n_pend; ++i) {
             int sec = 0;
             if constexpr (PFX) sec = pend[i].sec;
-            prev[i] = atomicAdd(p.ws_cnt + (pend[i].c_first + sec * C) * kMergeSlices + warp, 1u);
+            prev[i] = atomicAdd(p.ws_cnt + (pend[i].c_first + sec * C) * kMergeSlices + mslice, 1u);
         }
         fence_acq_rel_gpu();
     }
@@ -1682,8 +2172,8 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
             int sec = 0;
             if constexpr (PFX) sec = ps.sec;
             if (lane == 0)   // for the next call
-                p.ws_cnt[(ps.c_first + sec * C) * kMergeSlices + warp] = 0u;
-            merge_slice<D, GMAX, SLOTS, PFX>(p, ps, warp, lane, NT, members, seq_len, nv);
+                p.ws_cnt[(ps.c_first + sec * C) * kMergeSlices + mslice] = 0u;
+            merge_slice<D, GMAX, SLOTS, PFX>(p, ps, mslice, lane, NT, members, seq_len, nv);
             if constexpr (PFX)
                 if (ps.ud.kind != 0)
                     note_final<D>(p, ps.ud, ps.mt.h0, ps.mt.gca, members, seq_len, nv, fin_list,

@@ -143,6 +143,8 @@ pkv_status make_plan_quant(const pkv_qcache_desc *c, int Hq, const pkv_decode_op
         return fail(PKV_ERR_UNSUPPORTED, "8-bit caches use the tensor-core math (consumer 1 given)");
     pkv_status st = plan_groups(c->num_kv_heads, Hq, o, true, pl);
     if (st != PKV_OK) return st;
+    // E4M3 units of up to 4 heads: the tensor-core variant sized for 4
+    if (c->code_dtype == PKV_FP8_E4M3 && pl->GC <= 4) pl->gmax = 4;
     pl->variant = pkv::find_variant_quant(c->code_dtype, c->act_dtype, c->head_dim, pl->gmax);
     if (!pl->variant) return fail(PKV_ERR_UNSUPPORTED, "no kernel variant for this shape");
     return PKV_OK;

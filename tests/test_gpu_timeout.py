@@ -125,3 +125,51 @@ def test_timed_out_wait_static_scratch_recovers(case):
 def test_hook_rejects_negative_counts():
     with pytest.raises(binding.PkvError):
         binding.set_wait_fault(0, -1)
+
+
+def test_timed_out_wait_tensor_memory_path():
+    # The E4M3 decode runs its products on the tensor cores and holds tensor
+    # memory per CTA. A timed-out wait frees it on the way out: the next calls,
+    # with more CTAs than SMs (CTAs of a later wave allocate on SMs that
+    # earlier CTAs left), complete and match the oracle.
+    spec = W.WorkloadSpec("timeout_e4m3", 6, 32, 8, 128, 16, "bf16", 1.0)
+    lengths = [700, 65, 2049, 1, 300, 1500]
+    st, v = W.make_workload(spec, seed=42, lengths=lengths)
+    kp, vp = v["k_pool"].clone(), v["v_pool"].clone()
+    oracle.append(v["k_new"], v["v_new"], st.slot_mapping, kp, vp)
+    NB, Hk, B, D = kp.shape
+    slots = []
+    for s, L in enumerate(lengths):
+        slots += [int(st.block_tables[s, t // B]) * B + t % B for t in range(L)]
+    sl = torch.tensor(slots, dtype=torch.int64)
+    kr, vr = kp[sl // B, :, sl % B].contiguous(), vp[sl // B, :, sl % B].contiguous()
+
+    def pools(dev):
+        kc = torch.full((NB, Hk, B, D), 0x7F, dtype=torch.uint8, device=dev)
+        ks = torch.full((NB, Hk, B), float("nan"), dtype=torch.float32, device=dev)
+        return kc, kc.clone(), ks, ks.clone()
+
+    ref = pools("cpu")
+    oracle.append_quant("fp8_e4m3", kr, vr, sl, *ref)
+    cache = binding.QuantCache(*pools("cuda"), "fp8_e4m3", kr.dtype)
+    binding.append_quant(kr.cuda(), vr.cuda(), sl.cuda(), cache)
+    scale = 1.0 / math.sqrt(128)
+    want = oracle.decode_quant("fp8_e4m3", v["q"], *ref, st.block_tables, st.context_lens, scale)
+    q, bt, cl = v["q"].cuda(), st.block_tables.cuda(), st.context_lens.cuda()
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    ws = binding.alloc_quant_workspace(cache, 32, 0)
+    binding.set_wait_fault(SHORT_NS, 1)
+    try:
+        binding.decode_attention_quant(q, cache, bt, cl, scale, out_dtype=torch.float32,
+                                       workspace=ws)
+        status, word = binding.get_error_status()
+    finally:
+        binding.set_wait_fault(0, 0)
+    assert status == PKV_ERR_TIMEOUT and word & binding.DEVERR_TIMEOUT
+    for C in (0, 500):
+        ws = binding.alloc_quant_workspace(cache, 32, C)
+        out = binding.decode_attention_quant(q, cache, bt, cl, scale, out_dtype=torch.float32,
+                                             workspace=ws, num_ctas=C)
+        assert binding.get_error_status() == (0, 0)
+        assert _err(out, want) <= 2e-3
