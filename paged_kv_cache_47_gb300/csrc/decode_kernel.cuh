@@ -111,8 +111,14 @@ struct SplitCfg {
     // each, 1024-byte aligned); then the max-exchange slots, q scales, the
     // tensor-memory address and the group barriers
     static constexpr int TCB = TC ? NG * 8192 : 0;
-    static constexpr int TCX = TC ? 2048 : 0;
-    static constexpr int TMEM_COLS = NG <= 2 ? 128 : 256;   // S and O: 64 columns per group
+    // exchange slots (per group 2 slots x 4 warps x 64 B), q scales (per group
+    // 8 floats), the TMEM address, then 4 NG + 2 barriers (8-byte aligned);
+    // the region starts 16-byte aligned
+    static constexpr int TCX_QSC = NG * 512;
+    static constexpr int TCX_TSLOT = TCX_QSC + NG * 32;
+    static constexpr int TCX_BAR = TCX_TSLOT + 16;
+    static constexpr int TCX = TC ? ((TCX_BAR + (4 * NG + 2) * 8 + 16 + 255) / 256) * 256 : 0;
+    static constexpr int TMEM_COLS = NG <= 2 ? 128 : NG <= 4 ? 256 : 512;   // S, O: 64 columns per group
     // work sequences: tile prefix and length (and, prefix-aware, the table offset)
     static constexpr int SEQ_MAX = (2 * kMaxSeqsPerLaunch + 1) * 4 + (PFX ? kMaxPrefixWork * 6 : 0);
     static constexpr int FINB = PFX ? kMergeSlices * kFinCap * 4 : 0;
@@ -920,52 +926,39 @@ struct TcConsumer {
         idesc_qk = idesc_e4m3(128, wide ? 32 : 16, false, false);
         idesc_pv = idesc_e4m3(128, 16, true, true);
         dq = sdesc_sw128(qp, 16, 1024);
-        const int h = r >> 4, c8 = r & 15;   // head and 8-element chunk of this thread
-        float x[8];
+        // warp qw takes heads hb + qw (hb = 0, 4): lane t holds elements
+        // 4t .. 4t + 3, so a head's largest element is one warp reduction
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = 0.f;
-        if (h < gca) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(qslot + (size_t)h * D * sizeof(T) +
-                                                             c8 * 16);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int hb = 0; hb < GMAX; hb += 4) {
+            const int h = hb + qw;   // warp-uniform
+            if (h >= gca) break;
+            const uint2 v =
+                *reinterpret_cast<const uint2 *>(qslot + (size_t)h * D * sizeof(T) + lane * 8);
+            const float2 f0 = Elem<T>::unpack2(v.x), f1 = Elem<T>::unpack2(v.y);
+            const float x[4] = {f0.x, f0.y, f1.x, f1.y};
+            const float amax =
+                warp_max_f32(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+            // amax in [2^F, 2^(F+1)): c = 2^E, E = 7 - F, puts the head's largest
+            // element in [128, 256); E is clamped so that c and 1/c stay normal
+            const int F = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+            const int E = max(-120, min(120, 7 - F));
+            const float c = __uint_as_float((uint32_t)(127 + E) << 23);
+            float p1[4], p2[4], p3[4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 f = Elem<T>::unpack2(w[k]);
-                x[2 * k] = f.x;
-                x[2 * k + 1] = f.y;
-            }
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(x[k]));
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        // amax in [2^F, 2^(F+1)): c = 2^E, E = 7 - F, puts the head's largest
-        // element in [128, 256); E is clamped so that c and 1/c stay normal
-        const int F = (int)((__float_as_uint(amax) >> 23) & 0xffu) - 127;
-        const int E = max(-120, min(120, 7 - F));
-        const float c = __uint_as_float((uint32_t)(127 + E) << 23);
-        if (h < gca) {
-            uint32_t b[3][2];
-#pragma unroll
-            for (int hw = 0; hw < 2; ++hw) {
-                float p1[4], p2[4], p3[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) e4m3_parts(x[4 * hw + k] * c, p1[k], p2[k], p3[k]);
-                b[0][hw] = e4m3x2(p1[0], p1[1]) | (e4m3x2(p1[2], p1[3]) << 16);
-                b[1][hw] = e4m3x2(p2[0], p2[1]) | (e4m3x2(p2[2], p2[3]) << 16);
-                b[2][hw] = e4m3x2(p3[0], p3[1]) | (e4m3x2(p3[2], p3[3]) << 16);
-            }
+            for (int k = 0; k < 4; ++k) e4m3_parts(x[k] * c, p1[k], p2[k], p3[k]);
+            const uint32_t b[3] = {e4m3x2(p1[0], p1[1]) | (e4m3x2(p1[2], p1[3]) << 16),
+                                   e4m3x2(p2[0], p2[1]) | (e4m3x2(p2[2], p2[3]) << 16),
+                                   e4m3x2(p3[0], p3[1]) | (e4m3x2(p3[2], p3[3]) << 16)};
 #pragma unroll
             for (int j = 0; j < 3; ++j) {
                 const int n = 3 * h + j;
-                sts_u32x2(qp + n * 128 + ((((c8 >> 1) ^ (n & 7))) << 4) + (c8 & 1) * 8, b[j][0],
-                          b[j][1]);
-            }
-            if (c8 == 0)
-                asm volatile("st.shared.f32 [%0], %1;" ::"r"(qsc + 4 * h),
-                             "f"(__uint_as_float((uint32_t)(127 - E) << 23))
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(qp + n * 128 +
+                                                              ((((lane >> 2) ^ (n & 7))) << 4) +
+                                                              (lane & 3) * 4),
+                             "r"(b[j])
                              : "memory");
+            }
+            if (lane == 0) sts_f32(qsc + 4 * h, __uint_as_float((uint32_t)(127 - E) << 23));
         }
         fence_proxy_async_smem();
         if (!gsync(lane)) return false;
@@ -984,7 +977,9 @@ struct TcConsumer {
                                          int ntok, int lane) {
         const uint32_t ph = nproc & 1u;
         // ---- S = K Q^T: the issuing warp builds the (warp-uniform)
-        // descriptors, one elected lane issues
+        // descriptors, one elected lane issues. (Issuing the group's next
+        // tile's product right after this tile's PV product, when its stage
+        // was full, made the llama-shaped step slower: 69.2 -> 77.8 us.)
         if (issuer) {
             // K step k: 32 bytes further along each 128-byte row (start field + 2k)
             const uint64_t dk = sdesc_sw128(sK, 16, 1024);
@@ -1494,12 +1489,9 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    // TC: exchange slots (NG groups x 2 slots x 4 warps x 64 B), q scales
-    // (NG x 8 floats), the TMEM address, then 4 NG + 2 barriers (8-byte aligned)
+    // TC scratch: exchange slots, q scales, the TMEM address, barriers
     const uint32_t tcx = (sbase + Cfg::OFF_TCX + 15u) & ~15u;
-    const uint32_t tcbar = tcx + 1680;
-    static_assert(!Cfg::TC || (Cfg::NG <= 3 && 1680 + (4 * Cfg::NG + 2) * 8 + 15 <= Cfg::TCX),
-                  "TC scratch layout");
+    const uint32_t tcbar = tcx + Cfg::TCX_BAR;
     TileMeta *meta = reinterpret_cast<TileMeta *>(smem + Cfg::OFF_META);
     const uint32_t full0 = sbase + Cfg::OFF_FULL;
     const uint32_t empty0 = sbase + Cfg::OFF_EMPTY;
@@ -1599,8 +1591,10 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         // and the math warps never see stale or garbage rows.
         // LA = 4: the loop body is unrolled LA times and its code size shows
         // in the instruction fetch (measured on the Llama-shaped step: 8 tiles
-        // ahead 118.7 us, 6: 114.3, 4: 114.1, 3: 113.9, 2: 116.4 us)
-        constexpr int LA = 4;
+        // ahead 118.7 us, 6: 114.3, 4: 114.1, 3: 113.9, 2: 116.4 us). The
+        // tensor-core E4M3 variant, whose twelve math warps run more code,
+        // takes 2 (its step 73.6 -> 70.9 us).
+        constexpr int LA = Cfg::TC ? 2 : 4;
         constexpr int CPR = Cfg::ROWB / 16;          // 16-byte chunks per K/V row
         constexpr int CPRQ = Cfg::QROWB / 16;        // 16-byte chunks per q row
         const int pt = tid - Cfg::CW * 32;            // 0 .. kProducerThreads-1
@@ -1832,7 +1826,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
     // and frees them once every math warp has arrived on the done barrier,
     // on every way out of the loop below
     uint32_t tmem_base = 0;
-    const uint32_t tslot = tcx + 1664;
+    const uint32_t tslot = tcx + Cfg::TCX_TSLOT;
     const uint32_t bar_tready = tcbar + 8 * (4 * Cfg::NG), bar_done = bar_tready + 8;
     auto tc_leave = [&]() {
         if constexpr (Cfg::TC) {
@@ -1872,7 +1866,7 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         cs.qp = sbase + Cfg::OFF_TC + 8192 * cs.g;
         cs.pb = cs.qp + 4096;
         cs.xbuf = tcx + 512 * cs.g;
-        cs.qsc = tcx + 1536 + 32 * cs.g;
+        cs.qsc = tcx + Cfg::TCX_QSC + 32 * cs.g;
         cs.barS = tb + 8 * (0 * Cfg::NG + cs.g);
         cs.barO = tb + 8 * (1 * Cfg::NG + cs.g);
         cs.barX = tb + 8 * (2 * Cfg::NG + cs.g);
