@@ -942,7 +942,11 @@ def run_ours(args):
                                             row_bytes} if args.flat else {}),
                    **({"kv_cache": f"{args.kv_quant} codes + fp32 row scales "
                                    f"({row_bytes} B per token and kv head for K, same for V); "
-                                   f"{spec.dtype} activations; fp16 tensor-core math"}
+                                   f"{spec.dtype} activations; "
+                                   + ("tcgen05 kind::f8f6f4 products (codes as E4M3 operands, q "
+                                      "and p as three E4M3 parts, fp32 accumulators in TMEM)"
+                                      if args.kv_quant == "fp8_e4m3" else
+                                      "codes to fp16 in registers, mma.sync")}
                       if args.kv_quant else {}),
                    "l2": f"inputs > L2: the step cycles through {len(copies)} resident copies "
                          f"of the cache ({len(copies)} x {2 * st.num_blocks * spec.num_kv_heads * spec.block_size * row_bytes / 1e9:.2f} GB)",

@@ -271,20 +271,18 @@ __device__ __forceinline__ void lds_vec(uint32_t addr, float (&out)[N]) {
 // 8-bit codes -> fp16 (exact: every int8 and E4M3 value is an fp16 value)
 // ---------------------------------------------------------------------------
 // Four codes (lowest address in the low byte) -> two fp16 pairs.
+// The bias int8 codes carry into the fp16 mma operands.
+constexpr float kInt8Bias = 1152.f;
+
 template <int QK>
 __device__ __forceinline__ void codes_to_f16(uint32_t w, uint32_t &lo, uint32_t &hi) {
     if constexpr (QK == kQuantInt8) {
         // byte b + 128 placed under the fp16 exponent of 1024 (0x64nn) reads
-        // as 1024 + b + 128; subtracting 1152 leaves b exactly
+        // as b + 1152 exactly; the products keep that bias, and the scores and
+        // outputs take it off (kInt8Bias times the sum of q, resp. of p)
         const uint32_t u = w ^ 0x80808080u;
-        uint32_t a, b;
-        asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
-        asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
-        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-        __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
-        __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
-        lo = *reinterpret_cast<uint32_t *>(&ha);
-        hi = *reinterpret_cast<uint32_t *>(&hb);
+        asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+        asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
     } else {
         const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w & 0xffffu), __NV_E4M3);
         const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w >> 16), __NV_E4M3);
@@ -493,6 +491,10 @@ struct Consumer<T, D, GMAX, true, QK> {
     float scale_log2;
     float sl2[NTN][2];  // 8-bit caches: score factor of this thread's score heads
     float sigma;        // 8-bit caches: the accumulator holds o / sigma
+    // int8 caches: kInt8Bias x sum_d q of this thread's score heads, and this
+    // thread's share of sum_t p' (the fp16 parts the PV product used) of its
+    // score heads, scaled with the accumulator
+    float qsb[NTN][2], ps[NTN][2];
 
     __device__ __forceinline__ void reset() {
         sigma = 0.f;
@@ -502,6 +504,7 @@ struct Consumer<T, D, GMAX, true, QK> {
             for (int hh = 0; hh < 2; ++hh) {
                 m[nt][hh] = -CUDART_INF_F;
                 l[nt][hh] = 0.f;
+                ps[nt][hh] = 0.f;
             }
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks)
@@ -565,12 +568,29 @@ struct Consumer<T, D, GMAX, true, QK> {
                         __half2 q2 = __floats2half2_rn(x.x * mul, x.y * mul);
                         qb[nt][ks][half] = *reinterpret_cast<uint32_t *>(&q2);
                     }
+                // int8: sum of head h's fp16 q elements (the four lanes of h)
+                float qs = 0.f;
+                if constexpr (QK == kQuantInt8) {
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const float2 x = __half22float2(
+                                *reinterpret_cast<const __half2 *>(&qb[nt][ks][half]));
+                            qs += x.x + x.y;
+                        }
+                    qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+                    qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+                }
                 // score heads of this thread: 8nt + 2(lane%4) + hh, whose shift
-                // sits with lanes 4 * (2(lane%4) + hh)
+                // (and q sum) sits with lanes 4 * (2(lane%4) + hh)
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int es = __shfl_sync(0xffffffffu, e, ((lane & 3) * 2 + hh) * 4);
+                    const int src = ((lane & 3) * 2 + hh) * 4;
+                    const int es = __shfl_sync(0xffffffffu, e, src);
                     sl2[nt][hh] = scale_log2 * __uint_as_float((uint32_t)(127 + es) << 23);
+                    if constexpr (QK == kQuantInt8)
+                        qsb[nt][hh] = kInt8Bias * __shfl_sync(0xffffffffu, qs, src);
                 }
             }
         }
@@ -680,8 +700,13 @@ struct Consumer<T, D, GMAX, true, QK> {
             for (int hh = 0; hh < 2; ++hh) {
                 const float fa = QK != 0 ? ksA * sl2[nt][hh] : scale_log2;
                 const float fb = QK != 0 ? ksB * sl2[nt][hh] : scale_log2;
-                const float sa = vA ? s[nt][hh] * fa : -CUDART_INF_F;
-                const float sb = vB ? s[nt][2 + hh] * fb : -CUDART_INF_F;
+                float sva = s[nt][hh], svb = s[nt][2 + hh];
+                if constexpr (QK == kQuantInt8) {   // the codes' bias off the scores
+                    sva -= qsb[nt][hh];
+                    svb -= qsb[nt][hh];
+                }
+                const float sa = vA ? sva * fa : -CUDART_INF_F;
+                const float sb = vB ? svb * fb : -CUDART_INF_F;
                 float mx = fmaxf(sa, sb);
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -698,6 +723,7 @@ struct Consumer<T, D, GMAX, true, QK> {
                     acc[ks][nt][hh] *= ar;
                     acc[ks][nt][2 + hh] *= ar;
                 }
+                if constexpr (QK == kQuantInt8) ps[nt][hh] *= ar;
                 if constexpr (QK != 0) {   // p' = p * s_v / vmax for the PV product
                     p[nt][hh] *= fvA;
                     p[nt][2 + hh] *= fvB;
@@ -713,9 +739,13 @@ struct Consumer<T, D, GMAX, true, QK> {
             float r00, r01, r10, r11;
             const uint32_t hA = Elem<MT>::pack2(p[nt][0], p[nt][1], r00, r01);
             const uint32_t hB = Elem<MT>::pack2(p[nt][2], p[nt][3], r10, r11);
-            float d0, d1;
-            const uint32_t lA = Elem<MT>::pack2(p[nt][0] - r00, p[nt][1] - r01, d0, d1);
-            const uint32_t lB = Elem<MT>::pack2(p[nt][2] - r10, p[nt][3] - r11, d0, d1);
+            float d00, d01, d10, d11;
+            const uint32_t lA = Elem<MT>::pack2(p[nt][0] - r00, p[nt][1] - r01, d00, d01);
+            const uint32_t lB = Elem<MT>::pack2(p[nt][2] - r10, p[nt][3] - r11, d10, d11);
+            if constexpr (QK == kQuantInt8) {   // the p' values the product uses, per head
+                ps[nt][0] += (r00 + d00) + (r10 + d10);
+                ps[nt][1] += (r01 + d01) + (r11 + d11);
+            }
             const uint32_t offA = (lane >> 2) * 16 + (lane & 3) * 4;
             const uint32_t offB = offA + 8 * 16;
             asm volatile("st.shared.u32 [%0], %1;" ::"r"(hi + offA), "r"(hA) : "memory");
@@ -786,6 +816,20 @@ struct Consumer<T, D, GMAX, true, QK> {
                 }
             }
             const float sg = QK != 0 ? sigma : 1.f;
+            // int8: kInt8Bias x sum_t p' of heads 2(lane%4) and + 1 (their
+            // eight lanes' shares) comes off every element of those heads
+            float b0 = 0.f, b1 = 0.f;
+            if constexpr (QK == kQuantInt8) {
+                b0 = ps[nt][0];
+                b1 = ps[nt][1];
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    b0 += __shfl_xor_sync(0xffffffffu, b0, o);
+                    b1 += __shfl_xor_sync(0xffffffffu, b1, o);
+                }
+                b0 *= kInt8Bias;
+                b1 *= kInt8Bias;
+            }
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const int h = nt * 8 + (lane & 3) * 2;
@@ -793,10 +837,10 @@ struct Consumer<T, D, GMAX, true, QK> {
                 const int d = QK != 0 ? 16 * (lane >> 2) + 2 * mt : mt * 16 + (lane >> 2);
                 const int dd = QK != 0 ? 1 : 8;
                 float *o = comb_o + (warp * GMAX + h) * D;
-                o[comb_col<true, QK>(h, d)] = acc[mt][nt][0] * sg;
-                o[D + comb_col<true, QK>(h + 1, d)] = acc[mt][nt][1] * sg;
-                o[comb_col<true, QK>(h, d + dd)] = acc[mt][nt][2] * sg;
-                o[D + comb_col<true, QK>(h + 1, d + dd)] = acc[mt][nt][3] * sg;
+                o[comb_col<true, QK>(h, d)] = (acc[mt][nt][0] - b0) * sg;
+                o[D + comb_col<true, QK>(h + 1, d)] = (acc[mt][nt][1] - b1) * sg;
+                o[comb_col<true, QK>(h, d + dd)] = (acc[mt][nt][2] - b0) * sg;
+                o[D + comb_col<true, QK>(h + 1, d + dd)] = (acc[mt][nt][3] - b1) * sg;
             }
         }
     }
@@ -1592,9 +1636,9 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), 1)
         // LA = 4: the loop body is unrolled LA times and its code size shows
         // in the instruction fetch (measured on the Llama-shaped step: 8 tiles
         // ahead 118.7 us, 6: 114.3, 4: 114.1, 3: 113.9, 2: 116.4 us). The
-        // tensor-core E4M3 variant, whose twelve math warps run more code,
-        // takes 2 (its step 73.6 -> 70.9 us).
-        constexpr int LA = Cfg::TC ? 2 : 4;
+        // 8-bit variants, whose math warps run more code, take 2 (the
+        // tensor-core E4M3 step 73.6 -> 70.9 us, the int8 step 89.9 -> 88.6 us).
+        constexpr int LA = QK != 0 ? 2 : 4;
         constexpr int CPR = Cfg::ROWB / 16;          // 16-byte chunks per K/V row
         constexpr int CPRQ = Cfg::QROWB / 16;        // 16-byte chunks per q row
         const int pt = tid - Cfg::CW * 32;            // 0 .. kProducerThreads-1
