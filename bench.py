@@ -481,8 +481,9 @@ class PoolsQ:
     def prepared(self, q, kn, vn, slots, tables, lens, scale, out, ws, consumer=0,
                  pending_tail=0):
         from paged_kv_cache_47_gb300 import binding
-        # pending_tail is not used here: on the 8-bit path, which its math
-        # warps bound, overlapping the next call's start measured 1.7 % slower
+        # pending_tail is not used here: on the 8-bit path, overlapping the
+        # next call's start measured 1.7 % slower (mma.sync) and the tensor-core
+        # E4M3 step 69.3 -> 69.9 us; int8 88.7 us either way
         return (binding.PreparedAppendQuant(kn, vn, slots, self.cache),
                 binding.PreparedDecodeQuant(q, self.cache, tables, lens, scale, out, ws,
                                             tables_ready=True))
