@@ -484,7 +484,7 @@ class PoolsQ:
         # pending_tail is not used here: on the 8-bit path, overlapping the
         # next call's start measured 1.7 % slower (mma.sync) and the tensor-core
         # E4M3 step 69.3 -> 69.9 us; int8 88.7 us either way
-        return (binding.PreparedAppendQuant(kn, vn, slots, self.cache),
+        return (binding.PreparedAppendQuant(kn, vn, slots, self.cache, inputs_ready=True),
                 binding.PreparedDecodeQuant(q, self.cache, tables, lens, scale, out, ws,
                                             tables_ready=True))
 
@@ -930,7 +930,7 @@ def run_ours(args):
         "config": {**workload_config(spec, st,
                                      pending=not (cow is not None or args.kv_quant or
                                                   args.prefix_aware),
-                                     inputs_ready=not (args.kv_quant or args.flat),
+                                     inputs_ready=not args.flat,
                                      fused=fused),
                    **({"decode": "prefix-aware: the shared prefix decoded once per unit of "
                                  "several sharers' heads, each suffix apart, merged by "

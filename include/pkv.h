@@ -433,6 +433,16 @@ pkv_status pkv_append_quant(const pkv_qcache_desc *cache, const void *k_new, con
                             const int64_t *slot_mapping, int32_t num_tokens, void *k_codes,
                             void *v_codes, float *k_scales, float *v_scales, void *stream);
 
+/* pkv_append_quant with options (NULL = defaults). Same contract. With
+ * inputs_ready (see pkv_append_options) each row is read and quantized before
+ * the call waits for the preceding kernel on `stream`; only the code and
+ * scale stores wait for it. */
+pkv_status pkv_append_quant_ex(const pkv_qcache_desc *cache, const void *k_new,
+                               const void *v_new, const int64_t *slot_mapping,
+                               int32_t num_tokens, void *k_codes, void *v_codes,
+                               float *k_scales, float *v_scales, void *stream,
+                               const pkv_append_options *options);
+
 /* Workspace bytes for pkv_decode_attention_quant with num_ctas CTAs (0 = the
  * default launch). Same contract as pkv_decode_workspace_bytes_ex. */
 size_t pkv_decode_quant_workspace_bytes(const pkv_qcache_desc *cache, int32_t num_q_heads,

@@ -139,6 +139,9 @@ def lib():
         qp = ctypes.POINTER(QCacheDesc)
         L.pkv_append_quant.argtypes = [qp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
         L.pkv_append_quant.restype = i32
+        L.pkv_append_quant_ex.argtypes = [qp, vp, vp, vp, i32, vp, vp, vp, vp, vp,
+                                          ctypes.POINTER(AppendOptions)]
+        L.pkv_append_quant_ex.restype = i32
         L.pkv_decode_quant_workspace_bytes.argtypes = [qp, i32, i32]
         L.pkv_decode_quant_workspace_bytes.restype = sz
         L.pkv_decode_attention_quant.argtypes = [qp, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp,
@@ -448,13 +451,17 @@ class QuantCache:
                 self.v_scales.data_ptr())
 
 
-def append_quant(k_new, v_new, slot_mapping, cache: QuantCache, stream=None) -> None:
-    """Quantize k_new/v_new [N][Hk][D] (the cache's activation dtype) into their slots."""
+def append_quant(k_new, v_new, slot_mapping, cache: QuantCache, stream=None,
+                 inputs_ready: bool = False) -> None:
+    """Quantize k_new/v_new [N][Hk][D] (the cache's activation dtype) into their slots
+    (inputs_ready: see append)."""
     k_new, v_new = k_new.contiguous(), v_new.contiguous()
     sm = slot_mapping.contiguous()
     assert sm.dtype == torch.int64 and k_new.dtype == cache.act_dtype == v_new.dtype
-    _check(lib().pkv_append_quant(ctypes.byref(cache.desc), _ptr(k_new), _ptr(v_new), _ptr(sm),
-                                  sm.numel(), *cache.pointers(), _stream(stream)))
+    opts = AppendOptions(int(inputs_ready))
+    _check(lib().pkv_append_quant_ex(ctypes.byref(cache.desc), _ptr(k_new), _ptr(v_new), _ptr(sm),
+                                     sm.numel(), *cache.pointers(), _stream(stream),
+                                     ctypes.byref(opts)))
 
 
 def quant_workspace_bytes(cache: QuantCache, num_q_heads: int, num_ctas: int = 0) -> int:
@@ -538,18 +545,19 @@ class PreparedDecodeQuant:
 class PreparedAppendQuant:
     """pkv_append_quant with its arguments marshalled once (see PreparedDecode)."""
 
-    def __init__(self, k_new, v_new, slot_mapping, cache: QuantCache):
+    def __init__(self, k_new, v_new, slot_mapping, cache: QuantCache, inputs_ready: bool = False):
         for t in (k_new, v_new, slot_mapping):
             if not t.is_contiguous():
                 raise ValueError("prepared append needs contiguous tensors")
         assert slot_mapping.dtype == torch.int64 and k_new.dtype == cache.act_dtype
         self._keep = (k_new, v_new, slot_mapping, cache)
+        self._opts = AppendOptions(int(inputs_ready))
         self._args = (ctypes.byref(cache.desc), k_new.data_ptr(), v_new.data_ptr(),
                       slot_mapping.data_ptr(), slot_mapping.numel(), *cache.pointers())
-        self._fn = lib().pkv_append_quant
+        self._fn = lib().pkv_append_quant_ex
 
     def __call__(self, stream) -> None:
-        _check(self._fn(*self._args, _stream(stream)))
+        _check(self._fn(*self._args, _stream(stream), ctypes.byref(self._opts)))
 
 
 def block_copy_quant(pairs, cache: QuantCache, stream=None) -> None:

@@ -639,6 +639,15 @@ size_t pkv_decode_quant_workspace_bytes(const pkv_qcache_desc *cache, int32_t nu
 pkv_status pkv_append_quant(const pkv_qcache_desc *cache, const void *k_new, const void *v_new,
                             const int64_t *slot_mapping, int32_t num_tokens, void *k_codes,
                             void *v_codes, float *k_scales, float *v_scales, void *stream) {
+    return pkv_append_quant_ex(cache, k_new, v_new, slot_mapping, num_tokens, k_codes, v_codes,
+                               k_scales, v_scales, stream, nullptr);
+}
+
+pkv_status pkv_append_quant_ex(const pkv_qcache_desc *cache, const void *k_new,
+                               const void *v_new, const int64_t *slot_mapping,
+                               int32_t num_tokens, void *k_codes, void *v_codes,
+                               float *k_scales, float *v_scales, void *stream,
+                               const pkv_append_options *options) {
     pkv_status st = check_qcache(cache);
     if (st != PKV_OK) return st;
     if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
@@ -654,7 +663,8 @@ pkv_status pkv_append_quant(const pkv_qcache_desc *cache, const void *k_new, con
     cudaError_t e = pkv::launch_append_quant(cache->code_dtype, cache->act_dtype, k_new, v_new,
                                              slot_mapping, num_tokens, k_codes, v_codes, k_scales,
                                              v_scales, cache->num_blocks, cache->num_kv_heads,
-                                             cache->block_size, err,
+                                             cache->block_size,
+                                             options && options->inputs_ready ? 1 : 0, err,
                                              static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "quantized append launch");
     return PKV_OK;

@@ -192,7 +192,8 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
 cudaError_t launch_append_quant(int code_dtype, int act_dtype, const void *k_new,
                                 const void *v_new, const int64_t *slots, int num_tokens,
                                 void *k_codes, void *v_codes, float *k_scales, float *v_scales,
-                                int NB, int Hk, int B, unsigned *err, cudaStream_t st);
+                                int NB, int Hk, int B, int inputs_ready, unsigned *err,
+                                cudaStream_t st);
 
 constexpr int kCopyPairsPerLaunch = 128;
 struct CopyPairs {

@@ -205,9 +205,12 @@ def test_decode_quant_tables_ready_matches_default(kind):
     outs = []
     # pending_tail 1: every row but the appended one is gathered while the
     # append may still run
-    for ready, pend in ((False, 0), (True, 0), (True, 1)):
+    # inputs_ready: the append reads and quantizes its rows before it waits
+    # for the preceding decode, and only its stores wait
+    for ready, pend, inp in ((False, 0, False), (True, 0, False), (True, 1, False),
+                             (True, 0, True), (True, 1, True)):
         for _ in range(3):
-            binding.append_quant(kn, vn, sl, gpu)
+            binding.append_quant(kn, vn, sl, gpu, inputs_ready=inp)
             out = binding.decode_attention_quant(q, gpu, tab, lens, scale, out_dtype=torch.float32,
                                                  num_ctas=7, tables_ready=ready,
                                                  pending_tail=pend)
@@ -240,9 +243,31 @@ def test_block_copy_quant_is_byte_exact(kind):
         binding.block_copy_quant([[used[0], free[0]], [used[1], free[0]]], gpu)
 
 
+@pytest.mark.parametrize("kind", KINDS)
+def test_append_quant_inputs_ready_is_bit_exact(kind):
+    # the inputs-ready form (rows quantized before the wait on the preceding
+    # kernel, several rows per warp when the grid is full) writes the same
+    # codes and scales as the oracle
+    # 7695 tokens x 8 kv heads: more rows than the 4096 x 8 warps of a full grid
+    lengths = RAGGED + [3000, 2000]
+    spec = W.WorkloadSpec("q", len(lengths), 32, 8, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=58, lengths=lengths)
+    NB, Hk, B, D = vals["k_pool"].shape
+    kr, vr, sl = _token_rows(st, vals)
+    ref = _empty_pools(NB, Hk, B, D, "cpu")
+    oracle.append_quant(kind, kr, vr, sl, *ref)
+    gpu = binding.QuantCache(*_empty_pools(NB, Hk, B, D, "cuda"), kind, kr.dtype)
+    binding.append_quant(kr.cuda(), vr.cuda(), sl.cuda(), gpu, inputs_ready=True)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    assert_same_cache(ref, gpu)
+
+
 def test_append_quant_out_of_pool_slot_sets_error_word():
     gpu = binding.QuantCache.empty(2, 1, 16, 128, "int8", torch.float16)
     kn = torch.randn(2, 1, 128, device="cuda").to(torch.float16)
     binding.get_error()
     binding.append_quant(kn, kn, torch.tensor([0, 2 * 16], device="cuda"), gpu)
+    assert binding.get_error() == binding.DEVERR_SLOT
+    binding.append_quant(kn, kn, torch.tensor([0, 2 * 16], device="cuda"), gpu, inputs_ready=True)
     assert binding.get_error() == binding.DEVERR_SLOT
