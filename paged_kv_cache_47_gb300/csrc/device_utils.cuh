@@ -63,9 +63,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete, for at most
 // limit_ns. Returns false (and flags the error word) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err,
-                                          uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The waiting loop is out of line: inlined at every wait it made the kernels'
+// code larger, and their instruction fetch shows it (llama-shaped steps,
+// inline -> out of line: bf16 103.0 -> 102.7 us, E4M3 67.1 -> 66.1 us, int8
+// 86.3 -> 85.4 us).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, unsigned *err,
+                                                   uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -74,6 +77,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err,
+                                          uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, limit_ns);
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch
