@@ -443,6 +443,25 @@ pkv_status pkv_append_quant_ex(const pkv_qcache_desc *cache, const void *k_new,
                                float *k_scales, float *v_scales, void *stream,
                                const pkv_append_options *options);
 
+/*
+ * pkv_append_decode_attention_quant — pkv_append_decode_attention for an
+ * 8-bit cache: each sequence's new K/V row k_new[s] / v_new[s]
+ * ([num_seqs][num_kv_heads][head_dim] in act_dtype, 16-byte aligned) is
+ * quantized by the rule above (the same codes and scales as
+ * pkv_append_quant) and written to position context_lens[s] - 1 of its table
+ * row, and the decode attention (pkv_decode_attention_quant) runs over the
+ * context including it: the quantizing append, then the decode, on `stream`.
+ * The new rows are written after the preceding kernel on `stream` has
+ * completed. Other arguments, errors and workspace: as
+ * pkv_decode_attention_quant (and pkv_append_quant for the rows).
+ */
+pkv_status pkv_append_decode_attention_quant(
+    const pkv_qcache_desc *cache, const void *q, int32_t num_seqs, int32_t num_q_heads,
+    const void *k_new, const void *v_new, void *k_codes, void *v_codes, float *k_scales,
+    float *v_scales, const int32_t *block_tables, int32_t max_blocks_per_seq,
+    const int32_t *context_lens, float scale, void *out, int32_t out_dtype, void *workspace,
+    size_t workspace_bytes, void *stream, const pkv_decode_options *options);
+
 /* Workspace bytes for pkv_decode_attention_quant with num_ctas CTAs (0 = the
  * default launch). Same contract as pkv_decode_workspace_bytes_ex. */
 size_t pkv_decode_quant_workspace_bytes(const pkv_qcache_desc *cache, int32_t num_q_heads,

@@ -148,6 +148,10 @@ def lib():
                                                  ctypes.c_float, vp, i32, vp, sz, vp,
                                                  ctypes.POINTER(DecodeOptions)]
         L.pkv_decode_attention_quant.restype = i32
+        L.pkv_append_decode_attention_quant.argtypes = [qp, vp, i32, i32, vp, vp, vp, vp, vp, vp,
+                                                        vp, i32, vp, ctypes.c_float, vp, i32, vp,
+                                                        sz, vp, ctypes.POINTER(DecodeOptions)]
+        L.pkv_append_decode_attention_quant.restype = i32
         L.pkv_block_copy_quant.argtypes = [qp, vp, i32, vp, vp, vp, vp, vp]
         L.pkv_block_copy_quant.restype = i32
         L.pkv_decode_prefix_workspace_bytes.argtypes = [dp, i32, i32, i32,
@@ -532,6 +536,71 @@ class PreparedDecodeQuant:
                       float(scale), out.data_ptr(), DTYPE_CODE[out.dtype], workspace.data_ptr(),
                       workspace.numel())
         self._fn = lib().pkv_decode_attention_quant
+        self.out = out
+
+    def __call__(self, stream, timing_events: Optional[Sequence] = None) -> None:
+        opts = self._opts
+        for i in range(2):
+            ev = timing_events[i] if timing_events is not None else None
+            opts.timing_events[i] = None if ev is None else ev.cuda_event
+        _check(self._fn(*self._args, _stream(stream), ctypes.byref(opts)))
+
+
+def append_decode_attention_quant(q, k_new, v_new, cache: QuantCache, block_tables,
+                                  context_lens, scale: float, out: Optional[torch.Tensor] = None,
+                                  out_dtype: Optional[torch.dtype] = None,
+                                  workspace: Optional[torch.Tensor] = None, num_ctas: int = 0,
+                                  stream=None, tables_ready: bool = False,
+                                  pending_tail: int = 0) -> torch.Tensor:
+    """One decode step over an 8-bit cache (pkv_append_decode_attention_quant):
+    each sequence's new row k_new[s] / v_new[s] [S][Hk][D] is quantized into
+    position context_lens[s] - 1 of its table row, and the attention runs over
+    the context including it."""
+    S, Hq, D = q.shape
+    q, k_new, v_new = q.contiguous(), k_new.contiguous(), v_new.contiguous()
+    bt, cl = block_tables.contiguous(), context_lens.contiguous()
+    assert bt.dtype == torch.int32 and cl.dtype == torch.int32
+    assert q.dtype == k_new.dtype == v_new.dtype == cache.act_dtype
+    if out is None:
+        out = torch.empty(S, Hq, D, dtype=out_dtype or q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_quant_workspace(cache, Hq, num_ctas)
+    opts = DecodeOptions()
+    opts.num_ctas = num_ctas
+    opts.tables_ready = int(tables_ready)
+    opts.pending_tail = int(pending_tail)
+    _check(lib().pkv_append_decode_attention_quant(
+        ctypes.byref(cache.desc), _ptr(q), S, Hq, _ptr(k_new), _ptr(v_new), *cache.pointers(),
+        _ptr(bt), bt.shape[1], _ptr(cl), float(scale), _ptr(out), DTYPE_CODE[out.dtype],
+        _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(opts)))
+    return out
+
+
+class PreparedAppendDecodeQuant:
+    """pkv_append_decode_attention_quant with its arguments marshalled once (see
+    PreparedDecode)."""
+
+    def __init__(self, q, k_new, v_new, cache: QuantCache, block_tables, context_lens,
+                 scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                 num_ctas: int = 0, tables_ready: bool = False, pending_tail: int = 0):
+        for t in (q, k_new, v_new, block_tables, context_lens, out):
+            if not t.is_contiguous():
+                raise ValueError("prepared decode needs contiguous tensors")
+        assert q.dtype == k_new.dtype == v_new.dtype == cache.act_dtype
+        S, Hq, D = q.shape
+        if workspace is None:
+            workspace = alloc_quant_workspace(cache, Hq, num_ctas)
+        self._keep = (q, k_new, v_new, cache, block_tables, context_lens, out, workspace)
+        self._opts = DecodeOptions()
+        self._opts.num_ctas = num_ctas
+        self._opts.tables_ready = int(tables_ready)
+        self._opts.pending_tail = int(pending_tail)
+        self._args = (ctypes.byref(cache.desc), q.data_ptr(), S, Hq, k_new.data_ptr(),
+                      v_new.data_ptr(), *cache.pointers(), block_tables.data_ptr(),
+                      block_tables.shape[1], context_lens.data_ptr(), float(scale),
+                      out.data_ptr(), DTYPE_CODE[out.dtype], workspace.data_ptr(),
+                      workspace.numel())
+        self._fn = lib().pkv_append_decode_attention_quant
         self.out = out
 
     def __call__(self, stream, timing_events: Optional[Sequence] = None) -> None:

@@ -20,6 +20,7 @@
 #include <stdint.h>
 
 #include "pkv_internal.h"
+#include "quant_codec.cuh"
 
 namespace pkv {
 
@@ -32,52 +33,13 @@ __device__ __forceinline__ void allow_next_grid() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-template <typename T>
-__device__ __forceinline__ float act_to_f32(T x);
-template <>
-__device__ __forceinline__ float act_to_f32<__half>(__half x) { return __half2float(x); }
-template <>
-__device__ __forceinline__ float act_to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
-    return __bfloat162float(x);
-}
-
-// One code of x / s (s > 0).
-template <int CODE>
-__device__ __forceinline__ uint32_t encode(float x, float s) {
-    const float v = __fdiv_rn(x, s);
-    if constexpr (CODE == PKV_INT8) {
-        int c = __float2int_rn(v);
-        c = c > 127 ? 127 : (c < -127 ? -127 : c);
-        return (uint32_t)(uint8_t)(int8_t)c;
-    } else {
-        return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-    }
-}
-
 // The row `src` (D = 128 elements of T) quantized: this lane's four codes
 // (one 32-bit word) and the row's scale.
 template <typename T, int CODE>
 __device__ __forceinline__ void quantize_row(const T *__restrict__ src, uint32_t &word_out,
                                              float &scale_out, int lane) {
-    constexpr float kQmax = CODE == PKV_INT8 ? 127.f : 448.f;
-    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(src) + lane);
-    const T *e = reinterpret_cast<const T *>(&raw);
-    float x[4], a = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[i] = act_to_f32<T>(e[i]);
-        a = fmaxf(a, fabsf(x[i]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const float s = __fdiv_rn(a, kQmax);
-    uint32_t word = 0;
-    if (a != 0.f) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) word |= encode<CODE>(x[i], s) << (8 * i);
-    }
-    word_out = word;
-    scale_out = s;
+    quantize_lane4<T, CODE>(__ldg(reinterpret_cast<const uint2 *>(src) + lane), word_out,
+                            scale_out);
 }
 
 // One (token, kv head) row quantized, waiting to be stored.
@@ -87,15 +49,31 @@ struct QRow {
     float ks = 0.f, vs = 0.f;
 };
 
+// The slot of token tok: slots[tok], or (slots NULL) position lens[tok] - 1
+// of table row tok (-1 for an empty context or a block id outside the pool,
+// which the decode flags).
+__device__ __forceinline__ int64_t token_slot(const int64_t *slots, const int32_t *tables,
+                                              const int32_t *lens, int M, int B, int NB, int tok) {
+    if (slots) return __ldg(slots + tok);
+    int L = __ldg(lens + tok);
+    if (L > M * B) L = M * B;
+    if (L <= 0) return -1;
+    const int blk = __ldg(tables + (size_t)tok * M + (L - 1) / B);
+    if (blk < 0 || blk >= NB) return -1;
+    return (int64_t)blk * B + (L - 1) % B;
+}
+
 template <typename T, int CODE>
 __device__ __forceinline__ QRow quantize_token_row(const T *__restrict__ k_new,
                                                    const T *__restrict__ v_new,
-                                                   const int64_t *__restrict__ slots, int64_t r,
-                                                   int NB, int Hk, int B, unsigned *err, int lane) {
+                                                   const int64_t *__restrict__ slots,
+                                                   const int32_t *tables, const int32_t *lens,
+                                                   int M, int64_t r, int NB, int Hk, int B,
+                                                   unsigned *err, int lane) {
     constexpr int D = 128;
     QRow q;
     const int tok = (int)(r / Hk), g = (int)(r - (int64_t)tok * Hk);
-    const int64_t slot = __ldg(slots + tok);
+    const int64_t slot = token_slot(slots, tables, lens, M, B, NB, tok);
     if (slot < 0) return q;
     const int64_t blk = slot / B;
     const int off = (int)(slot - blk * B);
@@ -129,9 +107,9 @@ __device__ __forceinline__ void store_row(const QRow &q, uint8_t *__restrict__ k
 template <typename T, int CODE>
 __global__ void __launch_bounds__(256) append_quant_kernel(
     const T *__restrict__ k_new, const T *__restrict__ v_new, const int64_t *__restrict__ slots,
-    int num_tokens, uint8_t *__restrict__ k_codes, uint8_t *__restrict__ v_codes,
-    float *__restrict__ k_scales, float *__restrict__ v_scales, int NB, int Hk, int B,
-    int inputs_ready, unsigned *err) {
+    const int32_t *__restrict__ tables, const int32_t *__restrict__ lens, int M, int num_tokens,
+    uint8_t *__restrict__ k_codes, uint8_t *__restrict__ v_codes, float *__restrict__ k_scales,
+    float *__restrict__ v_scales, int NB, int Hk, int B, int inputs_ready, unsigned *err) {
     // programmatic serialisation: the previous kernel on the stream completes
     // before any pool byte is touched; the next one may be scheduled meanwhile
     allow_next_grid();
@@ -141,17 +119,22 @@ __global__ void __launch_bounds__(256) append_quant_kernel(
     int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     QRow first;
     const bool early = inputs_ready && r < rows;
-    if (early) first = quantize_token_row<T, CODE>(k_new, v_new, slots, r, NB, Hk, B, err, lane);
+    if (early)
+        first = quantize_token_row<T, CODE>(k_new, v_new, slots, tables, lens, M, r, NB, Hk, B, err,
+                                            lane);
     wait_prior_grid();
     for (bool have = early; r < rows; r += warps, have = false) {
         const QRow q =
-            have ? first : quantize_token_row<T, CODE>(k_new, v_new, slots, r, NB, Hk, B, err, lane);
+            have ? first
+                 : quantize_token_row<T, CODE>(k_new, v_new, slots, tables, lens, M, r, NB, Hk, B,
+                                               err, lane);
         store_row(q, k_codes, v_codes, k_scales, v_scales, lane);
     }
 }
 
 template <typename T, int CODE>
-cudaError_t launch(const void *k_new, const void *v_new, const int64_t *slots, int num_tokens,
+cudaError_t launch(const void *k_new, const void *v_new, const int64_t *slots,
+                   const int32_t *tables, const int32_t *lens, int M, int num_tokens,
                    void *k_codes, void *v_codes, float *k_scales, float *v_scales, int NB, int Hk,
                    int B, int inputs_ready, unsigned *err, cudaStream_t st) {
     const int64_t rows = (int64_t)num_tokens * Hk;
@@ -167,7 +150,7 @@ cudaError_t launch(const void *k_new, const void *v_new, const int64_t *slots, i
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, append_quant_kernel<T, CODE>, static_cast<const T *>(k_new),
-                              static_cast<const T *>(v_new), slots, num_tokens,
+                              static_cast<const T *>(v_new), slots, tables, lens, M, num_tokens,
                               static_cast<uint8_t *>(k_codes), static_cast<uint8_t *>(v_codes),
                               k_scales, v_scales, NB, Hk, B, inputs_ready, err);
 }
@@ -178,21 +161,14 @@ cudaError_t launch_append_quant(int code_dtype, int act_dtype, const void *k_new
                                 const void *v_new, const int64_t *slots, int num_tokens,
                                 void *k_codes, void *v_codes, float *k_scales, float *v_scales,
                                 int NB, int Hk, int B, int inputs_ready, unsigned *err,
-                                cudaStream_t st) {
-    if (act_dtype == PKV_F16)
-        return code_dtype == PKV_INT8
-                   ? launch<__half, PKV_INT8>(k_new, v_new, slots, num_tokens, k_codes, v_codes,
-                                              k_scales, v_scales, NB, Hk, B, inputs_ready, err, st)
-                   : launch<__half, PKV_FP8_E4M3>(k_new, v_new, slots, num_tokens, k_codes,
-                                                  v_codes, k_scales, v_scales, NB, Hk, B,
-                                                  inputs_ready, err, st);
-    return code_dtype == PKV_INT8
-               ? launch<__nv_bfloat16, PKV_INT8>(k_new, v_new, slots, num_tokens, k_codes, v_codes,
-                                                 k_scales, v_scales, NB, Hk, B, inputs_ready, err,
-                                                 st)
-               : launch<__nv_bfloat16, PKV_FP8_E4M3>(k_new, v_new, slots, num_tokens, k_codes,
-                                                     v_codes, k_scales, v_scales, NB, Hk, B,
-                                                     inputs_ready, err, st);
+                                cudaStream_t st, const int32_t *tables, const int32_t *lens,
+                                int M) {
+    auto *L = act_dtype == PKV_F16
+                  ? (code_dtype == PKV_INT8 ? &launch<__half, PKV_INT8> : &launch<__half, PKV_FP8_E4M3>)
+                  : (code_dtype == PKV_INT8 ? &launch<__nv_bfloat16, PKV_INT8>
+                                            : &launch<__nv_bfloat16, PKV_FP8_E4M3>);
+    return L(k_new, v_new, slots, tables, lens, M, num_tokens, k_codes, v_codes, k_scales,
+             v_scales, NB, Hk, B, inputs_ready, err, st);
 }
 
 }  // namespace pkv

@@ -189,11 +189,14 @@ cudaError_t launch_append(int dtype, const void *k_new, const void *v_new,
                           const int32_t *lens = nullptr, int M = 0);
 
 // 8-bit caches (append_quant.cu): D = 128.
+// slots NULL: token i is sequence i and its slot is position lens[i] - 1 of
+// its table row (tables [num_tokens][M])
 cudaError_t launch_append_quant(int code_dtype, int act_dtype, const void *k_new,
                                 const void *v_new, const int64_t *slots, int num_tokens,
                                 void *k_codes, void *v_codes, float *k_scales, float *v_scales,
                                 int NB, int Hk, int B, int inputs_ready, unsigned *err,
-                                cudaStream_t st);
+                                cudaStream_t st, const int32_t *tables = nullptr,
+                                const int32_t *lens = nullptr, int M = 0);
 
 constexpr int kCopyPairsPerLaunch = 128;
 struct CopyPairs {

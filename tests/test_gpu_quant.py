@@ -271,3 +271,80 @@ def test_append_quant_out_of_pool_slot_sets_error_word():
     assert binding.get_error() == binding.DEVERR_SLOT
     binding.append_quant(kn, kn, torch.tensor([0, 2 * 16], device="cuda"), gpu, inputs_ready=True)
     assert binding.get_error() == binding.DEVERR_SLOT
+
+
+def _base_and_step(kind, dtype, Hq, Hk, B, lengths, seed):
+    """A cache holding every context row but each sequence's newest, built the
+    same way on both sides, and that step's inputs."""
+    spec = W.WorkloadSpec("qf", len(lengths), Hq, Hk, 128, B, dtype, 1.0)
+    st, vals = W.make_workload(spec, seed=seed, lengths=lengths)
+    NB, Hk_, B_, D = vals["k_pool"].shape
+    kr, vr, sl = _token_rows(st, vals)
+    keep = ~torch.isin(sl, st.slot_mapping)          # not the newest rows
+    ref = _empty_pools(NB, Hk_, B_, D, "cpu")
+    oracle.append_quant(kind, kr[keep], vr[keep], sl[keep], *ref)
+    gpu = binding.QuantCache(*_empty_pools(NB, Hk_, B_, D, "cuda"), kind, kr.dtype)
+    binding.append_quant(kr[keep].cuda(), vr[keep].cuda(), sl[keep].cuda(), gpu)
+    torch.cuda.synchronize()
+    return st, vals, ref, gpu
+
+
+def _clone_cache(c):
+    return binding.QuantCache(c.k_codes.clone(), c.v_codes.clone(), c.k_scales.clone(),
+                              c.v_scales.clone(), c.code, c.act_dtype)
+
+
+@pytest.mark.parametrize("kind,dtype,Hq,Hk,B", [("fp8_e4m3", "bf16", 32, 8, 16),
+                                               ("fp8_e4m3", "f16", 64, 8, 8),
+                                               ("fp8_e4m3", "bf16", 16, 8, 32),
+                                               ("fp8_e4m3", "f16", 40, 2, 16),
+                                               ("int8", "bf16", 32, 8, 16)])
+@pytest.mark.parametrize("num_ctas", [0, 5, 300])
+def test_append_decode_attention_quant(kind, dtype, Hq, Hk, B, num_ctas):
+    # one step: the newest rows quantized into their slots (one launch for E4M3
+    # with up to 8 heads per kv head, append + decode otherwise). Pools bit-exact
+    # and output bitwise equal to pkv_append_quant + pkv_decode_attention_quant,
+    # and within tolerance of the oracle's append and decode
+    st, vals, ref, base = _base_and_step(kind, dtype, Hq, Hk, B, RAGGED, seed=61)
+    scale = 1.0 / math.sqrt(128)
+    q, kn, vn = vals["q"].cuda(), vals["k_new"].cuda(), vals["v_new"].cuda()
+    tab, lens = st.block_tables.cuda(), st.context_lens.cuda()
+    sep, fused = _clone_cache(base), _clone_cache(base)
+    binding.append_quant(kn, vn, st.slot_mapping.cuda(), sep)
+    want_gpu = binding.decode_attention_quant(q, sep, tab, lens, scale, out_dtype=torch.float32,
+                                              num_ctas=num_ctas)
+    got = binding.append_decode_attention_quant(q, kn, vn, fused, tab, lens, scale,
+                                                out_dtype=torch.float32, num_ctas=num_ctas)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+    assert torch.equal(fused.k_codes.cpu(), sep.k_codes.cpu())
+    assert torch.equal(fused.v_codes.cpu(), sep.v_codes.cpu())
+    assert torch.equal(fused.k_scales.cpu().view(torch.int32), sep.k_scales.cpu().view(torch.int32))
+    assert torch.equal(fused.v_scales.cpu().view(torch.int32), sep.v_scales.cpu().view(torch.int32))
+    assert torch.equal(got.cpu(), want_gpu.cpu())
+    oracle.append_quant(kind, vals["k_new"], vals["v_new"], st.slot_mapping, *ref)
+    assert_same_cache(ref, fused)
+    want = oracle.decode_quant(kind, vals["q"], *ref, st.block_tables, st.context_lens, scale)
+    assert_close(got.double().cpu().numpy(), want, f"{kind} {dtype} {Hq}/{Hk} B{B}")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_append_decode_attention_quant_chain(kind):
+    # steps in a row on one cache with the decode reading tables and lengths
+    # early and gathering all but the newest rows at once: the same bits each step
+    st, vals, ref, base = _base_and_step(kind, "bf16", 32, 8, 16, [0, 300, 129, 1000, 1], seed=62)
+    scale = 1.0 / math.sqrt(128)
+    q, kn, vn = vals["q"].cuda(), vals["k_new"].cuda(), vals["v_new"].cuda()
+    tab, lens = st.block_tables.cuda(), st.context_lens.cuda()
+    outs = []
+    for ready, pend in ((False, 0), (True, 1), (True, 2)):
+        for _ in range(3):
+            out = binding.append_decode_attention_quant(q, kn, vn, base, tab, lens, scale,
+                                                        out_dtype=torch.float32, num_ctas=7,
+                                                        tables_ready=ready, pending_tail=pend)
+        torch.cuda.synchronize()
+        assert binding.get_error() == 0
+        outs.append(out.cpu())
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+    assert torch.all(outs[0][0] == 0)
