@@ -118,14 +118,18 @@ struct SplitCfg {
     static constexpr int COMB_O = CWC * GMAX * D * 4;
     static constexpr int COMB_ML = 2 * CW * GMAX * 4;
     static constexpr int PBUF = (MMA && !TC) ? CW * NTN * 2 * 256 : 0;
-    // TC: per warp group, the q parts and the p parts (mma B operands, 4 KB
-    // each, 1024-byte aligned); then the max-exchange slots, q scales, the
-    // tensor-memory address and the group barriers
-    static constexpr int TCB = TC ? NG * 8192 : 0;
-    // exchange slots (per group 2 slots x 4 warps x 64 B), q scales (per group
-    // 8 floats), the TMEM address, then 4 NG + 2 barriers (8-byte aligned);
-    // the region starts 16-byte aligned
-    static constexpr int TCX_QSC = NG * 512;
+    // TC: per warp group, the q parts and the p parts (mma B operands,
+    // 1024-byte aligned; 2 KB each for units of up to 4 heads, 4 KB for 8);
+    // then the max-exchange slots, q scales, the tensor-memory address and the
+    // group barriers
+    static constexpr int TCG = GMAX <= 4 ? 4096 : 8192;   // bytes per group
+    static constexpr int TCB = TC ? NG * TCG : 0;
+    // exchange slots (per group 2 slots x 4 warps x XS bytes: GMAX maxima and
+    // the V scale maximum), q scales (per group 8 floats), the TMEM address,
+    // then 4 NG + 2 barriers (8-byte aligned); the region starts 16-byte aligned
+    static constexpr int XS = GMAX <= 4 ? 32 : 64;
+    static_assert(!TC || 4 * (GMAX + 1) <= XS, "exchange slot too small");
+    static constexpr int TCX_QSC = NG * 8 * XS;
     static constexpr int TCX_TSLOT = TCX_QSC + NG * 32;
     static constexpr int TCX_BAR = TCX_TSLOT + 16;
     static constexpr int TCX = TC ? ((TCX_BAR + (4 * NG + 2) * 8 + 16 + 255) / 256) * 256 : 0;
@@ -1067,7 +1071,8 @@ struct TcConsumer {
         // ---- the group's max of each head's scores and of the V row scales:
         // this warp's maxima to the exchange slot (heads 4j .. 4j + 3 reduced
         // together; lane 8i then holds head 4j + i)
-        const uint32_t slot = xbuf + (xph & 1u) * 4 * 64 + qw * 64;
+        constexpr int XS = GMAX <= 4 ? 32 : 64;   // exchange slot of one warp
+        const uint32_t slot = xbuf + (xph & 1u) * 4 * XS + qw * XS;
         const float m03 = warp_max4(s[0], s[1], s[2], s[3], lane);
         const float vmx = warp_max_f32(valid ? vs : 0.f);
         if ((lane & 7) == 0) sts_f32(slot + 4 * (lane >> 3), m03);
@@ -1079,14 +1084,14 @@ struct TcConsumer {
         }
         if (lane == 0) sts_f32(slot + 4 * GMAX, vmx);
         if (!gsync(lane)) return false;
-        const uint32_t slot0 = slot - qw * 64;
+        const uint32_t slot0 = slot - qw * XS;
         float M[GMAX + 1];
 #pragma unroll
         for (int h = 0; h <= GMAX; ++h) {
             M[h] = -CUDART_INF_F;
             if (h < GMAX && h >= gca) continue;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) M[h] = fmaxf(M[h], lds_f32(slot0 + w * 64 + 4 * h));
+            for (int w = 0; w < 4; ++w) M[h] = fmaxf(M[h], lds_f32(slot0 + w * XS + 4 * h));
         }
         float VM = M[GMAX];
         if (!(VM > 0.f)) VM = 1.f;   // all-zero V rows: p' = 0 whatever VM is
@@ -1918,9 +1923,9 @@ __global__ void __launch_bounds__(kernel_threads(QK, GMAX), two_ctas(QK, GMAX, M
         cs.issuer = cs.qw == 0;
         cs.tS = tmem_base + ((uint32_t)(cs.qw * 32) << 16) + 64 * cs.g;
         cs.tO = cs.tS + 32;
-        cs.qp = sbase + Cfg::OFF_TC + 8192 * cs.g;
-        cs.pb = cs.qp + 4096;
-        cs.xbuf = tcx + 512 * cs.g;
+        cs.qp = sbase + Cfg::OFF_TC + Cfg::TCG * cs.g;
+        cs.pb = cs.qp + Cfg::TCG / 2;
+        cs.xbuf = tcx + 8 * Cfg::XS * cs.g;
         cs.qsc = tcx + Cfg::TCX_QSC + 32 * cs.g;
         cs.barS = tb + 8 * (0 * Cfg::NG + cs.g);
         cs.barO = tb + 8 * (1 * Cfg::NG + cs.g);

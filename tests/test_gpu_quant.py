@@ -183,12 +183,26 @@ def test_decode_quant_large_values(kind):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-def test_decode_quant_llama_workload_sampled(kind):
+def test_decode_quant_llama_workload(kind):
+    # every sequence and head of the Llama-shaped workload
     st, vals = W.make_workload(1, seed=0)
     ref, gpu = build_caches(kind, st, vals)
-    ids = [0, 7, 21, 40, 63]
-    got, want = decode_both(kind, st, vals, ref, gpu, seq_ids=ids)
+    got, want = decode_both(kind, st, vals, ref, gpu)
     assert_close(got, want, "llama workload")
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("num_ctas", [0, 7])
+def test_decode_quant_many_short_sequences(kind, num_ctas):
+    # 300 short ragged contexts: many units per CTA, most of them whole
+    rng = np.random.default_rng(57)
+    lens = rng.integers(1, 200, size=300).tolist()
+    lens[255], lens[256] = 129, 1
+    spec = W.WorkloadSpec("q", len(lens), 32, 8, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=57, lengths=lens)
+    ref, gpu = build_caches(kind, st, vals)
+    got, want = decode_both(kind, st, vals, ref, gpu, num_ctas=num_ctas)
+    assert_close(got, want, f"{len(lens)} sequences, ctas={num_ctas}")
 
 
 @pytest.mark.parametrize("kind", KINDS)
