@@ -585,11 +585,15 @@ class PoolsPrefix(Pools16):
 
 
 # ------------------------------------------------------------------ other workloads
-# (workload, block size override, largest suffix override, prefix-aware decode)
-SWEEP = [(0, None, None, False), (2, None, None, False), (3, None, None, False),
-         (3, None, None, True), (3, None, 500, False), (3, None, 500, True),
-         (4, 8, None, False), (4, 16, None, False), (4, 32, None, False)]
+# (workload, block size override, largest suffix override, cache / decode):
+# None the 16-bit paged cache and its plain decode, "prefix" the prefix-aware
+# decode, "fp8_e4m3" / "int8" the 8-bit cache, "flat" flat spans
+SWEEP = [(0, None, None, None), (2, None, None, None), (3, None, None, None),
+         (3, None, None, "prefix"), (3, None, 500, None), (3, None, 500, "prefix"),
+         (4, 8, None, None), (4, 16, None, None), (4, 32, None, None),
+         (1, None, None, "fp8_e4m3"), (1, None, None, "int8"), (1, None, None, "flat")]
 TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
+QUANT = ("fp8_e4m3", "int8")
 
 
 def workload_sweep(args, dev, peak):
@@ -598,14 +602,16 @@ def workload_sweep(args, dev, peak):
     `steps` back-to-back steps, the decode kernel alone (CUDA events around
     each launch), algorithmic and unique bytes, the fraction of the measured
     peak, and the max-abs error of the whole output against the fp64 oracle
-    (every sequence, every head)."""
+    (every sequence, every head). The Llama-shaped step also runs over the
+    8-bit caches and over flat spans."""
     from oracle import oracle
     from paged_kv_cache_47_gb300 import binding
 
     from dataclasses import replace
     steps = max(args.steps, 10)
     res = []
-    for idx, B, suffix_hi, prefix_aware in SWEEP:
+    for idx, B, suffix_hi, mode in SWEEP:
+        prefix_aware, quant = mode == "prefix", mode if mode in QUANT else None
         spec = W.SPECS[idx] if B is None else W.SPECS[idx].with_block_size(B)
         if suffix_hi is not None:
             spec = replace(spec, suffix_hi=suffix_hi)
@@ -622,8 +628,13 @@ def workload_sweep(args, dev, peak):
             # but one holder: the group shares the blocks before it
             pools = PoolsPrefix(vals["k_pool"], vals["v_pool"],
                                 spec.shared_prefix // spec.block_size - (1 if cow is not None else 0))
+        elif quant:
+            pools = PoolsQ.fill(quant, st, vals, dev)
+        elif mode == "flat":
+            pools = PoolsFlat.fill(st, vals, dev)
         else:
             pools = Pools16(vals["k_pool"], vals["v_pool"])
+        fused = isinstance(pools, Pools16) and pools.fused and not prefix_aware
         out = torch.empty(S, Hq, D, dtype=vals["q"].dtype, device=dev)
         ws = pools.workspace(Hq)
         # one cache copy: each step's append rewrites the same last row, so the
@@ -662,8 +673,8 @@ def workload_sweep(args, dev, peak):
         if binding.get_error() != 0:
             raise RuntimeError(f"device error word set on workload {spec.name}")
         dec_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
-        row_bytes = cache_row_bytes(spec, None)
-        decode_bytes, append_bytes = step_bytes(st, spec, row_bytes)
+        row_bytes = cache_row_bytes(spec, quant)
+        decode_bytes, append_bytes = step_bytes(st, spec, row_bytes, fused=fused)
         total = decode_bytes + append_bytes
         if cow is not None:
             total += cow.shape[0] * 2 * 2 * spec.num_kv_heads * spec.block_size * row_bytes
@@ -671,11 +682,20 @@ def workload_sweep(args, dev, peak):
             + unique_kv_bytes(st, spec, row_bytes)
         # the oracle on the same inputs: copy-on-write, append, decode of all sequences
         t0 = time.perf_counter()
-        if cow is not None:
-            oracle.block_copy(cow, h["k_pool"], h["v_pool"])
-        oracle.append(h["k_new"], h["v_new"], st.slot_mapping, h["k_pool"], h["v_pool"])
-        ref = oracle.decode(h["q"], h["k_pool"], h["v_pool"], st.block_tables, st.context_lens,
-                            scale)
+        if quant:
+            # the oracle quantizes every context row (the appended one
+            # included) itself, then decodes over its own codes and scales
+            hq = host_inputs_from_generator(st, args.seed, dev, quant)
+            ref = oracle.decode_quant(quant, hq["q"], hq["k_codes"], hq["v_codes"],
+                                      hq["k_scales"], hq["v_scales"], st.block_tables,
+                                      st.context_lens, scale)
+            del hq
+        else:
+            if cow is not None:
+                oracle.block_copy(cow, h["k_pool"], h["v_pool"])
+            oracle.append(h["k_new"], h["v_new"], st.slot_mapping, h["k_pool"], h["v_pool"])
+            ref = oracle.decode(h["q"], h["k_pool"], h["v_pool"], st.block_tables,
+                                st.context_lens, scale)
         oracle_s = time.perf_counter() - t0
         got = out.double().cpu().numpy()
         err = float(abs(got - ref).max()) if got.size else 0.0
@@ -683,12 +703,19 @@ def workload_sweep(args, dev, peak):
             "workload": spec.name + (f" (suffix U[{spec.suffix_lo},{spec.suffix_hi}])"
                                      if suffix_hi is not None else ""),
             "decode": "prefix-aware (pkv_decode_attention_prefix)" if prefix_aware else
-                      ("pkv_append_decode_attention" if pools.fused else "plain"),
-            "block_size": spec.block_size, "kv_dtype": spec.dtype,
+                      (f"8-bit cache: pkv_append_quant_ex + pkv_decode_attention_quant"
+                       + (" (tcgen05 kind::f8f6f4)" if quant == "fp8_e4m3" else " (mma.sync)")
+                       if quant else
+                       "flat spans: pkv_flat_append + pkv_decode_attention_flat"
+                       if mode == "flat" else
+                       "pkv_append_decode_attention" if fused else "plain"),
+            "block_size": spec.block_size,
+            "kv_dtype": f"{quant} codes + fp32 row scales" if quant else spec.dtype,
             "num_seqs": S, "q_heads": Hq, "kv_heads": spec.num_kv_heads,
             "context_tokens": int(st.context_lens.sum()),
             "step_us": round(step_ms * 1000, 2),
             "step_gbs": round(total / (step_ms / 1000) / 1e9, 1),
+            "step_frac_of_measured": round(total / (step_ms / 1000) / 1e9 / peak, 4),
             "decode_us": round(dec_ms * 1000, 2),
             "algorithmic_bytes": decode_bytes, "unique_bytes": uniq,
             "decode_frac_of_measured": round(uniq / (dec_ms / 1000) / 1e9 / peak, 4),
