@@ -576,41 +576,6 @@ def append_decode_attention_quant(q, k_new, v_new, cache: QuantCache, block_tabl
     return out
 
 
-class PreparedAppendDecodeQuant:
-    """pkv_append_decode_attention_quant with its arguments marshalled once (see
-    PreparedDecode)."""
-
-    def __init__(self, q, k_new, v_new, cache: QuantCache, block_tables, context_lens,
-                 scale: float, out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
-                 num_ctas: int = 0, tables_ready: bool = False, pending_tail: int = 0):
-        for t in (q, k_new, v_new, block_tables, context_lens, out):
-            if not t.is_contiguous():
-                raise ValueError("prepared decode needs contiguous tensors")
-        assert q.dtype == k_new.dtype == v_new.dtype == cache.act_dtype
-        S, Hq, D = q.shape
-        if workspace is None:
-            workspace = alloc_quant_workspace(cache, Hq, num_ctas)
-        self._keep = (q, k_new, v_new, cache, block_tables, context_lens, out, workspace)
-        self._opts = DecodeOptions()
-        self._opts.num_ctas = num_ctas
-        self._opts.tables_ready = int(tables_ready)
-        self._opts.pending_tail = int(pending_tail)
-        self._args = (ctypes.byref(cache.desc), q.data_ptr(), S, Hq, k_new.data_ptr(),
-                      v_new.data_ptr(), *cache.pointers(), block_tables.data_ptr(),
-                      block_tables.shape[1], context_lens.data_ptr(), float(scale),
-                      out.data_ptr(), DTYPE_CODE[out.dtype], workspace.data_ptr(),
-                      workspace.numel())
-        self._fn = lib().pkv_append_decode_attention_quant
-        self.out = out
-
-    def __call__(self, stream, timing_events: Optional[Sequence] = None) -> None:
-        opts = self._opts
-        for i in range(2):
-            ev = timing_events[i] if timing_events is not None else None
-            opts.timing_events[i] = None if ev is None else ev.cuda_event
-        _check(self._fn(*self._args, _stream(stream), ctypes.byref(opts)))
-
-
 class PreparedAppendQuant:
     """pkv_append_quant with its arguments marshalled once (see PreparedDecode)."""
 
