@@ -315,29 +315,29 @@ def _clone_cache(c):
                                                ("int8", "bf16", 32, 8, 16)])
 @pytest.mark.parametrize("num_ctas", [0, 5, 300])
 def test_append_decode_attention_quant(kind, dtype, Hq, Hk, B, num_ctas):
-    # one step: the newest rows quantized into their slots (one launch for E4M3
-    # with up to 8 heads per kv head, append + decode otherwise). Pools bit-exact
-    # and output bitwise equal to pkv_append_quant + pkv_decode_attention_quant,
-    # and within tolerance of the oracle's append and decode
+    # one step: the newest rows quantized into their slots (found from the
+    # tables and lengths), then the decode. Pools bit-exact and output bitwise
+    # equal to pkv_append_quant + pkv_decode_attention_quant, and within
+    # tolerance of the oracle's append and decode
     st, vals, ref, base = _base_and_step(kind, dtype, Hq, Hk, B, RAGGED, seed=61)
     scale = 1.0 / math.sqrt(128)
     q, kn, vn = vals["q"].cuda(), vals["k_new"].cuda(), vals["v_new"].cuda()
     tab, lens = st.block_tables.cuda(), st.context_lens.cuda()
-    sep, fused = _clone_cache(base), _clone_cache(base)
+    sep, one = _clone_cache(base), _clone_cache(base)
     binding.append_quant(kn, vn, st.slot_mapping.cuda(), sep)
     want_gpu = binding.decode_attention_quant(q, sep, tab, lens, scale, out_dtype=torch.float32,
                                               num_ctas=num_ctas)
-    got = binding.append_decode_attention_quant(q, kn, vn, fused, tab, lens, scale,
+    got = binding.append_decode_attention_quant(q, kn, vn, one, tab, lens, scale,
                                                 out_dtype=torch.float32, num_ctas=num_ctas)
     torch.cuda.synchronize()
     assert binding.get_error() == 0
-    assert torch.equal(fused.k_codes.cpu(), sep.k_codes.cpu())
-    assert torch.equal(fused.v_codes.cpu(), sep.v_codes.cpu())
-    assert torch.equal(fused.k_scales.cpu().view(torch.int32), sep.k_scales.cpu().view(torch.int32))
-    assert torch.equal(fused.v_scales.cpu().view(torch.int32), sep.v_scales.cpu().view(torch.int32))
+    assert torch.equal(one.k_codes.cpu(), sep.k_codes.cpu())
+    assert torch.equal(one.v_codes.cpu(), sep.v_codes.cpu())
+    assert torch.equal(one.k_scales.cpu().view(torch.int32), sep.k_scales.cpu().view(torch.int32))
+    assert torch.equal(one.v_scales.cpu().view(torch.int32), sep.v_scales.cpu().view(torch.int32))
     assert torch.equal(got.cpu(), want_gpu.cpu())
     oracle.append_quant(kind, vals["k_new"], vals["v_new"], st.slot_mapping, *ref)
-    assert_same_cache(ref, fused)
+    assert_same_cache(ref, one)
     want = oracle.decode_quant(kind, vals["q"], *ref, st.block_tables, st.context_lens, scale)
     assert_close(got.double().cpu().numpy(), want, f"{kind} {dtype} {Hq}/{Hk} B{B}")
 
