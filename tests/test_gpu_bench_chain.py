@@ -10,7 +10,11 @@ with bench.py's own classes, runs it for several steps, and compares every
 output element of every cache copy, and every byte of each copy's pools, with
 the oracle: paging and launch overlap move bytes, not results ("PagedAttention
 — Math + Memory Model", sections "The operating-system analogy" and
-"PagedAttention: blocks and the block table").
+"PagedAttention: blocks and the block table"). The same holds for the
+8-bit steps bench.py times with --kv-quant (the quantizing append reading and
+quantizing its rows before its wait, the decode reading tables and lengths
+early): codes and scales bit for bit, outputs within tolerance of the
+oracle's own quantized cache.
 """
 import math
 
@@ -73,3 +77,45 @@ def test_bench_chain_matches_oracle(steps):
         got = o.double().cpu().numpy()
         err = float(abs(got - ref).max())
         assert err <= 2e-3, f"max abs err {err:.3e}"
+
+
+@pytest.mark.parametrize("kind", ["fp8_e4m3", "int8"])
+def test_bench_chain_8bit_matches_oracle(kind, steps=7):
+    dev = torch.device("cuda")
+    spec = W.SPECS[bench.WORKLOAD_INDEX]
+    st = W.make_structure(spec, 0)
+    vals = W.make_values(st, 0, device=dev)
+    scale = 1.0 / math.sqrt(spec.head_dim)
+    tables, lens = st.block_tables.to(dev), st.context_lens.to(dev)
+    slots = st.slot_mapping.to(dev)
+    S, Hq, D = vals["q"].shape
+    base = bench.PoolsQ.fill(kind, st, vals, dev)
+    copies = [base] + [base.clone() for _ in range(2)]
+    outs = [torch.full((S, Hq, D), float("nan"), dtype=vals["q"].dtype, device=dev)
+            for _ in copies]
+    wss = [c.workspace(Hq) for c in copies]
+    calls = [c.prepared(vals["q"], vals["k_new"], vals["v_new"], slots, tables, lens, scale, o,
+                        w)
+             for c, o, w in zip(copies, outs, wss)]
+    stream = torch.cuda.current_stream()
+    binding.get_error()
+    for i in range(steps):
+        app, dec = calls[i % len(calls)]
+        app(stream)
+        dec(stream)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+
+    # the oracle quantizes every context row (the appended ones included) itself
+    h = bench.host_inputs_from_generator(st, 0, dev, kind)
+    ref = oracle.decode_quant(kind, h["q"], h["k_codes"], h["v_codes"], h["k_scales"],
+                              h["v_scales"], st.block_tables, st.context_lens, scale)
+    for c, o in zip(copies, outs):
+        cache = c.cache
+        assert torch.equal(cache.k_codes.cpu(), h["k_codes"])
+        assert torch.equal(cache.v_codes.cpu(), h["v_codes"])
+        assert torch.equal(cache.k_scales.cpu().view(torch.int32), h["k_scales"].view(torch.int32))
+        assert torch.equal(cache.v_scales.cpu().view(torch.int32), h["v_scales"].view(torch.int32))
+        got = o.double().cpu().numpy()
+        err = float(abs(got - ref).max())
+        assert err <= 2e-3, f"{kind}: max abs err {err:.3e}"
