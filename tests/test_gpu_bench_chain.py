@@ -119,3 +119,41 @@ def test_bench_chain_8bit_matches_oracle(kind, steps=7):
         got = o.double().cpu().numpy()
         err = float(abs(got - ref).max())
         assert err <= 2e-3, f"{kind}: max abs err {err:.3e}"
+
+
+def test_bench_chain_flat_matches_oracle(steps=7):
+    # bench.py --flat: three flat caches (one virtual span per sequence), the
+    # flat append then the flat decode, with the decode reading lengths early
+    # and gathering every row but the appended one early
+    dev = torch.device("cuda")
+    spec = W.SPECS[bench.WORKLOAD_INDEX]
+    st = W.make_structure(spec, 0)
+    vals = W.make_values(st, 0, device=dev)
+    host = {k: v.cpu() for k, v in vals.items()}
+    scale = 1.0 / math.sqrt(spec.head_dim)
+    tables, lens = st.block_tables.to(dev), st.context_lens.to(dev)
+    slots = st.slot_mapping.to(dev)
+    S, Hq, D = vals["q"].shape
+    copies = [bench.PoolsFlat.fill(st, vals, dev) for _ in range(3)]
+    outs = [torch.full((S, Hq, D), float("nan"), dtype=vals["q"].dtype, device=dev)
+            for _ in copies]
+    wss = [c.workspace(Hq) for c in copies]
+    calls = [c.prepared(vals["q"], vals["k_new"], vals["v_new"], slots, tables, lens, scale, o,
+                        w, pending_tail=1)
+             for c, o, w in zip(copies, outs, wss)]
+    stream = torch.cuda.current_stream()
+    binding.get_error()
+    for i in range(steps):
+        app, dec = calls[i % len(calls)]
+        app(stream)
+        dec(stream)
+    torch.cuda.synchronize()
+    assert binding.get_error() == 0
+
+    oracle.append(host["k_new"], host["v_new"], st.slot_mapping, host["k_pool"], host["v_pool"])
+    ref = oracle.decode(host["q"], host["k_pool"], host["v_pool"], st.block_tables,
+                        st.context_lens, scale)
+    for o in outs:
+        got = o.double().cpu().numpy()
+        err = float(abs(got - ref).max())
+        assert err <= 2e-3, f"flat: max abs err {err:.3e}"
