@@ -591,7 +591,8 @@ class PoolsPrefix(Pools16):
 SWEEP = [(0, None, None, None), (2, None, None, None), (3, None, None, None),
          (3, None, None, "prefix"), (3, None, 500, None), (3, None, 500, "prefix"),
          (4, 8, None, None), (4, 16, None, None), (4, 32, None, None),
-         (1, None, None, "fp8_e4m3"), (1, None, None, "int8"), (1, None, None, "flat")]
+         (1, None, None, "fp8_e4m3"), (1, None, None, "int8"), (1, None, None, "flat"),
+         (4, 16, None, "fp8_e4m3"), (4, 16, None, "int8")]
 TOL = {"f32": 1e-5, "f16": 2e-3, "bf16": 2e-3}
 QUANT = ("fp8_e4m3", "int8")
 
@@ -603,7 +604,7 @@ def workload_sweep(args, dev, peak):
     each launch), algorithmic and unique bytes, the fraction of the measured
     peak, and the max-abs error of the whole output against the fp64 oracle
     (every sequence, every head). The Llama-shaped step also runs over the
-    8-bit caches and over flat spans."""
+    8-bit caches and over flat spans, the long-context one over the 8-bit caches."""
     from oracle import oracle
     from paged_kv_cache_47_gb300 import binding
 

@@ -506,10 +506,14 @@ struct Consumer<T, D, GMAX, true, QK> {
     float scale_log2;
     float sl2[NTN][2];  // 8-bit caches: score factor of this thread's score heads
     float sigma;        // 8-bit caches: the accumulator holds o / sigma
-    // int8 caches: kInt8Bias x sum_d q of this thread's score heads, and this
-    // thread's share of sum_t p' (the fp16 parts the PV product used) of its
-    // score heads, scaled with the accumulator
-    float qsb[NTN][2], ps[NTN][2];
+    // int8 caches: kInt8Bias x sum_d q of this thread's score heads, and
+    // kInt8Bias x sum_t p' over the warp's tokens of the last tile (the fp16
+    // parts its PV product used), which that product left in the
+    // accumulators of those heads. It comes off at the next tile's rescale
+    // (or the segment's end): left to pile up over a segment, the bias, far
+    // above the signal sum p' code, made the accumulators' rounding grow with
+    // the segment's length (9e-4 on outputs of ~0.006 over 34k tokens).
+    float qsb[NTN][2], pbias[NTN][2];
 
     __device__ __forceinline__ void reset() {
         sigma = 0.f;
@@ -519,7 +523,7 @@ struct Consumer<T, D, GMAX, true, QK> {
             for (int hh = 0; hh < 2; ++hh) {
                 m[nt][hh] = -CUDART_INF_F;
                 l[nt][hh] = 0.f;
-                ps[nt][hh] = 0.f;
+                pbias[nt][hh] = 0.f;
             }
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks)
@@ -733,12 +737,21 @@ struct Consumer<T, D, GMAX, true, QK> {
                 p[nt][2 + hh] = exp2f(sb - mn);
                 l[nt][hh] = l[nt][hh] * alpha + p[nt][hh] + p[nt][2 + hh];
                 const float ar = QK != 0 ? alpha * ratio : alpha;
+                if constexpr (QK == kQuantInt8) {
+                    // (acc - the last tile's bias) * ar, in one fma
+                    const float nb = -pbias[nt][hh] * ar;
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    acc[ks][nt][hh] *= ar;
-                    acc[ks][nt][2 + hh] *= ar;
+                    for (int ks = 0; ks < KS; ++ks) {
+                        acc[ks][nt][hh] = fmaf(acc[ks][nt][hh], ar, nb);
+                        acc[ks][nt][2 + hh] = fmaf(acc[ks][nt][2 + hh], ar, nb);
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        acc[ks][nt][hh] *= ar;
+                        acc[ks][nt][2 + hh] *= ar;
+                    }
                 }
-                if constexpr (QK == kQuantInt8) ps[nt][hh] *= ar;
                 if constexpr (QK != 0) {   // p' = p * s_v / vmax for the PV product
                     p[nt][hh] *= fvA;
                     p[nt][2 + hh] *= fvB;
@@ -748,6 +761,7 @@ struct Consumer<T, D, GMAX, true, QK> {
         // ---- P^T as the B operand: stage [token][head] hi/lo pairs, reload transposed
         __syncwarp();
         uint32_t bh[NTN][2], bl[NTN][2];
+        float psum[NTN][2];   // int8: this lane's share of sum_t p' per head
 #pragma unroll
         for (int nt = 0; nt < NTN; ++nt) {
             const uint32_t hi = pbuf + nt * 512, lo = hi + 256;
@@ -758,8 +772,8 @@ struct Consumer<T, D, GMAX, true, QK> {
             const uint32_t lA = Elem<MT>::pack2(p[nt][0] - r00, p[nt][1] - r01, d00, d01);
             const uint32_t lB = Elem<MT>::pack2(p[nt][2] - r10, p[nt][3] - r11, d10, d11);
             if constexpr (QK == kQuantInt8) {   // the p' values the product uses, per head
-                ps[nt][0] += (r00 + d00) + (r10 + d10);
-                ps[nt][1] += (r01 + d01) + (r11 + d11);
+                psum[nt][0] = (r00 + d00) + (r10 + d10);
+                psum[nt][1] = (r01 + d01) + (r11 + d11);
             }
             const uint32_t offA = (lane >> 2) * 16 + (lane & 3) * 4;
             const uint32_t offB = offA + 8 * 16;
@@ -797,6 +811,18 @@ struct Consumer<T, D, GMAX, true, QK> {
                         MmaOp<MT>::run(acc[mt][nt], a0, a1, a2, a3, bl[nt][0], bl[nt][1]);
                     }
                 }
+            if constexpr (QK == kQuantInt8) {
+                // this tile's bias: the eight lanes' shares of each head
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float b = psum[nt][hh];
+#pragma unroll
+                        for (int o = 4; o < 32; o <<= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+                        pbias[nt][hh] = kInt8Bias * b;
+                    }
+            }
         } else {
             const int tok = r0 + (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
@@ -831,19 +857,11 @@ struct Consumer<T, D, GMAX, true, QK> {
                 }
             }
             const float sg = QK != 0 ? sigma : 1.f;
-            // int8: kInt8Bias x sum_t p' of heads 2(lane%4) and + 1 (their
-            // eight lanes' shares) comes off every element of those heads
+            // int8: the last tile's bias of heads 2(lane%4) and + 1
             float b0 = 0.f, b1 = 0.f;
             if constexpr (QK == kQuantInt8) {
-                b0 = ps[nt][0];
-                b1 = ps[nt][1];
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    b0 += __shfl_xor_sync(0xffffffffu, b0, o);
-                    b1 += __shfl_xor_sync(0xffffffffu, b1, o);
-                }
-                b0 *= kInt8Bias;
-                b1 *= kInt8Bias;
+                b0 = pbias[nt][0];
+                b1 = pbias[nt][1];
             }
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {

@@ -192,6 +192,21 @@ def test_decode_quant_llama_workload(kind):
 
 
 @pytest.mark.parametrize("kind", KINDS)
+def test_decode_quant_long_single_segments(kind):
+    # one 131072-token context on 8 CTAs: each CTA runs one segment of about
+    # 1000 tiles, so any error that grows with the tiles accumulated in one
+    # segment shows (the int8 codes' bias in the PV accumulators); outputs are
+    # small here (~0.006), so the bound is tight in relative terms
+    spec = W.WorkloadSpec("q", 1, 32, 8, 128, 16, "bf16", 1.0)
+    st, vals = W.make_workload(spec, seed=58, lengths=[131072])
+    ref, gpu = build_caches(kind, st, vals)
+    got, want = decode_both(kind, st, vals, ref, gpu, num_ctas=8)
+    assert_close(got, want, "one 131072-token context, 8 CTAs")
+    rel = float(np.max(np.abs(got - want)) / np.max(np.abs(want)))
+    assert rel < 2e-2, f"max abs err / max |out| = {rel:.2e}"
+
+
+@pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("num_ctas", [0, 7])
 def test_decode_quant_many_short_sequences(kind, num_ctas):
     # 300 short ragged contexts: many units per CTA, most of them whole
