@@ -175,6 +175,20 @@ def test_long_context_gqa8_small(B):
     assert_close(got, ref, "bf16", f"B={B}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_long_single_segments(dtype):
+    # one 131072-token context on 8 CTAs: each CTA runs one segment of about
+    # 2000 tiles, so an error that grew with the tiles accumulated in one
+    # segment would show; outputs are small (~0.01), so the relative bound is
+    # the tight one
+    spec = spec_like(1, num_seqs=1, dtype=dtype)
+    st, vals = W.make_workload(spec, seed=9, lengths=[131072])
+    got, ref, _ = run_step(st, vals, out_dtype=torch.float32, num_ctas=8, check_pools=False)
+    assert_close(got, ref, dtype, "one 131072-token context, 8 CTAs")
+    rel = float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+    assert rel < 2e-2, f"max abs err / max |out| = {rel:.2e}"
+
+
 def test_zero_length_sequences_give_zeros():
     spec = W.WorkloadSpec("t", 4, 8, 2, 64, 16, "bf16", 1.0)
     st, vals = W.make_workload(spec, seed=7, lengths=[0, 33, 0, 90])
