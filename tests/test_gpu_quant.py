@@ -144,7 +144,12 @@ def test_append_quant_ties_and_zero_rows(kind):
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("dtype,Hq,Hk,B", [("bf16", 32, 8, 16), ("f16", 8, 8, 16),
                                            ("bf16", 64, 8, 8), ("f16", 40, 2, 32),
-                                           ("bf16", 16, 8, 16)])
+                                           ("bf16", 16, 8, 16),
+                                           # 3, 5 and 6 q heads a kv head: the E4M3
+                                           # tensor-core variants' partial units (a
+                                           # second PV product; scores on 32 columns)
+                                           ("bf16", 24, 8, 16), ("f16", 40, 8, 16),
+                                           ("bf16", 48, 8, 16)])
 def test_decode_quant_matches_oracle(kind, dtype, Hq, Hk, B):
     spec = W.WorkloadSpec("q", len(RAGGED), Hq, Hk, 128, B, dtype, 1.0)
     st, vals = W.make_workload(spec, seed=52, lengths=RAGGED)
