@@ -451,6 +451,7 @@ pkv_status pkv_append_quant_ex(const pkv_qcache_desc *cache, const void *k_new,
  * pkv_append_quant) and written to position context_lens[s] - 1 of its table
  * row, and the decode attention (pkv_decode_attention_quant) runs over the
  * context including it: the quantizing append, then the decode, on `stream`.
+ * A sequence with context_lens[s] == 0 has no new row (its output is zeros).
  * The new rows are written after the preceding kernel on `stream` has
  * completed. Other arguments, errors and workspace: as
  * pkv_decode_attention_quant (and pkv_append_quant for the rows).
